@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the ternary (TQ2_0-style) matvec on GB300.
+
+Workload (one "step"): the whole MiniCPM4-8B-shaped ternary stack streamed
+once at M=1 -- 32 layers x {q,o: 4096->4096; k,v: 4096->256; gate,up:
+4096->16384; down: 16384->4096} = 224 linears, 7.58e9 weights, 1.96 GB of
+packed codes + scales per step (more than 15x the 129 MB L2, so every step
+reads its weights from HBM).  Synthetic seeded inputs (codes P(1)=1/2,
+P(0)=P(2)=1/4; d ~ U[0.005,0.05] fp16; x ~ N(0,1) fp16), packed on the GPU
+with tq2_pack.  The 224 tq2_matvec calls are captured once in a CUDA graph
+(programmatic dependent launches between them) and replayed.
+
+Metric: HBM GB/s of algorithmic bytes (N*K/4 + 2*N*K/256 + 2*M*K + 4*M*N per
+linear) and the decode-equivalent tok/s (one step = one token).
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (the reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYER = [("q", 4096, 4096), ("k", 256, 4096), ("v", 256, 4096), ("o", 4096, 4096),
+         ("gate", 16384, 4096), ("up", 16384, 4096), ("down", 4096, 16384)]
+N_LAYERS = 32
+SEED = 1
+METRIC = "ternary matvec HBM GB/s (% of GB300 peak) and 8B-stack decode-equivalent tok/s"
+WORKLOAD = ("MiniCPM4-8B ternary stack: 224 linears (32 x q,k,v,o,gate,up,down), M=1, "
+            "fp16 x, fp32 y, TQ2_0 2-bit codes + fp16 per-256 scales")
+
+
+def linear_bytes(M, N, K, ybytes=4):
+    return N * K // 4 + 2 * N * (K // 256) + 2 * M * K + ybytes * M * N
+
+
+def stack_linears():
+    return [(L, *LAYER[L % 7]) for L in range(N_LAYERS * 7)]
+
+
+STACK_BYTES = sum(linear_bytes(1, N, K) for _, _, N, K in stack_linears())
+
+
+def _peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy, burst)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the GPU is loaded."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index_or_uuid):
+        self.ident = str(device_index_or_uuid)
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def build_stack(torch, tq2, syn, dev, with_prologue_scales=True):
+    """Generate and pack the 224 linears on the device (seeded)."""
+    lin = stack_linears()
+    qs, ds = [], []
+    x_off, y_off = [], []
+    xo = yo = 0
+    for L, name, N, K in lin:
+        bits = torch.from_numpy(syn.code_bits(SEED, syn.tensor_id(L, syn.SLOT_CODE_BITS),
+                                              N * K // 4)).to(dev)
+        codes = syn.codes_from_bits_torch(bits, N, K)
+        del bits
+        qs.append(tq2.pack(codes))
+        del codes
+        ds.append(torch.from_numpy(syn.scales(SEED, N, K // 256, linear=L)).to(dev))
+        x_off.append(xo)
+        y_off.append(yo)
+        xo += K
+        yo += N
+    x_host = torch.empty(xo, dtype=torch.float16).pin_memory()
+    import numpy as np
+    xh = x_host.numpy()
+    for (L, name, N, K), o in zip(lin, x_off):
+        xh[o:o + K] = syn.activations(SEED, 1, K, linear=L)[0]
+    X = x_host.to(dev)
+    Y = torch.zeros(yo, dtype=torch.float32, device=dev)
+    y_host = torch.empty(yo, dtype=torch.float32).pin_memory()
+    scales = [syn.act_scale(SEED, linear=L) for L, *_ in lin] if with_prologue_scales else None
+    torch.cuda.synchronize()
+    return dict(lin=lin, qs=qs, d=ds, x_off=x_off, y_off=y_off, X=X, Y=Y, x_host=x_host,
+                y_host=y_host, scales=scales)
+
+
+def capture(torch, tq2, st, calls, stream):
+    """calls: list of (x view, qs, d, y view, act_scale, impl) -> CUDA graph."""
+    with torch.cuda.stream(stream):
+        for x, qs, d, y, s, impl in calls:  # eager warm-up (kernel attributes, module load)
+            tq2.matvec(x, qs, d, y=y, act_scale=s, impl=impl)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for x, qs, d, y, s, impl in calls:
+                tq2.matvec(x, qs, d, y=y, act_scale=s, impl=impl)
+    stream.synchronize()
+    return g
+
+
+def stack_calls(st, prologue=False, impl=0):
+    calls = []
+    for i, (L, name, N, K) in enumerate(st["lin"]):
+        x = st["X"][st["x_off"][i]:st["x_off"][i] + K].view(1, K)
+        y = st["Y"][st["y_off"][i]:st["y_off"][i] + N].view(1, N)
+        calls.append((x, st["qs"][i], st["d"][i], y, st["scales"][i] if prologue else 0.0, impl))
+    return calls
+
+
+def time_graph(torch, g, stream, steps, warmup, barrier=None):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per replay
+
+
+SHAPE_GROUPS = {"qo_4096x4096": ("q", "o"), "kv_256x4096": ("k", "v"),
+                "gateup_16384x4096": ("gate", "up"), "down_4096x16384": ("down",)}
+
+
+def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None):
+    """Back-to-back calls of one shape over the stack's distinct tensors
+    (q/o: 64 tensors, 278 MB; k/v: 64, 18 MB -- L2-resident; gate/up: 64,
+    1.1 GB; down: 32, 555 MB)."""
+    out = {}
+    dev = st["X"].device
+    for gname, names in SHAPE_GROUPS.items():
+        if groups is not None and gname not in groups:
+            continue
+        idx = [i for i, (L, n, N, K) in enumerate(st["lin"]) if n in names]
+        N, K = st["lin"][idx[0]][2], st["lin"][idx[0]][3]
+        for M in M_list:
+            import tq2_synth as syn
+            x = torch.from_numpy(syn.activations(SEED + 7, M, K, linear=0)).to(dev)
+            ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in idx]
+            calls = [(x, st["qs"][i], st["d"][i], y, 0.0, impl) for i, y in zip(idx, ys)]
+            g = capture(torch, tq2, st, calls, stream)
+            one = time_graph(torch, g, stream, 2, 1)
+            reps = max(3, int(0.3 / max(one * 1e-3, 1e-6)))  # ~0.3 s of replays
+            ms = time_graph(torch, g, stream, reps, 3)
+            nbytes = len(idx) * linear_bytes(M, N, K)
+            out[(gname, M)] = dict(us_per_call=1e3 * ms / len(idx),
+                                   gbs=nbytes / (ms * 1e-3) / 1e9,
+                                   distinct_tensors=len(idx),
+                                   distinct_bytes=nbytes)
+            del g, ys
+    return out
+
+
+def cpu_baseline_oracle(budget_s=10.0):
+    """The CPU oracle (fp64, one thread, as it stands) on layer 0 of the stack."""
+    import numpy as np
+    import oracle
+    import tq2_synth as syn
+    done_bytes, t_total, n_lin = 0, 0.0, 0
+    for L, name, N, K in stack_linears()[:7]:
+        codes = syn.codes(SEED, N, K, linear=L)
+        qs, _ = oracle.pack(codes)
+        d = syn.scales(SEED, N, K // 256, linear=L)
+        x = syn.activations(SEED, 1, K, linear=L)
+        t0 = time.perf_counter()
+        oracle.matvec(x, qs, d, K)
+        t_total += time.perf_counter() - t0
+        done_bytes += linear_bytes(1, N, K)
+        n_lin += 1
+        if t_total > budget_s:
+            break
+    return dict(value=done_bytes / t_total / 1e9, unit="GB/s", cores=1, kind="oracle",
+                sample=f"layer 0 of the stack: {n_lin} linears, {done_bytes} algorithmic bytes, "
+                       f"plain C fp64 oracle, 1 thread, {t_total:.2f} s",
+                tok_s=1.0 / (t_total * STACK_BYTES / done_bytes))
+
+
+def read_profile_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source (sha256 match); else None."""
+    import hashlib
+    src = os.path.join(ROOT, "quantized_gemv_tq2_gb300", "csrc", "tq2_matvec_mma.cu")
+    prof = os.path.join(ROOT, "profiles", "tq2_matvec_mma_stack_m1.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        vals = {}
+        for line in open(prof):
+            if ":" in line and line.strip().startswith("- `"):
+                k, v = line.strip()[3:].split("`:", 1)
+                vals[k.strip()] = v.strip().strip("`")
+        if vals.get("kernel_source_sha256") != sha:
+            return None
+        return float(vals["traffic_bytes_per_launch_avg"])
+    except Exception:
+        return None
+
+
+def run_gpu(args):
+    import torch
+    import quantized_gemv_tq2_gb300 as tq2
+    import tq2_synth as syn
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        barrier = dist.barrier
+    tq2.load()
+
+    st = build_stack(torch, tq2, syn, dev)
+    stream = torch.cuda.Stream(device=dev)
+    g = capture(torch, tq2, st, stack_calls(st), stream)
+    launches_per_step = len(st["lin"])
+
+    # clocks: soak ~1 s under the same load, then the timed region, sampled throughout
+    props = torch.cuda.get_device_properties(dev)
+    ident = getattr(props, "uuid", None)
+    ident = f"GPU-{ident}" if ident is not None and not str(ident).startswith("GPU-") else (ident or local)
+    sampler = ClockSampler(ident)
+    sampler.start()
+    soak = time_graph(torch, g, stream, 1, 0)
+    time_graph(torch, g, stream, max(1, int(1.0 / max(soak * 1e-3, 1e-6))), 0)
+    ms = time_graph(torch, g, stream, args.steps, args.warmup, barrier)
+    clocks = sampler.stop()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # e2e: pinned host x -> device, the step, device y -> pinned host, every step
+    e2e_steps = max(3, min(args.steps, 300))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            st["X"].copy_(st["x_host"], non_blocking=True)
+            g.replay()
+            st["y_host"].copy_(st["Y"], non_blocking=True)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            st["X"].copy_(st["x_host"], non_blocking=True)
+            g.replay()
+            st["y_host"].copy_(st["Y"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    extras = {}
+    if not args.quick and rank == 0:
+        gp = capture(torch, tq2, st, stack_calls(st, prologue=True), stream)
+        ms_p = time_graph(torch, gp, stream, max(3, min(args.steps, 2000)), 5)
+        extras["stack_with_prologue"] = dict(ms_per_step=ms_p, gbs=STACK_BYTES / (ms_p * 1e-3) / 1e9,
+                                             tok_s=1e3 / ms_p)
+        del gp
+        shapes = shape_graphs(torch, tq2, st, stream, M_list=(1,))
+        extras["shapes_m1"] = {k[0]: v for k, v in shapes.items()}
+        simt = shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=2)
+        extras["shapes_m1_cuda_core_impl"] = {k[0]: v for k, v in simt.items()}
+        sweep = shape_graphs(torch, tq2, st, stream, M_list=(2, 4, 8, 16),
+                             groups=("gateup_16384x4096", "down_4096x16384"))
+        extras["m_sweep"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep.items()}
+
+    peak, peak_src = _peak()
+    value = world * STACK_BYTES / (ms * 1e-3) / 1e9
+    per_gpu = STACK_BYTES / (ms * 1e-3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded; MiniCPM4-8B shapes, no trained weights)",
+        "config": {
+            "workload": WORKLOAD,
+            "linears": len(st["lin"]),
+            "bytes_per_step": STACK_BYTES,
+            "M": 1,
+            "prologue": False,
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+            "l2": "inputs larger than L2 (1.96 GB of weights per step vs 129 MB L2)",
+            "launch": "CUDA graph of 224 tq2_matvec calls with programmatic dependent launch",
+        },
+        "tok_s": round(world * 1e3 / ms, 2),
+        "pct_of_peak": round(100 * per_gpu / peak, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "tq2::matvec_mma_kernel<1> (all 224 launches of a step)",
+            "achieved": round(per_gpu, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(per_gpu / peak, 4),
+            "traffic": read_profile_traffic(),
+            "peak_source": peak_src,
+            "per_launch": f"avg algorithmic bytes {STACK_BYTES / launches_per_step:.0f} / "
+                          f"avg launch time {1e3 * ms / launches_per_step:.3f} us",
+        },
+        "e2e": {
+            "value": round(world * STACK_BYTES / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 5),
+            "h2d_bytes_per_step": st["X"].numel() * 2,
+            "d2h_bytes_per_step": st["Y"].numel() * 4,
+            "path": "pinned host x -> device, graph replay of the tq2_matvec calls, y -> pinned host",
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if extras:
+        line["extras"] = extras
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_oracle(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The CPU oracle timed on the host cores, on this workload's metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    import tq2_synth as syn
+    # one step = the oracle's matvec of one k/v-shaped linear of the stack
+    # (4096 -> 256, 1.05e6 weights): a bounded sample of the stack workload
+    L, name, N, K = stack_linears()[1]
+    codes = syn.codes(SEED, N, K, linear=L)
+    qs, _ = oracle.pack(codes)
+    d = syn.scales(SEED, N, K // 256, linear=L)
+    x = syn.activations(SEED, 1, K, linear=L)
+    for _ in range(args.warmup):
+        oracle.matvec(x, qs, d, K)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matvec(x, qs, d, K)
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = linear_bytes(1, N, K)
+    v = nbytes / dt / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; MiniCPM4-8B shapes)",
+        "config": {"workload": WORKLOAD, "step_sample": "the k linear of layer 0 (4096->256)"},
+        "tok_s": round(v * 1e9 / STACK_BYTES, 4),
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one 4096->256 linear of the stack per step, plain C fp64 oracle, "
+                                   "1 thread"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only, no extras")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

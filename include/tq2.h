@@ -1,0 +1,164 @@
+/*
+ * tq2.h -- C ABI of the GB300-native ternary (TQ2_0-style) packed-weight
+ * matvec library (libtq2_gb300.so, built for sm_103a).
+ *
+ * The operation (BitCPM ternary page, "TQ2_0 (llama.cpp)" paragraph and the
+ * linear-factoring paragraph): along the reduction axis K, weights are split
+ * into 256-element blocks; each weight is a 2-bit code q in {0,1,2} standing
+ * for the value q-1 in {-1,0,+1}, and each block carries one fp16 scale d_b.
+ * For every activation row m and output row n
+ *
+ *     y[m][n] = sum_b d[n][b] * sum_{k in b} x'[m][k] * (q[n][k] - 1)
+ *
+ * where x' = x, or the static int8 fake-quant of x ("gemma4 wNa8o8 requires
+ * int8 activations" page): x' = s * clamp(rint(x * (1/s)), -128, 127).
+ *
+ * Data layout (all row-major, contiguous, caller-owned DEVICE memory):
+ *   codes  int8   [N, K]        one code per element (pack input / unpack output)
+ *   qs     uint8  [N, K/4]      code k of a row at bits 2*(k%4) of byte k/4
+ *   d      fp16   [N, K/256]    block scales, IEEE binary16 bit patterns
+ *   W      fp32 or fp16 [N, K]  a dequantised weight, W = d_b * (q - 1)
+ *   x      fp16   [M, K]        activations, M in 0..16
+ *   y      fp32 or fp16 [M, N]
+ * K must be a multiple of 256 (one block); N >= 0.
+ *
+ * Conventions
+ *   - Every call validates its arguments on the host and returns a status
+ *     synchronously, before anything is enqueued.  Work is enqueued on the
+ *     caller's stream and the call returns without synchronising; launch
+ *     failures come back as TQ2_ERR_CUDA.
+ *   - The library never allocates, frees or keeps device memory, and holds no
+ *     state between calls: calls are safe from several host threads and on
+ *     several streams.
+ *   - Data-dependent conditions (a code outside {0,1,2}, non-finite or
+ *     non-ternary W, a device wait that ran out) are reported by ORing flag
+ *     bits into an optional caller-owned device word `d_status` (may be NULL);
+ *     they never trap the GPU.  Nothing is truncated or clamped silently.
+ *   - Pointers must not alias each other (except as stated).
+ *   - Empty shapes (N == 0, M == 0, or K == 0 for pack/unpack/from_dense)
+ *     are valid no-ops; with K == 0 the matvec writes y = 0 (empty sums).
+ */
+#ifndef TQ2_H
+#define TQ2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TQ2_API __attribute__((visibility("default")))
+#else
+#define TQ2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *tq2_stream_t;
+
+typedef enum {
+    TQ2_OK = 0,
+    TQ2_ERR_NULL = 1,    /* a required pointer is NULL (with a non-empty shape) */
+    TQ2_ERR_SHAPE = 2,   /* K % 256 != 0, a negative size, M > 16, or size overflow */
+    TQ2_ERR_ALIGN = 3,   /* a pointer is not aligned as documented */
+    TQ2_ERR_DTYPE = 4,   /* unknown tq2_dtype value */
+    TQ2_ERR_ARG = 5,     /* act_scale negative / not finite, unknown impl, ... */
+    TQ2_ERR_CUDA = 6,    /* a CUDA runtime call or kernel launch failed */
+    TQ2_ERR_TIMEOUT = 7  /* reserved: reported through TQ2_FLAG_TIMEOUT */
+} tq2_status;
+
+typedef enum { TQ2_F32 = 0, TQ2_F16 = 1 } tq2_dtype;
+
+/* Flag bits ORed (asynchronously, by the kernels) into *d_status. */
+#define TQ2_FLAG_BAD_CODE 1u  /* pack: a code not in {0,1,2}; stored as code & 3 */
+#define TQ2_FLAG_NONFINITE 2u /* from_dense: NaN/Inf in W, or max|W| overflows fp16 */
+#define TQ2_FLAG_INEXACT 4u   /* from_dense: some W != d*(code-1) (lossy recovery) */
+#define TQ2_FLAG_TIMEOUT 8u   /* matvec: a bounded device wait ran out; y is invalid */
+
+/*
+ * tq2_pack -- codes int8 [N,K] -> qs uint8 [N,K/4].
+ * BitCPM ternary page, "TQ2_0 (llama.cpp)" paragraph: 2-bit codes {0,1,2}.
+ * Byte j of row n holds codes 4j..4j+3 at bits 0-1, 2-3, 4-5, 6-7.
+ * A code outside {0,1,2} is stored as (code & 3) and sets TQ2_FLAG_BAD_CODE.
+ * Alignment: none required.  The scale array is not touched: it is passed
+ * unchanged to tq2_matvec in its [N, K/256] layout.
+ */
+TQ2_API tq2_status tq2_pack(const int8_t *codes, int64_t N, int64_t K, uint8_t *qs,
+                    uint32_t *d_status, tq2_stream_t stream);
+
+/*
+ * tq2_unpack -- qs uint8 [N,K/4] -> codes int8 [N,K], every 2-bit field
+ * returned as stored (3 included).  Inverse of tq2_pack on valid codes.
+ */
+TQ2_API tq2_status tq2_unpack(const uint8_t *qs, int64_t N, int64_t K, int8_t *codes,
+                      tq2_stream_t stream);
+
+/*
+ * tq2_from_dense -- recover (qs, d) from a dequantised W [N,K]
+ * (BitCPM ternary page, recovery paragraph: d_block = max|W| in the block,
+ * exact because the nonzero magnitude is d; code = round(W/d) + 1).
+ * w_dtype: TQ2_F32 (float) or TQ2_F16 (binary16 bits).
+ * d is the fp16 round-to-nearest-even of the block's max|W|; codes are
+ * rint(W/d) (one fp32 division by the stored d, ties to even) clamped to
+ * [-1,1], plus 1.  An all-zero block gives d = 0 and codes 1; an element whose
+ * W/d is NaN gets code 1.  Flags: TQ2_FLAG_NONFINITE, TQ2_FLAG_INEXACT.
+ * For a true TQ2_0 W (W = d*(q-1), fp16 d, a nonzero code in the block) the
+ * recovery is bit-exact and sets no flag.
+ * Alignment: W 4-byte (fp32) or 2-byte (fp16) aligned.
+ */
+TQ2_API tq2_status tq2_from_dense(const void *W, tq2_dtype w_dtype, int64_t N, int64_t K,
+                          uint8_t *qs, uint16_t *d, uint32_t *d_status,
+                          tq2_stream_t stream);
+
+/*
+ * tq2_matvec -- y[M,N] = x'[M,K] (ternary W)^T, M in 0..16.
+ * BitCPM ternary page, linear-factoring paragraph:
+ *   sum_k x_k d_b (q_k - 1) = sum_b d_b sum_{k in b} x_k (q_k - 1).
+ * act_scale: 0 disables the prologue ("scale 0 = unquantized"); s > 0 applies
+ * the static int8 fake-quant of the gemma4 wNa8o8 page to x first, with the
+ * integer decision taken as rint(fp32(x) * fp32(1/s)) (ties to even, NaN -> 0)
+ * and the product kept as code * s (no fp16 re-rounding).
+ * y_dtype: TQ2_F32, or TQ2_F16 (round to nearest even from the fp32 sum).
+ * Accuracy: |y - exact| <= 1e-3 * sum_k |d_b x'_k| + 1e-6 per element; the
+ * result is bit-identical from run to run.
+ * Alignment: x and qs 16-byte aligned; d 2-byte; y 4-byte (fp32) / 2-byte.
+ * workspace / workspace_bytes: scratch for plans that need it; the current
+ * kernels need none (tq2_matvec_workspace_size returns 0) and ignore it.
+ * d_status: optional; TQ2_FLAG_TIMEOUT is set if a bounded device wait ran
+ * out (y is then invalid).
+ * Weights and scales are prefetched before the kernel waits on the previous
+ * kernel in the stream (programmatic dependent launch): qs and d must not be
+ * written by the kernel that immediately precedes this call on the stream
+ * when that kernel is itself a tq2_matvec.
+ */
+TQ2_API tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                      int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                      void *workspace, size_t workspace_bytes, uint32_t *d_status,
+                      tq2_stream_t stream);
+
+/* Bytes of workspace tq2_matvec needs for this shape (0 for every shape today). */
+TQ2_API size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * tq2_matvec_impl -- tq2_matvec with an explicit kernel choice, for
+ * measurement: impl 0 = automatic (what tq2_matvec runs), 1 = tensor-core
+ * (mma.sync on masked code words, TMA-staged weights), 2 = CUDA-core
+ * (fp32 FMA per code).  Impl 1 supports M <= 2 and returns TQ2_ERR_ARG for
+ * larger M.  Same contract as tq2_matvec otherwise.
+ */
+TQ2_API tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                           int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                           void *workspace, size_t workspace_bytes, uint32_t *d_status,
+                           tq2_stream_t stream, int impl);
+
+/* Static, human-readable name of a status. */
+TQ2_API const char *tq2_status_string(tq2_status status);
+
+/* Library version, 10000*major + 100*minor + patch. */
+TQ2_API int tq2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ2_H */

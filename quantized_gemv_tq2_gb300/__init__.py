@@ -1,0 +1,201 @@
+"""Python binding of the GB300-native ternary (TQ2_0-style) matvec library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``_lib/libtq2_gb300.so`` through its C ABI (``include/tq2.h``).
+PyTorch supplies device memory and streams; there is no CPU fallback, and
+the functions raise if the library is missing or a call fails.
+
+Functions take CUDA tensors and the current torch stream (or an explicit
+``stream``); outputs may be passed in or are allocated with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "TQ2Error", "lib", "load", "declared_symbols",
+    "pack", "unpack", "from_dense", "matvec", "matvec_workspace_size",
+    "status_string", "version",
+    "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT",
+    "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT",
+]
+
+F32, F16 = 0, 1
+FLAG_BAD_CODE, FLAG_NONFINITE, FLAG_INEXACT, FLAG_TIMEOUT = 1, 2, 4, 8
+IMPL_AUTO, IMPL_MMA, IMPL_SIMT = 0, 1, 2
+HEADER = os.path.join(os.path.dirname(_build.PKG), "include", "tq2.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TQ2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load the CUDA library (building it in-tree first if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"CUDA library not built: {path}")
+            _build.build()
+        L = ctypes.CDLL(path)
+        P, I64, I32, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                              ctypes.c_size_t)
+        L.tq2_pack.argtypes = [P, I64, I64, P, P, P]
+        L.tq2_unpack.argtypes = [P, I64, I64, P, P]
+        L.tq2_from_dense.argtypes = [P, I32, I64, I64, P, P, P, P]
+        L.tq2_matvec.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P]
+        L.tq2_matvec_impl.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P, I32]
+        L.tq2_matvec_workspace_size.argtypes = [I64, I64, I64]
+        L.tq2_matvec_workspace_size.restype = SZ
+        L.tq2_status_string.argtypes = [I32]
+        L.tq2_status_string.restype = ctypes.c_char_p
+        L.tq2_version.argtypes = []
+        for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
+                   "tq2_version"):
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared by include/tq2.h (the ABI this library exports)."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"TQ2_API\s+[\w\s\*]*?\b(tq2_\w+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load().tq2_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().tq2_version())
+
+
+# ------------------------------------------------------------------ helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise TQ2Error(status, where)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ------------------------------------------------------------------ ops
+def pack(codes, qs=None, status=None, stream=None):
+    """int8 codes [N,K] -> packed uint8 [N,K/4] (tq2_pack)."""
+    torch = _torch()
+    N, K = codes.shape
+    if codes.dtype != torch.int8:
+        raise TypeError("codes must be int8")
+    if qs is None:
+        qs = torch.empty((N, K // 4), dtype=torch.uint8, device=codes.device)
+    _need_cuda(codes, qs, status)
+    _check(load().tq2_pack(_ptr(codes), N, K, _ptr(qs), _ptr(status), _stream_ptr(stream)),
+           "tq2_pack")
+    return qs
+
+
+def unpack(qs, K, codes=None, stream=None):
+    """packed uint8 [N,K/4] -> int8 codes [N,K] (tq2_unpack)."""
+    torch = _torch()
+    N = qs.shape[0]
+    if codes is None:
+        codes = torch.empty((N, K), dtype=torch.int8, device=qs.device)
+    _need_cuda(codes, qs)
+    _check(load().tq2_unpack(_ptr(qs), N, K, _ptr(codes), _stream_ptr(stream)), "tq2_unpack")
+    return codes
+
+
+def from_dense(W, qs=None, d=None, status=None, stream=None):
+    """Dequantised W [N,K] (float32/float16) -> (qs uint8 [N,K/4], d float16 [N,K/256])."""
+    torch = _torch()
+    N, K = W.shape
+    if W.dtype == torch.float32:
+        wd = F32
+    elif W.dtype == torch.float16:
+        wd = F16
+    else:
+        raise TypeError("W must be float32 or float16")
+    if qs is None:
+        qs = torch.empty((N, K // 4), dtype=torch.uint8, device=W.device)
+    if d is None:
+        d = torch.empty((N, K // 256), dtype=torch.float16, device=W.device)
+    _need_cuda(W, qs, d, status)
+    _check(load().tq2_from_dense(_ptr(W), wd, N, K, _ptr(qs), _ptr(d), _ptr(status),
+                                 _stream_ptr(stream)), "tq2_from_dense")
+    return qs, d
+
+
+def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, status=None,
+           stream=None, impl: int = IMPL_AUTO, workspace=None):
+    """y [M,N] = ternary matvec of x [M,K] fp16 with packed qs/d (tq2_matvec)."""
+    torch = _torch()
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    M = x.shape[0]
+    N = qs.shape[0]
+    if K is None:
+        K = x.shape[1]
+    if x.dtype != torch.float16 or d.dtype != torch.float16 or qs.dtype != torch.uint8:
+        raise TypeError("x and d must be float16, qs uint8")
+    if y is None:
+        dt = torch.float32 if (y_dtype in (None, F32, torch.float32)) else torch.float16
+        y = torch.empty((M, N), dtype=dt, device=qs.device)
+    ycode = F32 if y.dtype == torch.float32 else F16
+    _need_cuda(x, qs, d, y, status)
+    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (ctypes.c_void_p(0), 0)
+    L = load()
+    if impl == IMPL_AUTO:
+        st = L.tq2_matvec(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
+                          ws_ptr, ws_bytes, _ptr(status), _stream_ptr(stream))
+    else:
+        st = L.tq2_matvec_impl(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode,
+                               float(act_scale), ws_ptr, ws_bytes, _ptr(status),
+                               _stream_ptr(stream), int(impl))
+    _check(st, "tq2_matvec")
+    return y
+
+
+def matvec_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load().tq2_matvec_workspace_size(M, N, K))

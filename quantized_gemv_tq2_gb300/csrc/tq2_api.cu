@@ -1,0 +1,192 @@
+// tq2_api.cu -- the C ABI (include/tq2.h): host-side validation, kernel
+// choice and launch on the caller's stream.  Every argument check happens
+// before any CUDA call, so invalid arguments return a status without touching
+// the device (these checks run even on a machine without a GPU).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "tq2_internal.cuh"
+
+namespace tq2 {
+
+static std::atomic<int> g_sm_count[64];
+
+int sm_count(int device)
+{
+    if (device < 0 || device >= 64) return 148;
+    int v = g_sm_count[device].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0)
+        v = 148;
+    g_sm_count[device].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+}  // namespace tq2
+
+namespace {
+
+constexpr int64_t kMaxElems = (int64_t)1 << 62;
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// N, K >= 0, K % 256 == 0, N*K representable.
+tq2_status check_nk(int64_t N, int64_t K)
+{
+    if (N < 0 || K < 0 || K % 256 != 0) return TQ2_ERR_SHAPE;
+    if (K > 0 && N > kMaxElems / K) return TQ2_ERR_SHAPE;
+    return TQ2_OK;
+}
+
+tq2_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return TQ2_OK;
+    cudaGetLastError();  // the error is returned; do not leave it sticky for the caller
+    return TQ2_ERR_CUDA;
+}
+
+tq2_status current_device(int *dev)
+{
+    return from_cuda(cudaGetDevice(dev));
+}
+
+tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                         int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                         uint32_t *d_status, tq2_stream_t stream, int impl)
+{
+    tq2_status st = check_nk(N, K);
+    if (st != TQ2_OK) return st;
+    if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
+    if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
+    if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 2) return TQ2_ERR_ARG;
+    if (impl == 1 && M > 2) return TQ2_ERR_ARG;
+    if (M == 0 || N == 0) return TQ2_OK;
+    if (y == nullptr) return TQ2_ERR_NULL;
+    if (K > 0 && (x == nullptr || qs == nullptr || d == nullptr)) return TQ2_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(d, 2)) return TQ2_ERR_ALIGN;
+    if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
+    if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t ybytes = (size_t)(M * N) * (y_dtype == TQ2_F32 ? 4 : 2);
+    if (K == 0)  // empty sums: y = 0 (all-zero bits are +0 in fp32 and fp16)
+        return from_cuda(cudaMemsetAsync(y, 0, ybytes, s));
+
+    int dev = 0;
+    if ((st = current_device(&dev)) != TQ2_OK) return st;
+    tq2::MatvecArgs a;
+    a.x = x;
+    a.qs = qs;
+    a.d = d;
+    a.y = y;
+    a.status = d_status;
+    a.N = N;
+    a.K = K;
+    a.M = (int)M;
+    a.y_f16 = (y_dtype == TQ2_F16);
+    a.act_scale = act_scale;
+    a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;  // IEEE-correct division
+    a.stream = s;
+
+    bool use_mma;
+    if (impl == 1) {
+        use_mma = true;
+        if (!tq2::mma_matvec_supported(a.M, N, K, dev)) return TQ2_ERR_ARG;
+    } else if (impl == 2) {
+        use_mma = false;
+    } else {
+        use_mma = tq2::mma_matvec_supported(a.M, N, K, dev);
+    }
+    cudaError_t e = use_mma ? tq2::launch_matvec_mma(a, dev) : tq2::launch_matvec_simt(a, dev);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+tq2_status tq2_pack(const int8_t *codes, int64_t N, int64_t K, uint8_t *qs, uint32_t *d_status,
+                    tq2_stream_t stream)
+{
+    tq2_status st = check_nk(N, K);
+    if (st != TQ2_OK) return st;
+    if (N == 0 || K == 0) return TQ2_OK;
+    if (codes == nullptr || qs == nullptr) return TQ2_ERR_NULL;
+    if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    return from_cuda(tq2::launch_pack(codes, N, K, qs, d_status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tq2_status tq2_unpack(const uint8_t *qs, int64_t N, int64_t K, int8_t *codes, tq2_stream_t stream)
+{
+    tq2_status st = check_nk(N, K);
+    if (st != TQ2_OK) return st;
+    if (N == 0 || K == 0) return TQ2_OK;
+    if (codes == nullptr || qs == nullptr) return TQ2_ERR_NULL;
+    return from_cuda(tq2::launch_unpack(qs, N, K, codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tq2_status tq2_from_dense(const void *W, tq2_dtype w_dtype, int64_t N, int64_t K, uint8_t *qs,
+                          uint16_t *d, uint32_t *d_status, tq2_stream_t stream)
+{
+    tq2_status st = check_nk(N, K);
+    if (st != TQ2_OK) return st;
+    if (w_dtype != TQ2_F32 && w_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
+    if (N == 0 || K == 0) return TQ2_OK;
+    if (W == nullptr || qs == nullptr || d == nullptr) return TQ2_ERR_NULL;
+    if (!aligned(W, w_dtype == TQ2_F32 ? 4 : 2) || !aligned(d, 2)) return TQ2_ERR_ALIGN;
+    if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    return from_cuda(tq2::launch_from_dense(W, w_dtype == TQ2_F16, N, K, qs, d, d_status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                      int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                      void *workspace, size_t workspace_bytes, uint32_t *d_status,
+                      tq2_stream_t stream)
+{
+    (void)workspace;
+    (void)workspace_bytes;
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, d_status, stream, 0);
+}
+
+tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                           int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                           void *workspace, size_t workspace_bytes, uint32_t *d_status,
+                           tq2_stream_t stream, int impl)
+{
+    (void)workspace;
+    (void)workspace_bytes;
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, d_status, stream, impl);
+}
+
+size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K)
+{
+    (void)M;
+    (void)N;
+    (void)K;
+    return 0;
+}
+
+const char *tq2_status_string(tq2_status status)
+{
+    switch (status) {
+    case TQ2_OK: return "TQ2_OK";
+    case TQ2_ERR_NULL: return "TQ2_ERR_NULL: a required pointer is NULL";
+    case TQ2_ERR_SHAPE: return "TQ2_ERR_SHAPE: invalid shape (K % 256, negative size, M > 16, overflow)";
+    case TQ2_ERR_ALIGN: return "TQ2_ERR_ALIGN: a pointer is not aligned as required";
+    case TQ2_ERR_DTYPE: return "TQ2_ERR_DTYPE: unknown dtype";
+    case TQ2_ERR_ARG: return "TQ2_ERR_ARG: invalid argument";
+    case TQ2_ERR_CUDA: return "TQ2_ERR_CUDA: a CUDA call or kernel launch failed";
+    case TQ2_ERR_TIMEOUT: return "TQ2_ERR_TIMEOUT: a bounded device wait ran out";
+    }
+    return "unknown tq2_status";
+}
+
+int tq2_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// tq2_internal.cuh -- declarations shared by the library's own translation
+// units (layout kernels, the two matvec kernels, the C-ABI shim).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tq2.h"
+
+namespace tq2 {
+
+// Everything a matvec launcher needs, already validated by the ABI shim.
+struct MatvecArgs {
+    const uint16_t *x;   // [M, K] fp16 bits
+    const uint8_t *qs;   // [N, K/4]
+    const uint16_t *d;   // [N, K/256] fp16 bits
+    void *y;             // [M, N] fp32 or fp16
+    uint32_t *status;    // optional device flag word
+    int64_t N, K;
+    int M;
+    int y_f16;           // 0: fp32 y, 1: fp16 y
+    float act_scale;     // 0: no prologue
+    float inv_scale;     // fp32(1/act_scale), correctly rounded on the host
+    cudaStream_t stream;
+};
+
+// Tensor-core path (mma.sync on masked code words, TMA bulk staging).
+// Returns false when the shape is outside what the kernel supports
+// (M > 2 or shared memory would not fit); nothing is launched then.
+bool mma_matvec_supported(int M, int64_t N, int64_t K, int device);
+cudaError_t launch_matvec_mma(const MatvecArgs &a, int device);
+
+// CUDA-core path (fp32 FMA per code), any M in 1..16.
+cudaError_t launch_matvec_simt(const MatvecArgs &a, int device);
+
+// Layout kernels.
+cudaError_t launch_pack(const int8_t *codes, int64_t N, int64_t K, uint8_t *qs,
+                        uint32_t *status, cudaStream_t s);
+cudaError_t launch_unpack(const uint8_t *qs, int64_t N, int64_t K, int8_t *codes,
+                          cudaStream_t s);
+cudaError_t launch_from_dense(const void *W, int w_f16, int64_t N, int64_t K, uint8_t *qs,
+                              uint16_t *d, uint32_t *status, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int sm_count(int device);
+
+}  // namespace tq2

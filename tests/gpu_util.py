@@ -1,0 +1,62 @@
+"""Helpers for the GPU parity tests: seeded cases, device transfer, and the
+element-wise comparison against the CPU oracle."""
+import numpy as np
+
+import oracle
+import tq2_synth as syn
+
+
+def dev(a, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+class Case:
+    """Seeded inputs of one linear plus the oracle's packed weights."""
+
+    def __init__(self, seed, M, N, K, heavy=False, prologue=False, linear=0):
+        self.M, self.N, self.K = M, N, K
+        self.codes = syn.codes(seed, N, K, linear=linear)
+        self.d = syn.scales(seed, N, K // 256, linear=linear)
+        self.x = syn.activations(seed, M, K, linear=linear, heavy=heavy)
+        self.s = syn.act_scale(seed, linear=linear) if prologue else 0.0
+        self.qs, flags = oracle.pack(self.codes)
+        assert flags == 0
+
+    def device(self):
+        return dev(self.x), dev(self.qs), dev(self.d)
+
+    def reference(self, rows=None):
+        if rows is None:
+            return oracle.matvec(self.x, self.qs, self.d, self.K, self.s)
+        return oracle.matvec_rows(self.x, self.qs, self.d, self.K, rows, self.s)
+
+
+def assert_within_tolerance(y_gpu, y_ref, tol_sum, what=""):
+    """|y_gpu - y_ref| <= 1e-3 * sum_k |d_b x'_k| + 1e-6, element by element."""
+    y = np.asarray(y_gpu, dtype=np.float64)
+    assert y.shape == y_ref.shape, (y.shape, y_ref.shape)
+    assert np.all(np.isfinite(y)), f"{what}: non-finite output"
+    err = np.abs(y - y_ref)
+    bound = oracle.tolerance(tol_sum)
+    bad = err > bound
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; first at {tuple(i)}: "
+            f"gpu={y[tuple(i)]!r} ref={y_ref[tuple(i)]!r} bound={bound[tuple(i)]!r}; "
+            f"max err/bound={float((err / bound).max()):.3g}")
+    return float((err / bound).max()) if err.size else 0.0
+
+
+def sample_rows(N, count, seed=0):
+    """Sorted distinct rows: the first/last few, every tile edge pattern, random."""
+    rng = np.random.default_rng(seed)
+    base = {0, 1, 15, 16, 17, N // 2, N - 17, N - 16, N - 2, N - 1}
+    r = set(int(v) for v in base if 0 <= v < N)
+    r.update(int(v) for v in rng.choice(N, size=min(count, N), replace=False))
+    return np.array(sorted(r), dtype=np.int64)

@@ -1,0 +1,90 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host (no GPU needed: every check below returns before any
+CUDA call; the fake pointers are never dereferenced)."""
+import ctypes
+
+import pytest
+
+import quantized_gemv_tq2_gb300 as tq2
+
+OK, NULL, SHAPE, ALIGN, DTYPE, ARG = 0, 1, 2, 3, 4, 5
+P = ctypes.c_void_p
+A16 = P(0x10000)   # 16-byte aligned fake device pointer
+A2 = P(0x10002)    # 2-byte aligned only
+NUL = P(0)
+S = P(0)           # stream
+
+
+@pytest.fixture(scope="module")
+def L():
+    return tq2.load()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = tq2.declared_symbols()
+    assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec",
+                          "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version"}
+    for n in names:
+        assert hasattr(L, n), n  # dlsym succeeds
+
+
+def test_version_and_status_strings(L):
+    assert tq2.version() >= 100
+    for st in range(8):
+        assert tq2.status_string(st).startswith("TQ2_")
+    assert "unknown" in tq2.status_string(99)
+    assert tq2.matvec_workspace_size(1, 4096, 4096) == 0
+
+
+def mv(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, st=NUL, impl=None):
+    if impl is None:
+        return L.tq2_matvec(x, M, qs, d, N, K, y, yd, s, NUL, 0, st, S)
+    return L.tq2_matvec_impl(x, M, qs, d, N, K, y, yd, s, NUL, 0, st, S, impl)
+
+
+def test_matvec_rejects_bad_shapes(L):
+    assert mv(L, K=300) == SHAPE
+    assert mv(L, K=-256) == SHAPE
+    assert mv(L, N=-1) == SHAPE
+    assert mv(L, M=17) == SHAPE
+    assert mv(L, M=-1) == SHAPE
+    assert mv(L, N=2 ** 62, K=2 ** 20) == SHAPE  # N*K overflows
+
+
+def test_matvec_rejects_bad_dtype_and_args(L):
+    assert mv(L, yd=2) == DTYPE
+    assert mv(L, s=-0.5) == ARG
+    assert mv(L, s=float("nan")) == ARG
+    assert mv(L, s=float("inf")) == ARG
+    assert mv(L, impl=3) == ARG
+    assert mv(L, impl=1, M=3) == ARG  # the tensor-core kernel takes M <= 2
+
+
+def test_matvec_empty_shapes_are_noops(L):
+    assert mv(L, M=0, x=NUL, y=NUL) == OK
+    assert mv(L, N=0, qs=NUL, d=NUL, y=NUL) == OK
+
+
+def test_matvec_rejects_null_and_misaligned(L):
+    assert mv(L, x=NUL) == NULL
+    assert mv(L, qs=NUL) == NULL
+    assert mv(L, d=NUL) == NULL
+    assert mv(L, y=NUL) == NULL
+    assert mv(L, x=A2) == ALIGN
+    assert mv(L, qs=A2) == ALIGN
+    assert mv(L, d=P(0x10001)) == ALIGN
+    assert mv(L, y=A2, yd=0) == ALIGN
+    assert mv(L, st=P(0x10002)) == ALIGN
+
+
+def test_layout_calls_reject_bad_arguments(L):
+    assert L.tq2_pack(A16, 4, 100, A16, NUL, S) == SHAPE
+    assert L.tq2_pack(NUL, 4, 256, A16, NUL, S) == NULL
+    assert L.tq2_pack(A16, 0, 256, A16, NUL, S) == OK
+    assert L.tq2_unpack(A16, -1, 256, A16, S) == SHAPE
+    assert L.tq2_unpack(A16, 4, 256, NUL, S) == NULL
+    assert L.tq2_from_dense(A16, 0, 4, 255, A16, A16, NUL, S) == SHAPE
+    assert L.tq2_from_dense(A16, 7, 4, 256, A16, A16, NUL, S) == DTYPE
+    assert L.tq2_from_dense(A16, 0, 4, 256, A16, NUL, NUL, S) == NULL
+    assert L.tq2_from_dense(A2, 0, 4, 256, A16, A16, NUL, S) == ALIGN  # fp32 W needs 4 bytes
+    assert L.tq2_from_dense(A16, 1, 0, 256, A16, A16, NUL, S) == OK

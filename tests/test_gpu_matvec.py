@@ -1,0 +1,212 @@
+"""GPU parity of tq2_matvec against the CPU oracle (element by element, within
+|dy| <= 1e-3 * sum_k |d_b x'_k| + 1e-6), plus the exact cases (one-hot x),
+determinism, empty shapes and the back-to-back launch configuration the
+benchmark times."""
+import numpy as np
+import pytest
+
+import oracle
+import tq2_synth as syn
+from gpu_util import Case, assert_within_tolerance, dev, host, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = {"auto": 0, "mma": 1, "simt": 2}
+
+
+@pytest.fixture(scope="module")
+def T():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import quantized_gemv_tq2_gb300 as tq2
+    tq2.load()
+    return torch
+
+
+def _run(T, case, impl, y_dtype=0, rows=None):
+    import quantized_gemv_tq2_gb300 as tq2
+    x, qs, d = case.device()
+    st = T.zeros(1, dtype=T.int32, device="cuda")
+    y = tq2.matvec(x, qs, d, y_dtype=y_dtype, act_scale=case.s, status=st, impl=impl)
+    T.cuda.synchronize()
+    assert int(st.item()) == 0
+    out = host(y).astype(np.float64)
+    return out if rows is None else out[:, rows]
+
+
+def _impls_for(M):
+    return ["auto", "mma", "simt"] if M <= 2 else ["auto", "simt"]
+
+
+# ---------------------------------------------------------------- small shapes, full compare
+@pytest.mark.parametrize("M,N,K", [
+    (1, 32, 512),      # the PR1 shape
+    (1, 1, 256), (1, 15, 256), (1, 17, 768), (2, 33, 1024), (1, 257, 4352),
+    (2, 100, 8448), (3, 40, 512), (16, 70, 1280), (1, 300, 2048),
+])
+@pytest.mark.parametrize("prologue", [False, True])
+def test_matvec_small_shapes(T, M, N, K, prologue):
+    case = Case(seed=M * 1000 + N + K, M=M, N=N, K=K, heavy=prologue, prologue=prologue)
+    y_ref, tol = case.reference()
+    for name in _impls_for(M):
+        for yd in (0, 1):
+            y = _run(T, case, IMPLS[name], y_dtype=yd)
+            assert_within_tolerance(y, y_ref, tol, f"{name} yd={yd} M={M} N={N} K={K}")
+
+
+def test_matvec_pr1_seed0(T):
+    case = Case(seed=0, M=1, N=32, K=512)
+    y_ref, tol = case.reference()
+    ye = oracle.matvec_exact(case.x, case.qs, case.d, 512)
+    for name in _impls_for(1):
+        y = _run(T, case, IMPLS[name])
+        assert_within_tolerance(y, y_ref, tol, name)
+        assert_within_tolerance(y, ye, tol, name + " vs exact")
+
+
+def test_matvec_pr1_exhaustive(T):
+    """K=512, N=32: every valid byte pattern at every byte position over three
+    code matrices, exact scales (1+2n+b)/1024, all 512 one-hot x (exact) and
+    four random x."""
+    import quantized_gemv_tq2_gb300 as tq2
+    pats = [c0 + 4 * c1 + 16 * c2 + 64 * c3
+            for c3 in range(3) for c2 in range(3) for c1 in range(3) for c0 in range(3)]
+    N, K = 32, 512
+    d = np.array([[(1 + 2 * n + b) / 1024.0 for b in range(2)] for n in range(N)],
+                 dtype=np.float16)
+    for t in range(3):
+        qs = np.array([[pats[(n + 32 * t + 7 * j) % 81] for j in range(K // 4)] for n in range(N)],
+                      dtype=np.uint8)
+        codes = oracle.unpack(qs, K).astype(np.float64)
+        want = (np.repeat(d.astype(np.float64), 256, axis=1) * (codes - 1)).T  # [K, N]
+        qd, dd = dev(qs), dev(d)
+        for impl, mstep in (("mma", 2), ("simt", 16), ("auto", 1)):
+            for k0 in range(0, K, mstep):
+                x = np.zeros((mstep, K), dtype=np.float16)
+                for i in range(mstep):
+                    x[i, k0 + i] = 1.0
+                for yd in (0, 1):
+                    y = tq2.matvec(dev(x), qd, dd, y_dtype=yd, impl=IMPLS[impl])
+                    T.cuda.synchronize()
+                    got = host(y).astype(np.float64)
+                    assert np.array_equal(got, want[k0:k0 + mstep]), (impl, t, k0, yd)
+        for seed in range(4):
+            x = syn.activations(seed, 2, K)
+            y_ref, tol = oracle.matvec(x, qs, d, K)
+            for impl in ("mma", "simt"):
+                y = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl])).astype(np.float64)
+                assert_within_tolerance(y, y_ref, tol, f"exhaustive t={t} seed={seed} {impl}")
+
+
+def test_matvec_one_hot_large_k(T):
+    import quantized_gemv_tq2_gb300 as tq2
+    N, K = 48, 16384
+    case = Case(seed=5, M=1, N=N, K=K)
+    qd, dd = dev(case.qs), dev(case.d)
+    for k in (0, 3, 4095, 4096, 9999, 16383):
+        x = np.zeros((1, K), dtype=np.float16)
+        x[0, k] = 1.0
+        want = case.d[:, k // 256].astype(np.float64) * (case.codes[:, k].astype(np.float64) - 1)
+        for impl in ("mma", "simt"):
+            got = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl]))[0].astype(np.float64)
+            assert np.array_equal(got, want), (impl, k)
+
+
+def test_matvec_extreme_values(T):
+    """Subnormal/large fp16 x and d, zero blocks: exact-arithmetic inputs."""
+    N, K = 40, 1024
+    case = Case(seed=9, M=2, N=N, K=K)
+    case.x[0, :8] = np.float16(6e-8)        # fp16 subnormals
+    case.x[0, 8:16] = np.float16(60000.0)
+    case.x[1, 256:512] = 0
+    case.d[0, :] = np.float16(6e-8)
+    case.d[1, :] = np.float16(60000.0)
+    case.d[2, 1] = 0
+    y_ref, tol = case.reference()
+    for name in ("mma", "simt"):
+        y = _run(T, case, IMPLS[name])
+        assert_within_tolerance(y, y_ref, tol, name)
+
+
+def test_matvec_empty_shapes(T):
+    import quantized_gemv_tq2_gb300 as tq2
+    x = T.zeros((1, 0), dtype=T.float16, device="cuda")
+    qs = T.zeros((8, 0), dtype=T.uint8, device="cuda")
+    d = T.zeros((8, 0), dtype=T.float16, device="cuda")
+    y = T.full((1, 8), 7.0, dtype=T.float32, device="cuda")
+    tq2.matvec(x, qs, d, K=0, y=y)
+    T.cuda.synchronize()
+    assert np.all(host(y) == 0.0)  # empty sums
+    x = T.zeros((0, 256), dtype=T.float16, device="cuda")
+    qs = T.zeros((8, 64), dtype=T.uint8, device="cuda")
+    d = T.zeros((8, 1), dtype=T.float16, device="cuda")
+    assert tq2.matvec(x, qs, d).shape == (0, 8)
+
+
+def test_matvec_is_deterministic(T):
+    import quantized_gemv_tq2_gb300 as tq2
+    case = Case(seed=21, M=2, N=1000, K=4096)
+    x, qs, d = case.device()
+    for impl in (1, 2):
+        first = host(tq2.matvec(x, qs, d, impl=impl))
+        for _ in range(20):
+            assert np.array_equal(host(tq2.matvec(x, qs, d, impl=impl)), first)
+
+
+# ---------------------------------------------------------------- the configurations
+@pytest.mark.parametrize("seed", [1, 2, 3])
+@pytest.mark.parametrize("N", [4096, 256])
+def test_matvec_qo_and_kv_full(T, seed, N):
+    case = Case(seed=seed, M=1, N=N, K=4096)
+    y_ref, tol = case.reference()
+    for name in ("auto", "mma", "simt"):
+        assert_within_tolerance(_run(T, case, IMPLS[name]), y_ref, tol, f"{name} N={N}")
+
+
+@pytest.mark.parametrize("N,K", [(16384, 4096), (4096, 16384)])
+@pytest.mark.parametrize("prologue", [False, True])
+def test_matvec_layer_big_shapes_full(T, N, K, prologue):
+    case = Case(seed=4, M=1, N=N, K=K, heavy=prologue, prologue=prologue)
+    y_ref, tol = case.reference()
+    for yd in (0, 1):
+        assert_within_tolerance(_run(T, case, 0, y_dtype=yd), y_ref, tol, f"yd={yd}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("N,K", [(16384, 4096), (4096, 16384)])
+@pytest.mark.parametrize("heavy", [False, True])
+def test_matvec_m_sweep_sampled(T, M, N, K, heavy):
+    case = Case(seed=100 + M, M=M, N=N, K=K, heavy=heavy, prologue=heavy)
+    rows = sample_rows(N, 96, seed=M)
+    y_ref, tol = case.reference(rows)
+    assert_within_tolerance(_run(T, case, 0, rows=rows), y_ref, tol, f"M={M} heavy={heavy}")
+
+
+def test_matvec_back_to_back_graph_like_bench(T):
+    """The launch configuration the benchmark times: one layer's seven calls
+    captured in a CUDA graph (programmatic dependent launches between them),
+    replayed; sampled rows of every output checked against the oracle."""
+    import quantized_gemv_tq2_gb300 as tq2
+    shapes = [(4096, 4096), (256, 4096), (256, 4096), (4096, 4096),
+              (16384, 4096), (16384, 4096), (4096, 16384)]
+    cases = [Case(seed=7, M=1, N=n, K=k, linear=i) for i, (n, k) in enumerate(shapes)]
+    dev_in = [c.device() for c in cases]
+    ys = [T.empty((1, c.N), dtype=T.float32, device="cuda") for c in cases]
+    s = T.cuda.Stream()
+    with T.cuda.stream(s):
+        for (x, qs, d), y in zip(dev_in, ys):  # warm-up outside capture
+            tq2.matvec(x, qs, d, y=y)
+        s.synchronize()
+        for y in ys:
+            y.zero_()
+        g = T.cuda.CUDAGraph()
+        with T.cuda.graph(g, stream=s):
+            for (x, qs, d), y in zip(dev_in, ys):
+                tq2.matvec(x, qs, d, y=y)
+        for _ in range(3):
+            g.replay()
+    s.synchronize()
+    for c, y in zip(cases, ys):
+        rows = sample_rows(c.N, 64)
+        y_ref, tol = c.reference(rows)
+        assert_within_tolerance(host(y)[:, rows].astype(np.float64), y_ref, tol, f"N={c.N}")

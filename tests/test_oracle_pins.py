@@ -401,3 +401,12 @@ def test_generator_words_equal_sequential_splitmix64():
         seq.append(mix(state))
     assert [int(w) for w in syn.words(seed, tid, 10)] == seq
     assert [int(w) for w in syn.words(seed, tid, 4, start=6)] == seq[6:]
+
+
+def test_generator_torch_code_expansion_matches_numpy():
+    import torch
+    bits = syn.code_bits(3, syn.tensor_id(2, syn.SLOT_CODE_BITS), 64 * 512 // 4)
+    a = syn.codes_from_bits(bits, 64, 512)
+    b = syn.codes_from_bits_torch(torch.from_numpy(bits), 64, 512).numpy()
+    assert np.array_equal(a, b)
+    assert np.array_equal(a, syn.codes(3, 64, 512, linear=2))

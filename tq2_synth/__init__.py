@@ -38,7 +38,7 @@ __all__ = [
     "SLOT_CODE_BITS", "SLOT_SCALES", "SLOT_X", "SLOT_HEAVY_SEL", "SLOT_HEAVY_Z",
     "SLOT_ACT_SCALE", "SLOT_DENSE",
     "tensor_id", "words", "uniform", "normal",
-    "code_bits", "codes_from_bits", "codes", "scales", "activations",
+    "code_bits", "codes_from_bits", "codes_from_bits_torch", "codes", "scales", "activations",
     "act_scale", "dense_normal",
 ]
 
@@ -108,6 +108,16 @@ def codes_from_bits(bits: np.ndarray, n: int, k: int) -> np.ndarray:
     out = np.empty((n, k // 4, 4), dtype=np.int8)
     for j in range(4):
         out[:, :, j] = ((b >> (2 * j)) & 1) + ((b >> (2 * j + 1)) & 1)
+    return out.reshape(n, k)
+
+
+def codes_from_bits_torch(bits, n: int, k: int):
+    """Same as ``codes_from_bits`` for a torch uint8 tensor (any device)."""
+    import torch
+    b = bits.reshape(n, k // 4)
+    out = torch.empty((n, k // 4, 4), dtype=torch.int8, device=bits.device)
+    for j in range(4):
+        out[:, :, j] = (((b >> (2 * j)) & 1) + ((b >> (2 * j + 1)) & 1)).to(torch.int8)
     return out.reshape(n, k)
 
 
