@@ -182,12 +182,14 @@ def time_graph(torch, g, stream, steps, warmup, barrier=None):
         barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("tq2_timed")
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(steps):
             g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     return e0.elapsed_time(e1) / steps  # ms per replay
 
 
@@ -297,11 +299,12 @@ def run_gpu(args):
     ident = getattr(props, "uuid", None)
     ident = f"GPU-{ident}" if ident is not None and not str(ident).startswith("GPU-") else (ident or local)
     sampler = ClockSampler(ident)
-    sampler.start()
-    soak = time_graph(torch, g, stream, 1, 0)
-    time_graph(torch, g, stream, max(1, int(1.0 / max(soak * 1e-3, 1e-6))), 0)
+    if not args.no_clocks:
+        sampler.start()
+        soak = time_graph(torch, g, stream, 1, 0)
+        time_graph(torch, g, stream, max(1, int(1.0 / max(soak * 1e-3, 1e-6))), 0)
     ms = time_graph(torch, g, stream, args.steps, args.warmup, barrier)
-    clocks = sampler.stop()
+    clocks = sampler.stop() if not args.no_clocks else {"skipped": True}
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms], device=dev)
@@ -413,6 +416,41 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ profiling case
+CASES = {"gateup": (16384, 4096), "down": (4096, 16384), "qo": (4096, 4096), "kv": (256, 4096)}
+
+
+def run_case(args):
+    """A small case for ncu: `copies` distinct weight sets of one shape (more
+    than L2 in total for the big shapes), `launches` eager tq2_matvec calls
+    round-robin over them.  Prints the mean wall time per call (not a bench
+    value: the calls are eager and may run under a profiler)."""
+    import torch
+    import quantized_gemv_tq2_gb300 as tq2
+    import tq2_synth as syn
+    N, K = CASES[args.case]
+    dev = torch.device("cuda", 0)
+    tq2.load()
+    ws = []
+    for c in range(args.copies):
+        bits = torch.from_numpy(syn.code_bits(SEED, syn.tensor_id(c, syn.SLOT_CODE_BITS),
+                                              N * K // 4)).to(dev)
+        ws.append((tq2.pack(syn.codes_from_bits_torch(bits, N, K)),
+                   torch.from_numpy(syn.scales(SEED, N, K // 256, linear=c)).to(dev)))
+    x = torch.from_numpy(syn.activations(SEED, args.M, K)).to(dev)
+    y = torch.empty((args.M, N), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.launches):
+        qs, d = ws[i % len(ws)]
+        tq2.matvec(x, qs, d, y=y, impl=args.case_impl)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.launches
+    print(json.dumps({"case": args.case, "N": N, "K": K, "M": args.M, "copies": args.copies,
+                      "launches": args.launches, "impl": args.case_impl,
+                      "wall_us_per_call_eager": round(dt * 1e6, 2)}))
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The CPU oracle timed on the host cores, on this workload's metric."""
@@ -462,8 +500,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only, no extras")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="no clock sampling / soak (for runs under a profiler)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", choices=sorted(CASES), help="profiling case instead of the bench")
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--copies", type=int, default=8)
+    ap.add_argument("--launches", type=int, default=8)
+    ap.add_argument("--case-impl", type=int, default=0)
     args = ap.parse_args()
+    if args.case:
+        return run_case(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

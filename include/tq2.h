@@ -152,6 +152,10 @@ TQ2_API tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *
                            void *workspace, size_t workspace_bytes, uint32_t *d_status,
                            tq2_stream_t stream, int impl);
 
+/* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
+ * host thread ("no error" if none): name and description, static storage. */
+TQ2_API const char *tq2_last_cuda_error(void);
+
 /* Static, human-readable name of a status. */
 TQ2_API const char *tq2_status_string(tq2_status status);
 

@@ -37,7 +37,10 @@ _lib = None
 class TQ2Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        msg = f"{where}: {status_string(status)} (status {status})"
+        if status == 6:
+            msg += f" [{load().tq2_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -64,6 +67,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_status_string.argtypes = [I32]
         L.tq2_status_string.restype = ctypes.c_char_p
         L.tq2_version.argtypes = []
+        L.tq2_last_cuda_error.argtypes = []
+        L.tq2_last_cuda_error.restype = ctypes.c_char_p
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
                    "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int

@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 
 #include "tq2_internal.cuh"
 
@@ -40,9 +41,12 @@ tq2_status check_nk(int64_t N, int64_t K)
     return TQ2_OK;
 }
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 tq2_status from_cuda(cudaError_t e)
 {
     if (e == cudaSuccess) return TQ2_OK;
+    t_last_cuda_error = e;
     cudaGetLastError();  // the error is returned; do not leave it sticky for the caller
     return TQ2_ERR_CUDA;
 }
@@ -188,5 +192,13 @@ const char *tq2_status_string(tq2_status status)
 }
 
 int tq2_version(void) { return 100; }
+
+const char *tq2_last_cuda_error(void)
+{
+    static thread_local char buf[256];
+    const cudaError_t e = t_last_cuda_error;
+    snprintf(buf, sizeof buf, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return buf;
+}
 
 }  // extern "C"

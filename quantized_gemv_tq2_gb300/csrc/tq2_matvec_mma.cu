@@ -10,10 +10,15 @@
 //
 // Data path per CTA (one CTA owns a contiguous range of output rows, all K):
 //   * a producer warp streams the CTA's packed rows into a shared-memory ring
-//     with 1-D TMA bulk copies (cp.async.bulk + mbarrier complete_tx), one
-//     copy per row segment, L2 evict-first; it starts before the kernel waits
-//     on the previous grid (programmatic dependent launch), because weights
-//     never depend on earlier kernels;
+//     of 16 KB stages with TMA, L2 evict-first: for K <= 4096 a stage is whole
+//     rows, contiguous in memory, fetched with one 1-D bulk copy
+//     (cp.async.bulk); for K > 4096 a stage is 16 rows x 4096 codes, fetched
+//     with one 2-D tensor copy of a 16-row box (8/4/2/1-row boxes for the
+//     CTA's last rows, so no other CTA's rows are read).  TMA throughput on
+//     this part scales with the size of each copy (1 KB copies cap a CTA at a
+//     few GB/s), hence one large copy per stage.  The producer starts before
+//     the kernel waits on the previous grid (programmatic dependent launch),
+//     because weights never depend on earlier kernels;
 //   * the d slice of the CTA's rows is staged to shared memory as fp32;
 //   * after griddepcontrol.wait, x (or its int8 fake-quant codes) is staged
 //     to shared memory in MMA-fragment order, with per-block sums X_b;
@@ -35,10 +40,12 @@
 // classes are combined with their powers of two.  Every step is exact except
 // fp32 accumulation, far inside the 1e-3 * sum|d x| tolerance.
 //
-// Layout of one 16-row A tile: mma row g <- smem row g, row g+8 <- g+8; the
-// smem row stride is padded so that rows g and g+1 fall 64 bytes apart in the
-// bank space, which makes the 16-byte fragment loads conflict-free.
+// Layout of one 16-row A tile: mma row g <- smem row g, row g+8 <- g+8, rows
+// dense in shared memory as TMA writes them.
+#include <cuda.h>
 #include <cuda_fp16.h>
+
+#include <cudaTypedefs.h>
 
 #include <atomic>
 
@@ -52,11 +59,14 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kMmaThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kChunkBlocks = 16;                    // 256-blocks per stage row (4096 codes)
 constexpr int kTargetSmem = 112 * 1024;             // two CTAs per SM (PDL overlap)
-constexpr int kMaxSmem = 227 * 1024;
 constexpr unsigned long long kTimeoutNs = 200ull * 1000 * 1000;
 
 struct MmaParams {
+    // K > 4096 only: qs as a 2-D tensor of uint64 [N][K/32], boxes of
+    // 128 x {16, 8, 4, 2, 1} rows
+    CUtensorMap tmap[5];  // 64-byte aligned by its type
     MatvecArgs a;
+    int tma2d;       // 0: 1-D bulk copies of whole rows; 1: 2-D tensor boxes
     int G;           // CTAs; CTA i owns rows [i*N/G, (i+1)*N/G)
     int B;           // 256-blocks per row
     int nbk_full;    // 256-blocks per stage row
@@ -92,15 +102,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// try_wait suspends the thread until the phase completes or the hint (ns)
+// runs out, so waiting warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(20000)
         : "memory");
     return ok != 0;
 }
@@ -112,15 +124,27 @@ __device__ __forceinline__ unsigned long long globaltimer()
     return t;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity; give up after kTimeoutNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
+    if (mbar_test_wait(bar, parity)) return true;  // non-blocking fast path
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer() - t0 > kTimeoutNs) return false;
     }
 }
@@ -142,11 +166,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+__device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                             uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void consumer_barrier()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
+// D = A * B + D
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1)
 {
@@ -156,6 +191,44 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+
+// D = A * B + c (the same scalar in all four accumulator registers)
+__device__ __forceinline__ void mma_16816_init(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1, float c)
+{
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c));
+}
+
+// shared-memory loads through 32-bit shared-window addresses (volatile:
+// they stay ordered after the mbarrier waits that publish the data)
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// One class c of one 16-code word pair: A lanes are q * 4^c * 2^-24.
+#define TQ2_MMA_CLASS(FIRST, C, MASK, CINIT)                                                   \
+    do {                                                                                       \
+        if (FIRST)                                                                             \
+            mma_16816_init(C, w0 & (MASK), w1 & (MASK), s0 & (MASK), s1 & (MASK), b0, b1, CINIT); \
+        else                                                                                   \
+            mma_16816(C, w0 & (MASK), w1 & (MASK), s0 & (MASK), s1 & (MASK), b0, b1);          \
+    } while (0)
 
 // Static int8 fake-quant code (gemma4 wNa8o8 page, "Implemented"):
 // rint(x * (1/s)) in fp32, ties to even, clamped to [-128, 127]; NaN -> 0.
@@ -224,17 +297,38 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
             const int rgb = s / p.n_kc, kc = s % p.n_kc;
             const int rg0 = rgb * p.rg_s;
             const int rows = min(p.rg_s * 16, nrows - rg0 * 16);
-            const int kb0 = kc * p.nbk_full;
-            const int nbk = min(p.nbk_full, p.B - kb0);
-            const uint32_t seg = (uint32_t)nbk * 64u;
             const uint32_t full = smem_addr(&bars[slot]);
-            if (lane == 0) mbar_arrive_expect_tx(full, seg * (uint32_t)rows);
-            __syncwarp();
             const uint32_t dst0 = smem_addr(ring + (size_t)slot * p.stage_bytes);
-            for (int r = lane; r < rows; r += 32) {
-                const uint8_t *src = p.a.qs + (r0 + rg0 * 16 + r) * row_bytes + (int64_t)kb0 * 64;
-                bulk_g2s(dst0 + (uint32_t)(r * p.rb), src, seg, full, pol);
+            if (!p.tma2d) {
+                // whole rows [rg0*16, rg0*16 + rows): one contiguous copy
+                const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full, bytes);
+                    bulk_g2s(dst0, p.a.qs + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
+                }
+            } else {
+                // 16 rows x 1024 bytes (columns past the row end read as zero);
+                // a partial group is split into boxes of 8, 4, 2, 1 rows
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)rows * 1024u);
+                __syncwarp();
+                const int y0 = (int)(r0 + rg0 * 16);
+                const int x = kc * 128;
+                if (rows == 16) {
+                    if (lane == 0) tensor2d_g2s(dst0, &p.tmap[0], x, y0, full, pol);
+                } else {
+                    int roff = 0, box = 0;
+#pragma unroll
+                    for (int i = 1; i < 5; ++i) {
+                        const int h = 16 >> i;
+                        if (rows & h) {
+                            if (lane == box) tensor2d_g2s(dst0 + roff * 1024, &p.tmap[i], x, y0 + roff, full, pol);
+                            roff += h;
+                            ++box;
+                        }
+                    }
+                }
             }
+            __syncwarp();
             issued = s + 1;
         }
         // No copy may still be writing shared memory when the CTA exits.
@@ -259,10 +353,27 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         const int rg = i / (kM * 16), rest = i - rg * (kM * 16);
         red[(rg * kConsumerWarps + warp) * kM * 16 + rest] = 0.0f;
     }
-    // d slice of this CTA's rows, fp32
-    for (int i = tid; i < nrows * B; i += kConsumerThreads) {
-        const int r = i / B, b = i - r * B;
-        dsm[r * p.dstr + b] = __half2float(__ushort_as_half(p.a.d[(r0 + r) * B + b]));
+    // d slice of this CTA's rows (contiguous in memory), fp32.  All loads of
+    // a batch are issued before the first store so their latencies overlap.
+    {
+        const int nd = nrows * B;
+        const uint16_t *dsrc = p.a.d + r0 * B;
+        for (int base = 0; base < nd; base += kConsumerThreads * 8) {
+            uint16_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kConsumerThreads + tid;
+                v[j] = (i < nd) ? dsrc[i] : (uint16_t)0;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kConsumerThreads + tid;
+                if (i < nd) {
+                    const int r = i / B, b = i - r * B;
+                    dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
+                }
+            }
+        }
     }
 
     // x depends on the previous kernel in the stream.
@@ -272,10 +383,27 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
     // is 16 bytes = words 2h and 2h+1 of the t-th quarter of the block, each
     // as (x[c], x[8+c], x[4+c], x[12+c]) of that 16-code word.
     {
-        const int total = kM * B * 16;  // 16-code words
-        for (int base = warp * 32; base < total; base += kConsumerThreads) {
-            const int L = base + lane;
-            const bool act = L < total;
+        // 16-code words of x; a thread takes words L = base0 + j*256 + lane
+        // (j < 4) and issues the loads of all four before using any.
+        constexpr int kXBatch = 4;
+        const int total = kM * B * 16;
+        for (int base0 = warp * 32; base0 < total; base0 += kConsumerThreads * kXBatch) {
+          uint4 xv[kXBatch][2];
+#pragma unroll
+          for (int j = 0; j < kXBatch; ++j) {
+              const int L = base0 + j * kConsumerThreads + lane;
+              if (L < total) {
+                  const int m = L / (B * 16);
+                  const int rem = L - m * B * 16;
+                  const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(rem >> 4) * 256 + (rem & 15) * 16;
+                  xv[j][0] = *reinterpret_cast<const uint4 *>(src);
+                  xv[j][1] = *reinterpret_cast<const uint4 *>(src + 8);
+              }
+          }
+#pragma unroll
+          for (int j = 0; j < kXBatch; ++j) {
+            const int L = base0 + j * kConsumerThreads + lane;
+            const bool act = L < total;  // uniform over each half-warp (total % 16 == 0)
             float sum = 0.0f;
             int m = 0, b = 0, wib = 0;
             if (act) {
@@ -283,36 +411,40 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 const int rem = L - m * B * 16;
                 b = rem >> 4;
                 wib = rem & 15;
-                const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)b * 256 + wib * 16;
-                const uint4 v0 = *reinterpret_cast<const uint4 *>(src);
-                const uint4 v1 = *reinterpret_cast<const uint4 *>(src + 8);
-                const uint32_t raw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                uint16_t h[16];
+                uint32_t raw[8] = {xv[j][0].x, xv[j][0].y, xv[j][0].z, xv[j][0].w,
+                                   xv[j][1].x, xv[j][1].y, xv[j][1].z, xv[j][1].w};
+                if (prologue) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    uint16_t hb = (uint16_t)(raw[j >> 1] >> (16 * (j & 1)));
-                    float f = __half2float(__ushort_as_half(hb));
-                    if (prologue) {
-                        f = fq_code(f, p.a.inv_scale);
-                        hb = __half_as_ushort(__float2half_rn(f));  // exact: |f| <= 128
+                    for (int q = 0; q < 8; ++q) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[q]));
+                        const __half2 h2 = __floats2half2_rn(fq_code(f.x, p.a.inv_scale),
+                                                             fq_code(f.y, p.a.inv_scale));  // exact
+                        raw[q] = *reinterpret_cast<const uint32_t *>(&h2);
                     }
-                    h[j] = hb;
-                    sum += f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[q]));
+                    sum += f.x + f.y;
                 }
                 const int t4 = wib >> 2, i4 = wib & 3;
-                uint8_t *dst = xs + (size_t)b * 512 * kM + (i4 >> 1) * (4 * kM * 64) + t4 * 16 +
-                               (i4 & 1) * 8;
+                const uint32_t dst = smem_addr(xs) + (uint32_t)(b * 512 * kM + (i4 >> 1) * (4 * kM * 64) +
+                                                              t4 * 16 + (i4 & 1) * 8 + m * 4 * 64);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint2 e;
-                    e.x = (uint32_t)h[c] | ((uint32_t)h[8 + c] << 16);
-                    e.y = (uint32_t)h[4 + c] | ((uint32_t)h[12 + c] << 16);
-                    *reinterpret_cast<uint2 *>(dst + (4 * m + c) * 64) = e;
+                    // (x[c], x[8+c]) and (x[4+c], x[12+c]): halves (c & 1) of the raw words
+                    const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+                    const uint32_t lo = __byte_perm(raw[c >> 1], raw[4 + (c >> 1)], sel);
+                    const uint32_t hi = __byte_perm(raw[2 + (c >> 1)], raw[6 + (c >> 1)], sel);
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst + (uint32_t)(c * 64)), "r"(lo),
+                                 "r"(hi)
+                                 : "memory");
                 }
             }
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
             if (act && (lane & 15) == 0) xsum[b * kM + m] = sum;
+          }
         }
     }
     consumer_barrier();
@@ -339,24 +471,99 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         }
     };
 
+    // per-thread shared-memory byte offsets, hoisted out of the loops
+    const uint32_t a_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
+    const uint32_t a_half = (uint32_t)(8 * p.rb);             // row g -> row g + 8
+    const uint32_t x_thr = smem_addr(xs) + (uint32_t)(gg * 64 + t * 16);
+    const uint32_t x_blk = 512u * kM;                          // per 256-block
+    const uint32_t x_half = 256u * kM;                         // words 0,1 -> 2,3
+    const uint32_t d_thr = smem_addr(dsm) + (uint32_t)(g * p.dstr) * 4u;
+    const uint32_t d_half = (uint32_t)(8 * p.dstr) * 4u;
+    const uint32_t xs_thr = smem_addr(xsum) + (uint32_t)mcol * 4u;
+    const uint32_t rg_stride_d = (uint32_t)(16 * p.dstr) * 4u;
+
+    int slot = 0, phase = 0, kc = 0, rg0 = 0;  // stage iterator (no divisions)
+    bool alive = true;        // false after this warp's wait ran out: no more waits
+    bool ready_lane = false;  // early, non-blocking test of this stage's barrier
     for (int s = 0; s < n_stages; ++s) {
-        const int slot = s % S;
         // every lane waits (acquire); the decision is made warp-uniform
-        bool ok = !__any_sync(0xffffffffu, *abort_flag != 0);
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[slot]), (s / S) & 1))) {
+        bool ok = alive;
+        if (ok && !__all_sync(0xffffffffu, ready_lane) &&
+            !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[slot]), (uint32_t)phase))) {
             if (lane == 0) report_timeout(p, abort_flag);
-            ok = false;
+            ok = alive = false;
+        }
+        ready_lane = false;
+        if (ok && s + 1 < n_stages) {
+            // test the next stage now; its latency overlaps this stage's math
+            const int nslot = (slot + 1 == S) ? 0 : slot + 1;
+            const int nphase = (slot + 1 == S) ? (phase ^ 1) : phase;
+            ready_lane = mbar_test_wait(smem_addr(&bars[nslot]), (uint32_t)nphase);
         }
         if (ok) {
-            const int rgb = s / p.n_kc, kc = s % p.n_kc;
-            const int rg0 = rgb * p.rg_s;
             const int nrg_s = min(p.rg_s, nrg - rg0);
             const int kb0 = kc * p.nbk_full;
             const int nbk = min(p.nbk_full, B - kb0);
-            const uint8_t *st = ring + (size_t)slot * p.stage_bytes;
-            const int units = nrg_s * nbk;
-            for (int u = warp; u < units; u += kConsumerWarps) {
-                const int j = u / nbk, bl = u - j * nbk;
+            const uint32_t st = a_thr + (uint32_t)(slot * p.stage_bytes);
+            if (nrg_s == 1 && nbk == 2 * kConsumerWarps) {
+                // Full 16-row x 16-block stage: this warp takes blocks warp and
+                // warp + 8 of row group rg0, computed together (8 independent
+                // MMA chains), straight-line.
+                const int rg = rg0;
+                if (rg != cur_rg) {
+                    if (cur_rg >= 0) flush(cur_rg);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = 0.0f;
+                    cur_rg = rg;
+                }
+                const int kbA = kb0 + warp, kbB = kbA + kConsumerWarps;
+                const uint32_t paA = st + (uint32_t)(warp * 64);
+                const uint32_t paB = paA + (uint32_t)(kConsumerWarps * 64);
+                const uint4 waA = lds128(paA), wbA = lds128(paA + a_half);
+                const uint4 waB = lds128(paB), wbB = lds128(paB + a_half);
+                const uint32_t pxA = x_thr + (uint32_t)kbA * x_blk, pxB = x_thr + (uint32_t)kbB * x_blk;
+                const uint4 xaA = lds128(pxA), xbA = lds128(pxA + x_half);
+                const uint4 xaB = lds128(pxB), xbB = lds128(pxB + x_half);
+                const uint32_t pdA = d_thr + (uint32_t)rg * rg_stride_d + (uint32_t)kbA * 4u;
+                const uint32_t pdB = pdA + (uint32_t)(kConsumerWarps * 4);
+                const float dgA = lds_f32(pdA), dg8A = lds_f32(pdA + d_half);
+                const float dgB = lds_f32(pdB), dg8B = lds_f32(pdB + d_half);
+                const float xiA = -lds_f32(xs_thr + (uint32_t)kbA * (4u * kM)) * 5.9604644775390625e-08f;
+                const float xiB = -lds_f32(xs_thr + (uint32_t)kbB * (4u * kM)) * 5.9604644775390625e-08f;
+                float a0[4], a1[4], a2[4], a3[4], e0[4], e1[4], e2[4], e3[4];
+#define TQ2_WORD_PAIR(FIRST, WA_, WB_, B0_, B1_, C0_, C1_, C2_, C3_, XI_)          \
+    {                                                                          \
+        const uint32_t w0 = WA_, w1 = WB_, s0 = w0 >> 8, s1 = w1 >> 8;         \
+        const uint32_t b0 = B0_, b1 = B1_;                                     \
+        TQ2_MMA_CLASS(FIRST, C0_, 0x00030003u, XI_);                           \
+        TQ2_MMA_CLASS(FIRST, C1_, 0x000C000Cu, 0.0f);                          \
+        TQ2_MMA_CLASS(FIRST, C2_, 0x00300030u, 0.0f);                          \
+        TQ2_MMA_CLASS(FIRST, C3_, 0x00C000C0u, 0.0f);                          \
+    }
+                TQ2_WORD_PAIR(true, waA.x, wbA.x, xaA.x, xaA.y, a0, a1, a2, a3, xiA)
+                TQ2_WORD_PAIR(true, waB.x, wbB.x, xaB.x, xaB.y, e0, e1, e2, e3, xiB)
+                TQ2_WORD_PAIR(false, waA.y, wbA.y, xaA.z, xaA.w, a0, a1, a2, a3, 0.0f)
+                TQ2_WORD_PAIR(false, waB.y, wbB.y, xaB.z, xaB.w, e0, e1, e2, e3, 0.0f)
+                TQ2_WORD_PAIR(false, waA.z, wbA.z, xbA.x, xbA.y, a0, a1, a2, a3, 0.0f)
+                TQ2_WORD_PAIR(false, waB.z, wbB.z, xbB.x, xbB.y, e0, e1, e2, e3, 0.0f)
+                TQ2_WORD_PAIR(false, waA.w, wbA.w, xbA.z, xbA.w, a0, a1, a2, a3, 0.0f)
+                TQ2_WORD_PAIR(false, waB.w, wbB.w, xbB.z, xbB.w, e0, e1, e2, e3, 0.0f)
+#undef TQ2_WORD_PAIR
+                acc[0][0] = fmaf(dgB, e0[0], fmaf(dgA, a0[0], acc[0][0]));
+                acc[0][1] = fmaf(dg8B, e0[2], fmaf(dg8A, a0[2], acc[0][1]));
+                acc[1][0] = fmaf(dgB, e1[1], fmaf(dgA, a1[1], acc[1][0]));
+                acc[1][1] = fmaf(dg8B, e1[3], fmaf(dg8A, a1[3], acc[1][1]));
+                acc[2][0] = fmaf(dgB, e2[0], fmaf(dgA, a2[0], acc[2][0]));
+                acc[2][1] = fmaf(dg8B, e2[2], fmaf(dg8A, a2[2], acc[2][1]));
+                acc[3][0] = fmaf(dgB, e3[1], fmaf(dgA, a3[1], acc[3][0]));
+                acc[3][1] = fmaf(dg8B, e3[3], fmaf(dg8A, a3[3], acc[3][1]));
+            } else {
+            int j = 0, bl = warp;  // unit u = warp + 8 i  ->  (16-row group j, block bl)
+            while (bl >= nbk) {
+                bl -= nbk;
+                ++j;
+            }
+            while (j < nrg_s) {
                 const int rg = rg0 + j, kb = kb0 + bl;
                 if (rg != cur_rg) {
                     if (cur_rg >= 0) flush(cur_rg);
@@ -364,32 +571,48 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                     for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = 0.0f;
                     cur_rg = rg;
                 }
-                const uint8_t *pa = st + (j * 16 + g) * p.rb + bl * 64 + t * 16;
-                const uint4 wa = *reinterpret_cast<const uint4 *>(pa);
-                const uint4 wb = *reinterpret_cast<const uint4 *>(pa + 8 * p.rb);
-                const uint8_t *px = xs + (size_t)kb * 512 * kM + gg * 64 + t * 16;
-                const uint4 xa = *reinterpret_cast<const uint4 *>(px);
-                const uint4 xb = *reinterpret_cast<const uint4 *>(px + 4 * kM * 64);
-                const float dg = dsm[(rg * 16 + g) * p.dstr + kb];
-                const float dg8 = dsm[(rg * 16 + g + 8) * p.dstr + kb];
-                const float xi = -xsum[kb * kM + mcol] * 5.9604644775390625e-08f;  // 2^-24
-                float c0[4] = {xi, xi, xi, xi};
-                float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f},
-                      c3[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t w0[4] = {wa.x, wa.y, wa.z, wa.w};
-                const uint32_t w1[4] = {wb.x, wb.y, wb.z, wb.w};
-                const uint32_t bx[4][2] = {{xa.x, xa.y}, {xa.z, xa.w}, {xb.x, xb.y}, {xb.z, xb.w}};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t s0 = w0[i] >> 8, s1 = w1[i] >> 8;
-                    mma_16816(c0, w0[i] & 0x00030003u, w1[i] & 0x00030003u, s0 & 0x00030003u,
-                              s1 & 0x00030003u, bx[i][0], bx[i][1]);
-                    mma_16816(c1, w0[i] & 0x000C000Cu, w1[i] & 0x000C000Cu, s0 & 0x000C000Cu,
-                              s1 & 0x000C000Cu, bx[i][0], bx[i][1]);
-                    mma_16816(c2, w0[i] & 0x00300030u, w1[i] & 0x00300030u, s0 & 0x00300030u,
-                              s1 & 0x00300030u, bx[i][0], bx[i][1]);
-                    mma_16816(c3, w0[i] & 0x00C000C0u, w1[i] & 0x00C000C0u, s0 & 0x00C000C0u,
-                              s1 & 0x00C000C0u, bx[i][0], bx[i][1]);
+                const uint32_t pa = st + (uint32_t)(j * 16 * p.rb + bl * 64);
+                const uint4 wa = lds128(pa);
+                const uint4 wb = lds128(pa + a_half);
+                const uint32_t px = x_thr + (uint32_t)kb * x_blk;
+                const uint4 xa = lds128(px);
+                const uint4 xb = lds128(px + x_half);
+                const uint32_t pd = d_thr + (uint32_t)rg * rg_stride_d + (uint32_t)kb * 4u;
+                const float dg = lds_f32(pd);
+                const float dg8 = lds_f32(pd + d_half);
+                const float xi = -lds_f32(xs_thr + (uint32_t)kb * (4u * kM)) * 5.9604644775390625e-08f;
+                float c0[4], c1[4], c2[4], c3[4];
+                {
+                    const uint32_t w0 = wa.x, w1 = wb.x, s0 = w0 >> 8, s1 = w1 >> 8;
+                    const uint32_t b0 = xa.x, b1 = xa.y;
+                    TQ2_MMA_CLASS(true, c0, 0x00030003u, xi);
+                    TQ2_MMA_CLASS(true, c1, 0x000C000Cu, 0.0f);
+                    TQ2_MMA_CLASS(true, c2, 0x00300030u, 0.0f);
+                    TQ2_MMA_CLASS(true, c3, 0x00C000C0u, 0.0f);
+                }
+                {
+                    const uint32_t w0 = wa.y, w1 = wb.y, s0 = w0 >> 8, s1 = w1 >> 8;
+                    const uint32_t b0 = xa.z, b1 = xa.w;
+                    TQ2_MMA_CLASS(false, c0, 0x00030003u, 0.0f);
+                    TQ2_MMA_CLASS(false, c1, 0x000C000Cu, 0.0f);
+                    TQ2_MMA_CLASS(false, c2, 0x00300030u, 0.0f);
+                    TQ2_MMA_CLASS(false, c3, 0x00C000C0u, 0.0f);
+                }
+                {
+                    const uint32_t w0 = wa.z, w1 = wb.z, s0 = w0 >> 8, s1 = w1 >> 8;
+                    const uint32_t b0 = xb.x, b1 = xb.y;
+                    TQ2_MMA_CLASS(false, c0, 0x00030003u, 0.0f);
+                    TQ2_MMA_CLASS(false, c1, 0x000C000Cu, 0.0f);
+                    TQ2_MMA_CLASS(false, c2, 0x00300030u, 0.0f);
+                    TQ2_MMA_CLASS(false, c3, 0x00C000C0u, 0.0f);
+                }
+                {
+                    const uint32_t w0 = wa.w, w1 = wb.w, s0 = w0 >> 8, s1 = w1 >> 8;
+                    const uint32_t b0 = xb.z, b1 = xb.w;
+                    TQ2_MMA_CLASS(false, c0, 0x00030003u, 0.0f);
+                    TQ2_MMA_CLASS(false, c1, 0x000C000Cu, 0.0f);
+                    TQ2_MMA_CLASS(false, c2, 0x00300030u, 0.0f);
+                    TQ2_MMA_CLASS(false, c3, 0x00C000C0u, 0.0f);
                 }
                 acc[0][0] = fmaf(dg, c0[0], acc[0][0]);
                 acc[0][1] = fmaf(dg8, c0[2], acc[0][1]);
@@ -399,10 +622,24 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 acc[2][1] = fmaf(dg8, c2[2], acc[2][1]);
                 acc[3][0] = fmaf(dg, c3[1], acc[3][0]);
                 acc[3][1] = fmaf(dg8, c3[3], acc[3][1]);
+                bl += kConsumerWarps;
+                while (bl >= nbk) {
+                    bl -= nbk;
+                    ++j;
+                }
+            }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+        }
+        if (++kc == p.n_kc) {
+            kc = 0;
+            rg0 += p.rg_s;
+        }
     }
     if (cur_rg >= 0) flush(cur_rg);
     consumer_barrier();
@@ -427,18 +664,22 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 // ------------------------------------------------------------------ host side
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Shared-memory plan for G CTAs; returns false if it cannot fit.
-bool make_plan(int M, int64_t N, int64_t K, int G, MmaParams &p)
+// Shared-memory plan for G CTAs within max_dyn bytes of dynamic shared
+// memory; returns false if it cannot fit.
+bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaParams &p)
 {
+    const int kMaxSmem = max_dyn;
     const int64_t B = K / 256;
     if (B > (1 << 20)) return false;
     p.G = G;
     p.B = (int)B;
-    if (B >= kChunkBlocks) {
+    if (B > kChunkBlocks) {  // 16 rows x 4096 codes per stage, 2-D tensor boxes
+        p.tma2d = 1;
         p.nbk_full = kChunkBlocks;
         p.n_kc = (int)((B + kChunkBlocks - 1) / kChunkBlocks);
         p.rg_s = 1;
-    } else {
+    } else {                 // whole rows, contiguous: 1-D bulk copies
+        p.tma2d = 0;
         p.nbk_full = (int)B;
         p.n_kc = 1;
         p.rg_s = kChunkBlocks / (int)B;
@@ -446,9 +687,7 @@ bool make_plan(int M, int64_t N, int64_t K, int G, MmaParams &p)
     const int64_t max_rows = (N + G - 1) / G;
     p.max_rg = (int)((max_rows + 15) / 16);
     if (p.rg_s > p.max_rg) p.rg_s = p.max_rg;
-    // row stride = nbk*64 (+64 when nbk is even) keeps rows g, g+1 64 bytes
-    // apart modulo 128 -> conflict-free 16-byte fragment loads
-    p.rb = p.nbk_full * 64 + ((p.nbk_full % 2 == 0) ? 64 : 0);
+    p.rb = p.nbk_full * 64;  // dense rows, as TMA writes them
     p.stage_bytes = p.rg_s * 16 * p.rb;
     p.dstr = (int)B + 1;
     int off = 0;
@@ -477,24 +716,93 @@ bool make_plan(int M, int64_t N, int64_t K, int G, MmaParams &p)
     return p.smem_total <= kMaxSmem;
 }
 
-std::atomic<int> g_smem_attr_set[2][64];
+// Largest dynamic shared memory the kernel for kM may use on `device`
+// (the per-block opt-in limit minus the kernel's static shared memory);
+// the kernel attribute is raised to it once per device.  0 on failure.
+std::atomic<int> g_max_dyn[2][64];
+
+template <int kM>
+int max_dynamic_smem(int device)
+{
+    if (device < 0 || device >= 64) return 0;
+    int v = g_max_dyn[kM - 1][device].load();
+    if (v > 0) return v;
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, matvec_mma_kernel<kM>) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    v = optin - (int)fa.sharedSizeBytes;
+    if (cudaFuncSetAttribute(matvec_mma_kernel<kM>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_max_dyn[kM - 1][device].store(v);
+    return v;
+}
+
+// Grid and plan: one CTA per SM while the per-CTA share fits, more CTAs otherwise.
+bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaParams &p)
+{
+    if (max_dyn <= 0) return false;
+    int G = (int)((N < (int64_t)sm_count(device)) ? N : sm_count(device));
+    while (!make_plan(M, N, K, G, max_dyn, p)) {
+        if (G >= N) return false;
+        G = (int)((2 * (int64_t)G < N) ? 2 * G : N);
+    }
+    return true;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load();
+    if (f) return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    fn.store(f);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// qs as uint64 [N][K/32]; boxes 128 x {16, 8, 4, 2, 1}
+cudaError_t encode_qs_maps(const MatvecArgs &a, MmaParams &p)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int i = 0; i < 5; ++i) {
+        const cuuint32_t box[2] = {128, (cuuint32_t)(16 >> i)};
+        CUresult r = enc(&p.tmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.qs), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
 
 template <int kM>
 cudaError_t launch_impl(const MatvecArgs &a, int device)
 {
     MmaParams p{};
     p.a = a;
-    int G = (int)((a.N < (int64_t)sm_count(device)) ? a.N : sm_count(device));
-    while (!make_plan(kM, a.N, a.K, G, p)) {
-        if (G >= a.N) return cudaErrorInvalidConfiguration;
-        G = (int)((2 * (int64_t)G < a.N) ? 2 * G : a.N);
+    if (!plan_for(kM, a.N, a.K, device, max_dynamic_smem<kM>(device), p))
+        return cudaErrorInvalidConfiguration;
+    if (p.tma2d) {
+        cudaError_t e = encode_qs_maps(a, p);
+        if (e != cudaSuccess) return e;
     }
     auto kern = matvec_mma_kernel<kM>;
-    if (device >= 0 && device < 64 && !g_smem_attr_set[kM - 1][device].load()) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-        if (e != cudaSuccess) return e;
-        g_smem_attr_set[kM - 1][device].store(1);
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.G);
     cfg.blockDim = dim3(kMmaThreads);
@@ -514,12 +822,8 @@ bool mma_matvec_supported(int M, int64_t N, int64_t K, int device)
 {
     if (M < 1 || M > 2 || N < 1 || K < 256) return false;
     MmaParams p{};
-    int G = (int)((N < (int64_t)sm_count(device)) ? N : sm_count(device));
-    while (!make_plan(M, N, K, G, p)) {
-        if (G >= N) return false;
-        G = (int)((2 * (int64_t)G < N) ? 2 * G : N);
-    }
-    return true;
+    const int max_dyn = (M == 1) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
+    return plan_for(M, N, K, device, max_dyn, p);
 }
 
 cudaError_t launch_matvec_mma(const MatvecArgs &a, int device)
