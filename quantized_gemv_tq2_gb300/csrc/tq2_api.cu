@@ -65,8 +65,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
     if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
-    if (impl < 0 || impl > 2) return TQ2_ERR_ARG;
-    if (impl == 1 && M > 2) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 3) return TQ2_ERR_ARG;
+    if ((impl == 1 || impl == 3) && M > 2) return TQ2_ERR_ARG;
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
     if (K > 0 && (x == nullptr || qs == nullptr || d == nullptr)) return TQ2_ERR_NULL;
@@ -95,16 +95,19 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;  // IEEE-correct division
     a.stream = s;
 
-    bool use_mma;
-    if (impl == 1) {
-        use_mma = true;
-        if (!tq2::mma_matvec_supported(a.M, N, K, dev)) return TQ2_ERR_ARG;
-    } else if (impl == 2) {
-        use_mma = false;
-    } else {
-        use_mma = tq2::mma_matvec_supported(a.M, N, K, dev);
-    }
-    cudaError_t e = use_mma ? tq2::launch_matvec_mma(a, dev) : tq2::launch_matvec_simt(a, dev);
+    // impl 0: mma.sync when the shape fits it, else CUDA cores.  The tcgen05
+    // kernel is correct but slower at M <= 2: a tcgen05.mma costs ~113 cycles
+    // per instruction at N <= 64, and a matvec gives each one only
+    // 128 rows x 16 codes (measured on GB300), so it is used only on request.
+    int which = impl;
+    if (impl == 0) which = tq2::mma_matvec_supported(a.M, N, K, dev) ? 1 : 2;
+    else if (impl == 1 && !tq2::mma_matvec_supported(a.M, N, K, dev))
+        return TQ2_ERR_ARG;
+    else if (impl == 3 && !tq2::tc05_matvec_supported(a.M, N, K, dev))
+        return TQ2_ERR_ARG;
+    cudaError_t e = (which == 3)   ? tq2::launch_matvec_tc05(a, dev)
+                    : (which == 1) ? tq2::launch_matvec_mma(a, dev)
+                                   : tq2::launch_matvec_simt(a, dev);
     if (e == cudaSuccess) e = cudaGetLastError();
     return from_cuda(e);
 }

@@ -30,6 +30,11 @@ struct MatvecArgs {
 bool mma_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_mma(const MatvecArgs &a, int device);
 
+// 5th-generation tensor-core path (tcgen05 MMA, A in tensor memory), M <= 2,
+// K a multiple of 512 with K / S <= 4096.  Returns false when unsupported.
+bool tc05_matvec_supported(int M, int64_t N, int64_t K, int device);
+cudaError_t launch_matvec_tc05(const MatvecArgs &a, int device);
+
 // CUDA-core path (fp32 FMA per code), any M in 1..16.
 cudaError_t launch_matvec_simt(const MatvecArgs &a, int device);
 
