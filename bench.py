@@ -349,6 +349,8 @@ def run_gpu(args):
         extras["shapes_m1"] = {k[0]: v for k, v in shapes.items()}
         simt = shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=2)
         extras["shapes_m1_cuda_core_impl"] = {k[0]: v for k, v in simt.items()}
+        pre = shape_graphs(torch, tq2, st, stream, M_list=(1, 2), impl=4)
+        extras["shapes_prescaled_impl"] = {f"{k[0]}_M{k[1]}": v for k, v in pre.items()}
         sweep = shape_graphs(torch, tq2, st, stream, M_list=(2, 4, 8, 16),
                              groups=("gateup_16384x4096", "down_4096x16384"))
         extras["m_sweep"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep.items()}

@@ -2,7 +2,9 @@
 // choice and launch on the caller's stream.  Every argument check happens
 // before any CUDA call, so invalid arguments return a status without touching
 // the device (these checks run even on a machine without a GPU).
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
@@ -23,6 +25,23 @@ int sm_count(int device)
         v = 148;
     g_sm_count[device].store(v, std::memory_order_relaxed);
     return v;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load();
+    if (f) return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    fn.store(f);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
 }  // namespace tq2
@@ -65,7 +84,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
     if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
-    if (impl < 0 || impl > 3) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 4) return TQ2_ERR_ARG;
     if ((impl == 1 || impl == 3) && M > 2) return TQ2_ERR_ARG;
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
@@ -95,18 +114,27 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;  // IEEE-correct division
     a.stream = s;
 
-    // impl 0: mma.sync when the shape fits it, else CUDA cores.  The tcgen05
-    // kernel is correct but slower at M <= 2: a tcgen05.mma costs ~113 cycles
-    // per instruction at N <= 64, and a matvec gives each one only
-    // 128 rows x 16 codes (measured on GB300), so it is used only on request.
+    // impl 0: for M <= 2 the class-column mma.sync kernel, for larger M (or
+    // when that kernel does not fit) the pre-scaled mma.sync kernel, CUDA
+    // cores as the last resort.  The tcgen05 kernel is correct but slower at
+    // M <= 2: a tcgen05.mma costs ~113 cycles per instruction at N <= 64, and
+    // a matvec gives each one only 128 rows x 16 codes (measured on GB300),
+    // so it is used only on request.
     int which = impl;
-    if (impl == 0) which = tq2::mma_matvec_supported(a.M, N, K, dev) ? 1 : 2;
-    else if (impl == 1 && !tq2::mma_matvec_supported(a.M, N, K, dev))
+    if (impl == 0) {
+        if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
+        else if (tq2::ps_matvec_supported(a.M, N, K, dev)) which = 4;
+        else which = 2;
+    } else if (impl == 1 && !tq2::mma_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
-    else if (impl == 3 && !tq2::tc05_matvec_supported(a.M, N, K, dev))
+    } else if (impl == 3 && !tq2::tc05_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
+    } else if (impl == 4 && !tq2::ps_matvec_supported(a.M, N, K, dev)) {
+        return TQ2_ERR_ARG;
+    }
     cudaError_t e = (which == 3)   ? tq2::launch_matvec_tc05(a, dev)
                     : (which == 1) ? tq2::launch_matvec_mma(a, dev)
+                    : (which == 4) ? tq2::launch_matvec_ps(a, dev)
                                    : tq2::launch_matvec_simt(a, dev);
     if (e == cudaSuccess) e = cudaGetLastError();
     return from_cuda(e);

@@ -2,7 +2,9 @@
 // units (layout kernels, the two matvec kernels, the C-ABI shim).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "../../include/tq2.h"
@@ -35,6 +37,12 @@ cudaError_t launch_matvec_mma(const MatvecArgs &a, int device);
 bool tc05_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_tc05(const MatvecArgs &a, int device);
 
+// Tensor-core path with pre-scaled x (all four code classes in one
+// accumulator, 8 activation rows per n-tile), M in 1..16.  Returns false
+// when the shape does not fit.
+bool ps_matvec_supported(int M, int64_t N, int64_t K, int device);
+cudaError_t launch_matvec_ps(const MatvecArgs &a, int device);
+
 // CUDA-core path (fp32 FMA per code), any M in 1..16.
 cudaError_t launch_matvec_simt(const MatvecArgs &a, int device);
 
@@ -48,5 +56,8 @@ cudaError_t launch_from_dense(const void *W, int w_f16, int64_t N, int64_t K, ui
 
 // Number of SMs of the current device (cached per device).
 int sm_count(int device);
+
+// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 }  // namespace tq2

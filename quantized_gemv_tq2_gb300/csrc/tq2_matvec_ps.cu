@@ -1,0 +1,653 @@
+// tq2_matvec_ps.cu -- tensor-core ternary matvec for M = 1..16 activation
+// rows with pre-scaled x (sm_103a).
+//
+// What it computes (BitCPM ternary page, linear-factoring paragraph):
+//   y[m][n] = sum_b d[n][b] * sum_{k in b} x'[m][k] * (q[n][k] - 1)
+//
+// The unpack is the one of the M <= 2 kernel: ANDing a packed 32-bit word
+// (16 codes of one row) with 0x00030003 << 2c leaves two fp16 lanes whose bit
+// patterns are q * 4^c, i.e. the exact values q * 2^(2c - 24); the same on the
+// word shifted right by 8 gives the other two bytes.  Here the B operand is
+// pre-scaled per class instead of giving each class its own accumulator:
+// B_c = x * 4^(3 - c), so every product is q * x * 2^-18 whatever the class,
+// and all four classes of a word accumulate into one MMA accumulator whose 8
+// columns are 8 activation rows (two n-tiles for M = 9..16).  The unpack cost
+// (one LOP3 per two codes) is then shared by all M rows.
+//
+// x * 64 is exact in fp16 while |x| <= 1023.5.  A block whose x reaches 1024
+// uses B_c = x * 4^-c instead (products q * x * 2^-24); the few low bits that
+// x / 64 can lose in the subnormal range are below 2^-19 per element, far
+// inside the tolerance of a block that holds a value >= 1024.  The block's
+// "-1" term (sum_k x_k) starts the accumulator; the result is scaled back by
+// the block's power of two and by d_b with one multiply each per lane.
+//
+// Data path per CTA (one CTA per SM, a contiguous range of output rows):
+//   * a producer warp streams the rows into a ring of 16 KB stages with TMA
+//     (whole rows in one 1-D bulk copy when K <= 4096, else 2-D boxes of
+//     16 rows x up to 4096 codes), before griddepcontrol.wait;
+//   * the d slice of the CTA's rows is staged to shared memory as fp32;
+//   * after griddepcontrol.wait, x is turned into B fragments in shared
+//     memory: all of K when it fits (stages then go row group by row group),
+//     else one K range at a time (stages go K range by K range, x is
+//     re-staged between ranges);
+//   * 8 consumer warps take (16-row group, 256-block) units of each stage and
+//     keep per-warp partials per row group; the partials are summed in a
+//     fixed order at the end (run-to-run deterministic).
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "tq2_device.cuh"
+#include "tq2_internal.cuh"
+
+namespace tq2 {
+namespace {
+
+using namespace dev;
+
+constexpr int kWarps = 8;                      // consumer warps
+constexpr int kConsumers = kWarps * 32;
+constexpr int kThreads = kConsumers + 32;      // + one producer warp
+constexpr int kMaxStages = 8;
+constexpr int kTwoPerSm = 112 * 1024;          // shared memory that lets two CTAs share an SM
+
+struct PsParams {
+    CUtensorMap tmap[5];  // qs as uint64 [N][K/32], boxes (kcb*8) x {16, 8, 4, 2, 1} rows
+    MatvecArgs a;
+    int G;        // CTAs
+    int B;        // 256-blocks along K
+    int NT;       // n-tiles of 8 activation rows
+    int kcb;      // 256-blocks per stage K range (<= 16)
+    int n_kc;     // K ranges
+    int xkc;      // K ranges per x chunk (all of them, or 1)
+    int R;        // 16-row groups per stage
+    int tma2d;    // 0: a stage is R*16 whole rows (n_kc == 1), one 1-D bulk copy
+    int rb;       // bytes per stage row in shared memory (kcb * 64)
+    int stage_bytes, stages;
+    int max_rg;   // row groups of the largest CTA
+    int dstr;     // floats per row of the d slice (B + 1: odd, conflict-free)
+    int xblocks;  // 256-blocks per x chunk (kcb * xkc)
+    int off_bar, off_red, off_dsm, off_xinfo, off_frag, off_ring, smem_total;
+};
+
+__device__ __forceinline__ void consumers_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+__device__ __forceinline__ void report_timeout(const PsParams &p, volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    if (p.a.status) atomicOr(p.a.status, TQ2_FLAG_TIMEOUT);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Byte offsets of one block's B fragments and per-column scalars.
+//   frag:  block bx (within the x chunk) holds 512*M bytes; n-tile nt starts
+//          at 4096*nt and has Mt = min(8, M - 8nt) columns; word slot jw
+//          (0..3) is a 128*Mt region; in it, (half h, quad t, column g) is a
+//          16-byte entry at (h*4*Mt + t*Mt + g)*16.  Half 0 holds classes 0, 1,
+//          half 1 classes 2, 3, each class as the (b0, b1) register pair.
+//   xinfo: float2 (C init, rescale) per (block, column), 8*NT columns a block.
+__device__ __forceinline__ uint32_t frag_off(int bx, int nt, int jw, int h, int t, int g, int M)
+{
+    const int Mt = min(8, M - 8 * nt);
+    return (uint32_t)(bx * 512 * M + nt * 4096 + jw * 128 * Mt + (h * 4 * Mt + t * Mt + g) * 16);
+}
+
+// Turn x (rows m, blocks [kb0, kb0 + nbx)) into B fragments and xinfo.
+// One warp per (block, row) pair; lane l takes the 8 codes' x values
+// 8l .. 8l+7 of the block.
+template <int NT>
+__device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uint32_t frag, float2 *xinfo,
+                                        int warp, int lane)
+{
+    const int M = p.a.M;
+    const int64_t K = p.a.K;
+    const bool prologue = p.a.act_scale != 0.0f;
+    const int h = lane & 1, w = lane >> 1;
+    constexpr int kBatch = 4;
+    const int npairs = nbx * M;
+    // pair index pr -> (m = pr / nbx, bx = pr - m * nbx), stepped without division
+    int m0 = 0, bx0 = warp;
+    while (bx0 >= nbx && m0 < M) {
+        bx0 -= nbx;
+        ++m0;
+    }
+    for (int pr0 = warp; pr0 < npairs; pr0 += kWarps * kBatch) {
+        uint4 v[kBatch];
+        int mm[kBatch], bb[kBatch];
+        int m = m0, bx = bx0;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            mm[i] = m;
+            bb[i] = bx;
+            if (m < M) {
+                const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(kb0 + bx) * 256 + 8 * lane;
+                v[i] = *reinterpret_cast<const uint4 *>(src);
+            }
+            bx += kWarps;
+            while (bx >= nbx && m < M) {
+                bx -= nbx;
+                ++m;
+            }
+        }
+        m0 = m;
+        bx0 = bx;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (mm[i] >= M) break;  // uniform over the warp
+            uint32_t r[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            if (prologue) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r[q]));
+                    const __half2 c2 = __floats2half2_rn(fq_code(f.x, p.a.inv_scale), fq_code(f.y, p.a.inv_scale));
+                    r[q] = *reinterpret_cast<const uint32_t *>(&c2);
+                }
+            }
+            float sum = 0.0f;
+            bool big = false;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r[q]));
+                sum += f.x + f.y;
+                big |= ((r[q] & 0x7FFFu) >= 0x6400u) || (((r[q] >> 16) & 0x7FFFu) >= 0x6400u);
+            }
+            big = __any_sync(0xffffffffu, big);
+            // class scales: positions 8h + (0,1 | 2,3 | 4,5 | 6,7) have classes (0,1 | 2,3 | 0,1 | 2,3)
+            const __half2 s01 = big ? __floats2half2_rn(1.0f, 0.25f) : __floats2half2_rn(64.0f, 16.0f);
+            const __half2 s23 = big ? __floats2half2_rn(0.0625f, 0.015625f) : __floats2half2_rn(4.0f, 1.0f);
+            uint32_t sv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __half2 prod = __hmul2(*reinterpret_cast<const __half2 *>(&r[q]), (q & 1) ? s23 : s01);
+                sv[q] = *reinterpret_cast<const uint32_t *>(&prod);
+            }
+            // this lane's two entries of each class: positions (8h + c, 8h + 4 + c)
+            uint32_t mine[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) mine[c] = __byte_perm(sv[c >> 1], sv[2 + (c >> 1)], (c & 1) ? 0x7632 : 0x5410);
+            // lane h = 0 writes classes 0, 1; lane h = 1 writes classes 2, 3
+            const uint32_t recv0 = __shfl_xor_sync(0xffffffffu, h ? mine[0] : mine[2], 1);
+            const uint32_t recv1 = __shfl_xor_sync(0xffffffffu, h ? mine[1] : mine[3], 1);
+            const uint32_t own0 = h ? mine[2] : mine[0], own1 = h ? mine[3] : mine[1];
+            const uint32_t lo0 = h ? recv0 : own0, hi0 = h ? own0 : recv0;
+            const uint32_t lo1 = h ? recv1 : own1, hi1 = h ? own1 : recv1;
+            const int mi = mm[i], nt = mi >> 3;
+            sts128(frag + frag_off(bb[i], nt, w & 3, h, w >> 2, mi & 7, M), __byte_perm(lo0, hi0, 0x5410),
+                   __byte_perm(lo0, hi0, 0x7632), __byte_perm(lo1, hi1, 0x5410), __byte_perm(lo1, hi1, 0x7632));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) {
+                const float sc = big ? 5.9604644775390625e-08f : 3.814697265625e-06f;  // 2^-24, 2^-18
+                const float rs = big ? 16777216.0f : 262144.0f;
+                xinfo[bb[i] * 8 * NT + mi] = make_float2(-sum * sc, rs);
+            }
+        }
+    }
+}
+
+// 16 HMMA of one (16-row group, 256-block) unit for n-tile nt: words jw of
+// rows g and g + 8 are (wa, wb); two accumulator chains, merged on return.
+__device__ __forceinline__ void unit_mma(float (&c)[4], const uint32_t (&wa)[4], const uint32_t (&wb)[4],
+                                         uint32_t fb, uint32_t jw_stride, float2 init)
+{
+    float ca[4] = {init.x, init.y, init.x, init.y};
+    float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int jw = 0; jw < 4; ++jw) {
+        const uint32_t w0 = wa[jw], w1 = wb[jw], s0 = w0 >> 8, s1 = w1 >> 8;
+        const uint4 f0 = lds128(fb + (uint32_t)jw * jw_stride);
+        const uint4 f1 = lds128(fb + (uint32_t)jw * jw_stride + 64u * (jw_stride >> 7));
+        float (&cc)[4] = (jw < 2) ? ca : cb;
+        mma_16816(cc, w0 & 0x00030003u, w1 & 0x00030003u, s0 & 0x00030003u, s1 & 0x00030003u, f0.x, f0.y);
+        mma_16816(cc, w0 & 0x000C000Cu, w1 & 0x000C000Cu, s0 & 0x000C000Cu, s1 & 0x000C000Cu, f0.z, f0.w);
+        mma_16816(cc, w0 & 0x00300030u, w1 & 0x00300030u, s0 & 0x00300030u, s1 & 0x00300030u, f1.x, f1.y);
+        mma_16816(cc, w0 & 0x00C000C0u, w1 & 0x00C000C0u, s0 & 0x00C000C0u, s1 & 0x00C000C0u, f1.z, f1.w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = ca[i] + cb[i];
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(const __grid_constant__ PsParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int abort_shared;
+    volatile int *abort_flag = &abort_shared;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int M = p.a.M;
+    const int64_t N = p.a.N, K = p.a.K;
+    const int64_t r0 = (int64_t)blockIdx.x * N / p.G;
+    const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / p.G;
+    const int nrows = (int)(r1 - r0);
+    const int nrg = (nrows + 15) >> 4;
+    const int n_rgs = (nrg + p.R - 1) / p.R;  // stage row steps
+    const int n_xc = (p.n_kc + p.xkc - 1) / p.xkc;
+    const int n_stages = n_rgs * p.n_kc;      // every (row step, K range) once
+    const int S = p.stages;
+    const int B = p.B;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // full[S], empty[S]
+    uint8_t *ring = smem + p.off_ring;
+
+    // Let the next kernel in the stream start its own weight prefetch.
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_addr(&bars[s]), 1);
+            mbar_init(smem_addr(&bars[S + s]), kWarps);
+        }
+        abort_shared = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ------------------------------------------------------ producer warp
+        // Stage order: x chunk, then row step, then K range within the chunk.
+        const uint64_t pol = evict_first_policy();
+        const int64_t row_bytes = K / 4;
+        int issued = 0;
+        int xc = 0, rgi = 0, kci = 0;
+        for (int s = 0; s < n_stages; ++s) {
+            const int slot = s % S;
+            const int round = s / S;
+            if (round > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[S + slot]), (round - 1) & 1))) {
+                if (lane == 0) report_timeout(p, abort_flag);
+                break;
+            }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            const int kc = xc * p.xkc + kci;
+            const int rg0 = rgi * p.R;
+            const int rows = min(p.R * 16, nrows - rg0 * 16);
+            const uint32_t full = smem_addr(&bars[slot]);
+            const uint32_t dst0 = smem_addr(ring + (size_t)slot * p.stage_bytes);
+            if (!p.tma2d) {
+                const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full, bytes);
+                    bulk_g2s(dst0, p.a.qs + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
+                }
+            } else {
+                // boxes of 16 rows x (kcb*64) bytes; the last group split into 8/4/2/1
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)rows * (uint32_t)p.rb);
+                __syncwarp();
+                const int x = kc * p.kcb * 8;
+                int roff = 0, box = 0;
+                while (roff + 16 <= rows) {
+                    if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[0], x, (int)(r0 + rg0 * 16 + roff), full, pol);
+                    roff += 16;
+                    ++box;
+                }
+#pragma unroll
+                for (int i = 1; i < 5; ++i) {
+                    const int hh = 16 >> i;
+                    if ((rows - roff) & hh) {
+                        if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[i], x, (int)(r0 + rg0 * 16 + roff), full, pol);
+                        roff += hh;
+                        ++box;
+                    }
+                }
+            }
+            __syncwarp();
+            issued = s + 1;
+            // advance (xc, rgi, kci)
+            const int xkc_here = min(p.xkc, p.n_kc - xc * p.xkc);
+            if (++kci == xkc_here) {
+                kci = 0;
+                if (++rgi == n_rgs) {
+                    rgi = 0;
+                    ++xc;
+                }
+            }
+        }
+        // No copy may still be writing shared memory when the CTA exits.
+        for (int slot = 0; slot < S && slot < issued; ++slot) {
+            const int last = slot + ((issued - 1 - slot) / S) * S;
+            if (!mbar_wait(smem_addr(&bars[slot]), (last / S) & 1) && lane == 0) report_timeout(p, abort_flag);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumer warps
+    float *red = reinterpret_cast<float *>(smem + p.off_red);  // [max_rg][8 warps][16 rows][M]
+    float *dsm = reinterpret_cast<float *>(smem + p.off_dsm);
+    float2 *xinfo = reinterpret_cast<float2 *>(smem + p.off_xinfo);
+    const uint32_t frag = smem_addr(smem + p.off_frag);
+    const bool prologue = p.a.act_scale != 0.0f;
+
+    for (int i = tid; i < nrg * kWarps * 16 * M; i += kConsumers) red[i] = 0.0f;
+    for (int i = tid; i < p.xblocks * 8 * NT; i += kConsumers) xinfo[i] = make_float2(0.0f, 0.0f);
+    {
+        const int nd = nrows * B;
+        const uint16_t *dsrc = p.a.d + r0 * B;
+        for (int base = 0; base < nd; base += kConsumers * 8) {
+            uint16_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kConsumers + tid;
+                v[j] = (i < nd) ? dsrc[i] : (uint16_t)0;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + j * kConsumers + tid;
+                if (i < nd) {
+                    const int r = i / B, b = i - r * B;
+                    dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
+                }
+            }
+        }
+    }
+
+    // x depends on the previous kernel in the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    consumers_sync();  // xinfo zeroed before it is written
+    stage_x<NT>(p, 0, min(p.xblocks, B), frag, xinfo, warp, lane);
+    consumers_sync();
+
+    const int g = lane >> 2, t = lane & 3;
+    int gsel[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) gsel[nt] = (8 * nt + g < M) ? g : 0;
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+    int cur_rg = -1;
+
+    auto flush = [&](int rg) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = 8 * nt + 2 * t;
+            float *rp = red + ((rg * kWarps + warp) * 16) * M;
+            if (col < M) {
+                rp[g * M + col] += acc[nt][0];
+                rp[(g + 8) * M + col] += acc[nt][2];
+            }
+            if (col + 1 < M) {
+                rp[g * M + col + 1] += acc[nt][1];
+                rp[(g + 8) * M + col + 1] += acc[nt][3];
+            }
+        }
+    };
+
+    const uint32_t ring_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
+    const uint32_t a_half = (uint32_t)(8 * p.rb);
+
+    int slot = 0, phase = 0;
+    int xc = 0, rgi = 0, kci = 0;
+    bool alive = true;
+    for (int s = 0; s < n_stages; ++s) {
+        if (s > 0 && kci == 0 && rgi == 0) {
+            // a new x chunk: every warp is done with the previous one
+            consumers_sync();
+            stage_x<NT>(p, xc * p.xblocks, min(p.xblocks, B - xc * p.xblocks), frag, xinfo, warp, lane);
+            consumers_sync();
+        }
+        bool ok = alive;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[slot]), (uint32_t)phase))) {
+            if (lane == 0) report_timeout(p, abort_flag);
+            ok = alive = false;
+        }
+        if (ok) {
+            const int kc = xc * p.xkc + kci;
+            const int rg0 = rgi * p.R;
+            const int Rs = min(p.R, nrg - rg0);
+            const int kb0 = kc * p.kcb;
+            const int nbk = min(p.kcb, B - kb0);
+            const int units = Rs * nbk;
+            const int kbx0 = kb0 - xc * p.xblocks;  // first block of this K range within the x chunk
+            const uint32_t st = ring_thr + (uint32_t)(slot * p.stage_bytes);
+            int j = 0, bl = warp;
+            while (bl >= nbk) {
+                bl -= nbk;
+                ++j;
+            }
+            for (int u = warp; u < units; u += kWarps) {
+                const int rg = rg0 + j;
+                if (rg != cur_rg) {
+                    if (cur_rg >= 0) flush(cur_rg);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+                    cur_rg = rg;
+                }
+                const uint32_t pa = st + (uint32_t)(j * 16 * p.rb + bl * 64);
+                const uint4 va = lds128(pa), vb = lds128(pa + a_half);
+                const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+                const int kb = kb0 + bl, bx = kbx0 + bl;
+                const float d0 = dsm[(rg * 16 + g) * p.dstr + kb];
+                const float d8 = dsm[(rg * 16 + g + 8) * p.dstr + kb];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int Mt = min(8, M - 8 * nt);
+                    const uint32_t fb = frag + frag_off(bx, nt, 0, 0, t, gsel[nt], M);
+                    const float4 xi = *reinterpret_cast<const float4 *>(&xinfo[bx * 8 * NT + 8 * nt + 2 * t]);
+                    float c[4];
+                    unit_mma(c, wa, wb, fb, (uint32_t)(128 * Mt), make_float2(xi.x, xi.z));
+                    acc[nt][0] = fmaf(c[0], xi.y * d0, acc[nt][0]);
+                    acc[nt][1] = fmaf(c[1], xi.w * d0, acc[nt][1]);
+                    acc[nt][2] = fmaf(c[2], xi.y * d8, acc[nt][2]);
+                    acc[nt][3] = fmaf(c[3], xi.w * d8, acc[nt][3]);
+                }
+                // next unit of this warp: u + 8
+                bl += kWarps;
+                while (bl >= nbk) {
+                    bl -= nbk;
+                    ++j;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+        }
+        const int xkc_here = min(p.xkc, p.n_kc - xc * p.xkc);
+        if (++kci == xkc_here) {
+            kci = 0;
+            if (++rgi == n_rgs) {
+                rgi = 0;
+                ++xc;
+            }
+        }
+    }
+    (void)n_xc;
+    if (cur_rg >= 0) flush(cur_rg);
+    consumers_sync();
+    if (*abort_flag) return;  // y is invalid; TQ2_FLAG_TIMEOUT was reported
+
+    // y[m][r0 + r] = sum over warps (fixed order) of the partials
+    for (int i = tid; i < M * nrows; i += kConsumers) {
+        const int m = i / nrows, r = i - m * nrows;
+        const int rg = r >> 4, ri = r & 15;
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += red[((rg * kWarps + w) * 16 + ri) * M + m];
+        if (prologue) s *= p.a.act_scale;
+        const int64_t o = (int64_t)m * N + r0 + r;
+        if (p.a.y_f16)
+            reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(s);
+        else
+            reinterpret_cast<float *>(p.a.y)[o] = s;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Shared-memory plan for G CTAs within `cap` bytes; false if it cannot fit.
+bool make_plan(int M, int64_t N, int64_t K, int G, int cap, bool resident, int kcb_try, PsParams &p)
+{
+    const int64_t B = K / 256;
+    if (B < 1 || B > (1 << 20)) return false;
+    p.G = G;
+    p.B = (int)B;
+    p.NT = (M + 7) / 8;
+    const int64_t max_rows = (N + G - 1) / G;
+    p.max_rg = (int)((max_rows + 15) / 16);
+    if (resident) {
+        if (B <= 16) {
+            p.kcb = (int)B;
+            p.n_kc = 1;
+            p.tma2d = 0;
+            p.R = 16 / (int)B;
+        } else {
+            p.kcb = 16;
+            p.n_kc = (int)((B + 15) / 16);
+            p.tma2d = 1;
+            p.R = 1;
+        }
+        p.xkc = p.n_kc;
+        p.xblocks = (int)B;
+    } else {
+        if (kcb_try > B) return false;
+        p.kcb = kcb_try;
+        p.n_kc = (int)((B + kcb_try - 1) / kcb_try);
+        p.tma2d = (p.n_kc > 1) ? 1 : 0;
+        p.R = 16 / kcb_try;
+        p.xkc = 1;
+        p.xblocks = kcb_try;
+    }
+    if (p.R > p.max_rg) p.R = p.max_rg;
+    p.rb = p.kcb * 64;
+    p.stage_bytes = p.R * 16 * p.rb;
+    p.dstr = (int)B + 1;
+    int64_t off = 0;
+    p.off_bar = 0;
+    off += 2 * kMaxStages * 8;
+    p.off_red = (int)off;
+    off += align_up(p.max_rg * kWarps * 16 * M * 4, 16);
+    p.off_dsm = (int)off;
+    off += (int64_t)p.max_rg * 16 * p.dstr * 4;
+    off = (off + 15) / 16 * 16;
+    p.off_xinfo = (int)off;
+    off += (int64_t)p.xblocks * 8 * p.NT * 8;
+    p.off_frag = (int)off;
+    off += (int64_t)p.xblocks * 512 * M;
+    off = (off + 127) / 128 * 128;
+    p.off_ring = (int)off;
+    if (off + 2 * (int64_t)p.stage_bytes > cap) return false;
+    int S = (int)((cap - off) / p.stage_bytes);
+    if (S > kMaxStages) S = kMaxStages;
+    p.stages = S;
+    p.smem_total = (int)off + S * p.stage_bytes;
+    return true;
+}
+
+std::atomic<int> g_max_dyn[2][64];
+
+template <int NT>
+int max_dynamic_smem(int device)
+{
+    if (device < 0 || device >= 64) return 0;
+    int v = g_max_dyn[NT - 1][device].load();
+    if (v > 0) return v;
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, matvec_ps_kernel<NT>) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    v = optin - (int)fa.sharedSizeBytes;
+    if (cudaFuncSetAttribute(matvec_ps_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_max_dyn[NT - 1][device].store(v);
+    return v;
+}
+
+// Prefer a plan that lets two CTAs share an SM (the next call's weights then
+// stream while this one computes), resident x before K-chunked x, and one CTA
+// per SM before more.
+bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
+{
+    const int max_dyn = (M <= 8) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
+    if (max_dyn <= 0 || M < 1 || M > 16) return false;
+    const int nsm = sm_count(device);
+    int G = (int)((N < (int64_t)nsm) ? N : nsm);
+    for (;;) {
+        for (int cap : {kTwoPerSm, max_dyn}) {
+            if (cap > max_dyn) continue;
+            if (make_plan(M, N, K, G, cap, true, 0, p)) return true;
+            for (int kcb : {16, 8, 4, 2, 1})
+                if (make_plan(M, N, K, G, cap, false, kcb, p)) return true;
+        }
+        if (G >= N) return false;
+        G = (int)((2 * (int64_t)G < N) ? 2 * G : N);
+    }
+}
+
+// qs as uint64 [N][K/32]; boxes (kcb*8) x {16, 8, 4, 2, 1}
+cudaError_t encode_maps(const MatvecArgs &a, PsParams &p)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int i = 0; i < 5; ++i) {
+        const cuuint32_t box[2] = {(cuuint32_t)(p.kcb * 8), (cuuint32_t)(16 >> i)};
+        CUresult r = enc(&p.tmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.qs), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+template <int NT>
+cudaError_t launch_impl(const MatvecArgs &a, int device)
+{
+    PsParams p{};
+    p.a = a;
+    if (!plan_for(a.M, a.N, a.K, device, p)) return cudaErrorInvalidConfiguration;
+    if (p.tma2d) {
+        cudaError_t e = encode_maps(a, p);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)p.smem_total;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, matvec_ps_kernel<NT>, p);
+}
+
+}  // namespace
+
+bool ps_matvec_supported(int M, int64_t N, int64_t K, int device)
+{
+    if (M < 1 || M > 16 || N < 1 || K < 256) return false;
+    PsParams p{};
+    return plan_for(M, N, K, device, p);
+}
+
+cudaError_t launch_matvec_ps(const MatvecArgs &a, int device)
+{
+    if (a.M >= 1 && a.M <= 8) return launch_impl<1>(a, device);
+    if (a.M >= 9 && a.M <= 16) return launch_impl<2>(a, device);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tq2

@@ -56,9 +56,11 @@ def test_matvec_rejects_bad_dtype_and_args(L):
     assert mv(L, s=-0.5) == ARG
     assert mv(L, s=float("nan")) == ARG
     assert mv(L, s=float("inf")) == ARG
-    assert mv(L, impl=4) == ARG
-    assert mv(L, impl=1, M=3) == ARG  # the tensor-core kernels take M <= 2
+    assert mv(L, impl=5) == ARG
+    assert mv(L, impl=-1) == ARG
+    assert mv(L, impl=1, M=3) == ARG  # the class-column tensor-core kernels take M <= 2
     assert mv(L, impl=3, M=3) == ARG
+    assert mv(L, impl=4, M=17) == SHAPE  # the pre-scaled kernel takes M <= 16, as the API
 
 
 def test_matvec_empty_shapes_are_noops(L):

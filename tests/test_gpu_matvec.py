@@ -11,7 +11,7 @@ from gpu_util import Case, assert_within_tolerance, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = {"auto": 0, "mma": 1, "simt": 2, "tc05": 3}
+IMPLS = {"auto": 0, "mma": 1, "simt": 2, "tc05": 3, "ps": 4}
 
 
 @pytest.fixture(scope="module")
@@ -31,7 +31,7 @@ def _run(T, case, impl, y_dtype=0, rows=None):
     try:
         y = tq2.matvec(x, qs, d, y_dtype=y_dtype, act_scale=case.s, status=st, impl=impl)
     except tq2.TQ2Error as e:
-        if e.status == 5 and impl in (1, 3):
+        if e.status == 5 and impl in (1, 3, 4):
             return None
         raise
     T.cuda.synchronize()
@@ -41,7 +41,7 @@ def _run(T, case, impl, y_dtype=0, rows=None):
 
 
 def _impls_for(M):
-    return ["auto", "tc05", "mma", "simt"] if M <= 2 else ["auto", "simt"]
+    return ["auto", "tc05", "mma", "ps", "simt"] if M <= 2 else ["auto", "ps", "simt"]
 
 
 # ---------------------------------------------------------------- small shapes, full compare
@@ -49,6 +49,7 @@ def _impls_for(M):
     (1, 32, 512),      # the PR1 shape
     (1, 1, 256), (1, 15, 256), (1, 17, 768), (2, 33, 1024), (1, 257, 4352),
     (2, 100, 8448), (3, 40, 512), (16, 70, 1280), (1, 300, 2048),
+    (5, 48, 8448), (9, 20, 768), (8, 17, 4352), (16, 50, 16384), (4, 100, 2048),
 ])
 @pytest.mark.parametrize("prologue", [False, True])
 def test_matvec_small_shapes(T, M, N, K, prologue):
@@ -88,7 +89,7 @@ def test_matvec_pr1_exhaustive(T):
         codes = oracle.unpack(qs, K).astype(np.float64)
         want = (np.repeat(d.astype(np.float64), 256, axis=1) * (codes - 1)).T  # [K, N]
         qd, dd = dev(qs), dev(d)
-        for impl, mstep in (("mma", 2), ("tc05", 2), ("simt", 16), ("auto", 1)):
+        for impl, mstep in (("mma", 2), ("tc05", 2), ("ps", 16), ("ps", 4), ("simt", 16), ("auto", 1)):
             for k0 in range(0, K, mstep):
                 x = np.zeros((mstep, K), dtype=np.float16)
                 for i in range(mstep):
@@ -101,7 +102,7 @@ def test_matvec_pr1_exhaustive(T):
         for seed in range(4):
             x = syn.activations(seed, 2, K)
             y_ref, tol = oracle.matvec(x, qs, d, K)
-            for impl in ("mma", "tc05", "simt"):
+            for impl in ("mma", "tc05", "ps", "simt"):
                 y = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl])).astype(np.float64)
                 assert_within_tolerance(y, y_ref, tol, f"exhaustive t={t} seed={seed} {impl}")
 
@@ -115,7 +116,7 @@ def test_matvec_one_hot_large_k(T):
         x = np.zeros((1, K), dtype=np.float16)
         x[0, k] = 1.0
         want = case.d[:, k // 256].astype(np.float64) * (case.codes[:, k].astype(np.float64) - 1)
-        for impl in ("mma", "tc05", "simt"):
+        for impl in ("mma", "tc05", "ps", "simt"):
             got = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl]))[0].astype(np.float64)
             assert np.array_equal(got, want), (impl, k)
 
@@ -131,7 +132,7 @@ def test_matvec_extreme_values(T):
     case.d[1, :] = np.float16(60000.0)
     case.d[2, 1] = 0
     y_ref, tol = case.reference()
-    for name in ("mma", "tc05", "simt"):
+    for name in ("mma", "tc05", "ps", "simt"):
         y = _run(T, case, IMPLS[name])
         assert_within_tolerance(y, y_ref, tol, name)
 
@@ -155,7 +156,7 @@ def test_matvec_is_deterministic(T):
     import quantized_gemv_tq2_gb300 as tq2
     case = Case(seed=21, M=2, N=1000, K=4096)
     x, qs, d = case.device()
-    for impl in (1, 2, 3):
+    for impl in (1, 2, 3, 4):
         first = host(tq2.matvec(x, qs, d, impl=impl))
         for _ in range(20):
             assert np.array_equal(host(tq2.matvec(x, qs, d, impl=impl)), first)
@@ -167,7 +168,7 @@ def test_matvec_is_deterministic(T):
 def test_matvec_qo_and_kv_full(T, seed, N):
     case = Case(seed=seed, M=1, N=N, K=4096)
     y_ref, tol = case.reference()
-    for name in ("auto", "tc05", "mma", "simt"):
+    for name in ("auto", "tc05", "mma", "ps", "simt"):
         assert_within_tolerance(_run(T, case, IMPLS[name]), y_ref, tol, f"{name} N={N}")
 
 
