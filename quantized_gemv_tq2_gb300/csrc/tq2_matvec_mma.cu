@@ -57,7 +57,10 @@ namespace {
 
 using namespace dev;
 
-constexpr int kConsumerWarps = 8;
+#ifndef TQ2_MMA_WARPS
+#define TQ2_MMA_WARPS 8
+#endif
+constexpr int kConsumerWarps = TQ2_MMA_WARPS;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kMmaThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kChunkBlocks = 16;                    // 256-blocks per stage row (4096 codes)
@@ -251,24 +254,28 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
           for (int j = 0; j < kXBatch; ++j) {
               const int L = base0 + j * kConsumerThreads + lane;
               if (L < total) {
-                  const int m = L / (B * 16);
+                  const int m = (kM == 2 && L >= B * 16) ? 1 : 0;  // kM <= 2: no division
                   const int rem = L - m * B * 16;
                   const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(rem >> 4) * 256 + (rem & 15) * 16;
                   xv[j][0] = *reinterpret_cast<const uint4 *>(src);
                   xv[j][1] = *reinterpret_cast<const uint4 *>(src + 8);
               }
           }
+          // per-thread partial sums of the batch first, then all four
+          // half-warp reductions together (their shuffle latencies overlap)
+          float sum[kXBatch];
+          int bm[kXBatch];
 #pragma unroll
           for (int j = 0; j < kXBatch; ++j) {
             const int L = base0 + j * kConsumerThreads + lane;
             const bool act = L < total;  // uniform over each half-warp (total % 16 == 0)
-            float sum = 0.0f;
-            int m = 0, b = 0, wib = 0;
+            sum[j] = 0.0f;
+            bm[j] = -1;
             if (act) {
-                m = L / (B * 16);
+                const int m = (kM == 2 && L >= B * 16) ? 1 : 0;
                 const int rem = L - m * B * 16;
-                b = rem >> 4;
-                wib = rem & 15;
+                const int b = rem >> 4, wib = rem & 15;
+                bm[j] = b * kM + m;
                 uint32_t raw[8] = {xv[j][0].x, xv[j][0].y, xv[j][0].z, xv[j][0].w,
                                    xv[j][1].x, xv[j][1].y, xv[j][1].z, xv[j][1].w};
                 if (prologue) {
@@ -280,11 +287,13 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                         raw[q] = *reinterpret_cast<const uint32_t *>(&h2);
                     }
                 }
+                float s2[2] = {0.0f, 0.0f};
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[q]));
-                    sum += f.x + f.y;
+                    s2[q & 1] += f.x + f.y;
                 }
+                sum[j] = s2[0] + s2[1];
                 const int t4 = wib >> 2, i4 = wib & 3;
                 const uint32_t dst = smem_addr(xs) + (uint32_t)(b * 512 * kM + (i4 >> 1) * (4 * kM * 64) +
                                                               t4 * 16 + (i4 & 1) * 8 + m * 4 * 64);
@@ -299,10 +308,15 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                                  : "memory");
                 }
             }
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (act && (lane & 15) == 0) xsum[b * kM + m] = sum;
           }
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) {
+#pragma unroll
+            for (int j = 0; j < kXBatch; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], off);
+          }
+#pragma unroll
+          for (int j = 0; j < kXBatch; ++j)
+            if (bm[j] >= 0 && (lane & 15) == 0) xsum[bm[j]] = sum[j];
         }
     }
     consumer_barrier();
@@ -363,7 +377,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
             const int kb0 = kc * p.nbk_full;
             const int nbk = min(p.nbk_full, B - kb0);
             const uint32_t st = a_thr + (uint32_t)(slot * p.stage_bytes);
-            if (nrg_s == 1 && nbk == 2 * kConsumerWarps) {
+            if (kConsumerWarps == 8 && nrg_s == 1 && nbk == 2 * kConsumerWarps) {
                 // Full 16-row x 16-block stage: this warp takes blocks warp and
                 // warp + 8 of row group rg0, computed together (8 independent
                 // MMA chains), straight-line.
