@@ -215,10 +215,13 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         red[(rg * kConsumerWarps + warp) * kM * 16 + rest] = 0.0f;
     }
     // d slice of this CTA's rows (contiguous in memory), fp32.  All loads of
-    // a batch are issued before the first store so their latencies overlap.
+    // a batch are issued before the first store so their latencies overlap;
+    // element i = tid + 256 j sits at (row, block) stepped without division.
     {
         const int nd = nrows * B;
         const uint16_t *dsrc = p.a.d + r0 * B;
+        const int q_step = kConsumerThreads / B, r_step = kConsumerThreads - q_step * B;
+        int r = tid / B, b = tid - (tid / B) * B;
         for (int base = 0; base < nd; base += kConsumerThreads * 8) {
             uint16_t v[8];
 #pragma unroll
@@ -229,9 +232,12 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = base + j * kConsumerThreads + tid;
-                if (i < nd) {
-                    const int r = i / B, b = i - r * B;
-                    dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
+                if (i < nd) dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
+                r += q_step;
+                b += r_step;
+                if (b >= B) {
+                    b -= B;
+                    ++r;
                 }
             }
         }
@@ -402,33 +408,37 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 const float dgB = lds_f32(pdB), dg8B = lds_f32(pdB + d_half);
                 const float xiA = -lds_f32(xs_thr + (uint32_t)kbA * (4u * kM)) * 5.9604644775390625e-08f;
                 const float xiB = -lds_f32(xs_thr + (uint32_t)kbB * (4u * kM)) * 5.9604644775390625e-08f;
-                float a0[4], a1[4], a2[4], a3[4], e0[4], e1[4], e2[4], e3[4];
-#define TQ2_WORD_PAIR(FIRST, WA_, WB_, B0_, B1_, C0_, C1_, C2_, C3_, XI_)          \
-    {                                                                          \
-        const uint32_t w0 = WA_, w1 = WB_, s0 = w0 >> 8, s1 = w1 >> 8;         \
-        const uint32_t b0 = B0_, b1 = B1_;                                     \
-        TQ2_MMA_CLASS(FIRST, C0_, 0x00030003u, XI_);                           \
-        TQ2_MMA_CLASS(FIRST, C1_, 0x000C000Cu, 0.0f);                          \
-        TQ2_MMA_CLASS(FIRST, C2_, 0x00300030u, 0.0f);                          \
-        TQ2_MMA_CLASS(FIRST, C3_, 0x00C000C0u, 0.0f);                          \
-    }
-                TQ2_WORD_PAIR(true, waA.x, wbA.x, xaA.x, xaA.y, a0, a1, a2, a3, xiA)
-                TQ2_WORD_PAIR(true, waB.x, wbB.x, xaB.x, xaB.y, e0, e1, e2, e3, xiB)
-                TQ2_WORD_PAIR(false, waA.y, wbA.y, xaA.z, xaA.w, a0, a1, a2, a3, 0.0f)
-                TQ2_WORD_PAIR(false, waB.y, wbB.y, xaB.z, xaB.w, e0, e1, e2, e3, 0.0f)
-                TQ2_WORD_PAIR(false, waA.z, wbA.z, xbA.x, xbA.y, a0, a1, a2, a3, 0.0f)
-                TQ2_WORD_PAIR(false, waB.z, wbB.z, xbB.x, xbB.y, e0, e1, e2, e3, 0.0f)
-                TQ2_WORD_PAIR(false, waA.w, wbA.w, xbA.z, xbA.w, a0, a1, a2, a3, 0.0f)
-                TQ2_WORD_PAIR(false, waB.w, wbB.w, xbB.z, xbB.w, e0, e1, e2, e3, 0.0f)
-#undef TQ2_WORD_PAIR
-                acc[0][0] = fmaf(dgB, e0[0], fmaf(dgA, a0[0], acc[0][0]));
-                acc[0][1] = fmaf(dg8B, e0[2], fmaf(dg8A, a0[2], acc[0][1]));
-                acc[1][0] = fmaf(dgB, e1[1], fmaf(dgA, a1[1], acc[1][0]));
-                acc[1][1] = fmaf(dg8B, e1[3], fmaf(dg8A, a1[3], acc[1][1]));
-                acc[2][0] = fmaf(dgB, e2[0], fmaf(dgA, a2[0], acc[2][0]));
-                acc[2][1] = fmaf(dg8B, e2[2], fmaf(dg8A, a2[2], acc[2][1]));
-                acc[3][0] = fmaf(dgB, e3[1], fmaf(dgA, a3[1], acc[3][0]));
-                acc[3][1] = fmaf(dg8B, e3[3], fmaf(dg8A, a3[3], acc[3][1]));
+                // Two units (blocks kbA, kbB), four class accumulators each,
+                // starting at zero; the "-1" of q - 1 is added below as
+                // d_b * (-X_b * 2^-24) to the class-0 sums.
+                const uint32_t W0[2][4] = {{waA.x, waA.y, waA.z, waA.w}, {waB.x, waB.y, waB.z, waB.w}};
+                const uint32_t W1[2][4] = {{wbA.x, wbA.y, wbA.z, wbA.w}, {wbB.x, wbB.y, wbB.z, wbB.w}};
+                const uint32_t BX[2][4][2] = {{{xaA.x, xaA.y}, {xaA.z, xaA.w}, {xbA.x, xbA.y}, {xbA.z, xbA.w}},
+                                              {{xaB.x, xaB.y}, {xaB.z, xaB.w}, {xbB.x, xbB.y}, {xbB.z, xbB.w}}};
+                float c[2][4][4];
+#pragma unroll
+                for (int jw = 0; jw < 4; ++jw) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t w0 = W0[u][jw], w1 = W1[u][jw], s0 = w0 >> 8, s1 = w1 >> 8;
+#pragma unroll
+                        for (int cl = 0; cl < 4; ++cl) {
+                            const uint32_t m = 0x00030003u << (2 * cl);
+                            if (jw == 0)
+                                mma_16816_zero(c[u][cl], w0 & m, w1 & m, s0 & m, s1 & m, BX[u][jw][0], BX[u][jw][1]);
+                            else
+                                mma_16816(c[u][cl], w0 & m, w1 & m, s0 & m, s1 & m, BX[u][jw][0], BX[u][jw][1]);
+                        }
+                    }
+                }
+                acc[0][0] = fmaf(dgB, c[1][0][0] + xiB, fmaf(dgA, c[0][0][0] + xiA, acc[0][0]));
+                acc[0][1] = fmaf(dg8B, c[1][0][2] + xiB, fmaf(dg8A, c[0][0][2] + xiA, acc[0][1]));
+                acc[1][0] = fmaf(dgB, c[1][1][1], fmaf(dgA, c[0][1][1], acc[1][0]));
+                acc[1][1] = fmaf(dg8B, c[1][1][3], fmaf(dg8A, c[0][1][3], acc[1][1]));
+                acc[2][0] = fmaf(dgB, c[1][2][0], fmaf(dgA, c[0][2][0], acc[2][0]));
+                acc[2][1] = fmaf(dg8B, c[1][2][2], fmaf(dg8A, c[0][2][2], acc[2][1]));
+                acc[3][0] = fmaf(dgB, c[1][3][1], fmaf(dgA, c[0][3][1], acc[3][0]));
+                acc[3][1] = fmaf(dg8B, c[1][3][3], fmaf(dg8A, c[0][3][3], acc[3][1]));
             } else {
             int j = 0, bl = warp;  // unit u = warp + 8 i  ->  (16-row group j, block bl)
             while (bl >= nbk) {
@@ -519,7 +529,8 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 
     // y[m][r0 + r] = sum over warps (fixed order) of the partials
     for (int i = tid; i < kM * nrows; i += kConsumerThreads) {
-        const int m = i / nrows, r = i - m * nrows;
+        const int m = (kM == 2 && i >= nrows) ? 1 : 0;  // kM <= 2: no division
+        const int r = i - m * nrows;
         const int rg = r >> 4, ri = r & 15;
         float s = 0.0f;
 #pragma unroll
