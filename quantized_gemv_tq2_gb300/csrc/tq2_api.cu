@@ -84,8 +84,9 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
     if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
-    if (impl < 0 || impl > 4) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 5) return TQ2_ERR_ARG;
     if ((impl == 1 || impl == 3) && M > 2) return TQ2_ERR_ARG;
+    if (impl == 5 && M > 1) return TQ2_ERR_ARG;
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
     if (K > 0 && (x == nullptr || qs == nullptr || d == nullptr)) return TQ2_ERR_NULL;
@@ -131,10 +132,13 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
         return TQ2_ERR_ARG;
     } else if (impl == 4 && !tq2::ps_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
+    } else if (impl == 5 && !tq2::dp4_matvec_supported(a.M, N, K, dev)) {
+        return TQ2_ERR_ARG;
     }
     cudaError_t e = (which == 3)   ? tq2::launch_matvec_tc05(a, dev)
                     : (which == 1) ? tq2::launch_matvec_mma(a, dev)
                     : (which == 4) ? tq2::launch_matvec_ps(a, dev)
+                    : (which == 5) ? tq2::launch_matvec_dp4(a, dev)
                                    : tq2::launch_matvec_simt(a, dev);
     if (e == cudaSuccess) e = cudaGetLastError();
     return from_cuda(e);

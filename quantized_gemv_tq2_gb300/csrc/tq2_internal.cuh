@@ -43,6 +43,11 @@ cudaError_t launch_matvec_tc05(const MatvecArgs &a, int device);
 bool ps_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_ps(const MatvecArgs &a, int device);
 
+// Integer-dot path (dp4a on x split into 8-bit pieces per 256-block), M = 1,
+// K <= 16384.  Returns false when the shape does not fit.
+bool dp4_matvec_supported(int M, int64_t N, int64_t K, int device);
+cudaError_t launch_matvec_dp4(const MatvecArgs &a, int device);
+
 // CUDA-core path (fp32 FMA per code), any M in 1..16.
 cudaError_t launch_matvec_simt(const MatvecArgs &a, int device);
 

@@ -56,7 +56,8 @@ def test_matvec_rejects_bad_dtype_and_args(L):
     assert mv(L, s=-0.5) == ARG
     assert mv(L, s=float("nan")) == ARG
     assert mv(L, s=float("inf")) == ARG
-    assert mv(L, impl=5) == ARG
+    assert mv(L, impl=6) == ARG
+    assert mv(L, impl=5, M=2) == ARG  # the dp4a kernel takes M = 1
     assert mv(L, impl=-1) == ARG
     assert mv(L, impl=1, M=3) == ARG  # the class-column tensor-core kernels take M <= 2
     assert mv(L, impl=3, M=3) == ARG
