@@ -50,6 +50,24 @@ def stack_linears():
 STACK_BYTES = sum(linear_bytes(1, N, K) for _, _, N, K in stack_linears())
 
 
+def max_over_ranks(value, device=None):
+    """The largest `value` over all ranks of the default process group (the
+    value itself when no group is initialised): the slowest replica sets the
+    step time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world, bytes_per_step, ms_per_step):
+    """Whole-job throughput: every replica streams bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def _peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -305,11 +323,7 @@ def run_gpu(args):
         time_graph(torch, g, stream, max(1, int(1.0 / max(soak * 1e-3, 1e-6))), 0)
     ms = time_graph(torch, g, stream, args.steps, args.warmup, barrier)
     clocks = sampler.stop() if not args.no_clocks else {"skipped": True}
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     # e2e: pinned host x -> device, the step, device y -> pinned host, every step
     e2e_steps = max(3, min(args.steps, 300))
@@ -332,11 +346,7 @@ def run_gpu(args):
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     extras = {}
     if not args.quick and rank == 0:
@@ -356,7 +366,7 @@ def run_gpu(args):
         extras["m_sweep"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep.items()}
 
     peak, peak_src = _peak()
-    value = world * STACK_BYTES / (ms * 1e-3) / 1e9
+    value = job_gbs(world, STACK_BYTES, ms)
     per_gpu = STACK_BYTES / (ms * 1e-3) / 1e9
     if rank != 0:
         return
@@ -398,7 +408,7 @@ def run_gpu(args):
                           f"avg launch time {1e3 * ms / launches_per_step:.3f} us",
         },
         "e2e": {
-            "value": round(world * STACK_BYTES / (e2e_ms * 1e-3) / 1e9, 2),
+            "value": round(job_gbs(world, STACK_BYTES, e2e_ms), 2),
             "unit": "GB/s",
             "ms_per_step": round(e2e_ms, 5),
             "h2d_bytes_per_step": st["X"].numel() * 2,
