@@ -191,6 +191,40 @@ def stack_calls(st, prologue=False, impl=0):
     return calls
 
 
+def grouped_stack(st):
+    """The stack as a decoder would run it with shared inputs: per layer
+    q,k,v as one tq2_matvec_grouped call on q's x, o, gate,up as one grouped
+    call on gate's x, down -- 4 launches per layer.  Returns (calls, bytes):
+    each call is (x view, [qs], [d], [y views]); bytes count x once per call."""
+    calls, nbytes = [], 0
+    lin = st["lin"]
+    i = 0
+    while i < len(lin):
+        name = lin[i][1]
+        n = 3 if name == "q" else (2 if name == "gate" else 1)  # q,k,v / gate,up / single
+        idx = list(range(i, i + n))
+        K = lin[i][3]
+        x = st["X"][st["x_off"][i]:st["x_off"][i] + K].view(1, K)
+        ys = [st["Y"][st["y_off"][j]:st["y_off"][j] + lin[j][2]].view(1, lin[j][2]) for j in idx]
+        calls.append((x, [st["qs"][j] for j in idx], [st["d"][j] for j in idx], ys))
+        nbytes += 2 * K + sum(linear_bytes(1, lin[j][2], K) - 2 * K for j in idx)
+        i += len(idx)
+    return calls, nbytes
+
+
+def capture_grouped(torch, tq2, calls, stream):
+    with torch.cuda.stream(stream):
+        for x, qs, d, ys in calls:  # eager warm-up
+            tq2.matvec_grouped(x, qs, d, y_list=ys)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for x, qs, d, ys in calls:
+                tq2.matvec_grouped(x, qs, d, y_list=ys)
+    stream.synchronize()
+    return g
+
+
 def time_graph(torch, g, stream, steps, warmup, barrier=None):
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -355,6 +389,15 @@ def run_gpu(args):
         extras["stack_with_prologue"] = dict(ms_per_step=ms_p, gbs=STACK_BYTES / (ms_p * 1e-3) / 1e9,
                                              tok_s=1e3 / ms_p)
         del gp
+        gcalls, gbytes = grouped_stack(st)
+        gg = capture_grouped(torch, tq2, gcalls, stream)
+        ms_g = time_graph(torch, gg, stream, max(3, min(args.steps, 2000)), 5)
+        extras["stack_grouped"] = dict(
+            ms_per_step=ms_g, gbs=gbytes / (ms_g * 1e-3) / 1e9, tok_s=1e3 / ms_g,
+            launches_per_step=len(gcalls), bytes_per_step=gbytes,
+            how="per layer q,k,v as one tq2_matvec_grouped launch on a shared x, o, gate,up as one "
+                "grouped launch on a shared x, down: 4 launches per layer, the same 224 weight sets")
+        del gg
         shapes = shape_graphs(torch, tq2, st, stream, M_list=(1,))
         extras["shapes_m1"] = {k[0]: v for k, v in shapes.items()}
         simt = shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=2)

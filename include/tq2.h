@@ -137,6 +137,37 @@ TQ2_API tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, c
                       void *workspace, size_t workspace_bytes, uint32_t *d_status,
                       tq2_stream_t stream);
 
+/* Largest number of weight matrices in one tq2_matvec_grouped call. */
+#define TQ2_MAX_GROUP 4
+
+/*
+ * tq2_matvec_grouped -- several matvecs that share x and K (in a decoder
+ * layer: q, k and v of the attention input; gate and up of the MLP input),
+ * BitCPM ternary page, linear-factoring paragraph, applied to each matrix:
+ *   y_j[m][n] = sum_b d_j[n][b] * sum_{k in b} x'[m][k] * (q_j[n][k] - 1).
+ *
+ *   x          device, fp16 [M, K] row-major, 16-byte aligned, read only.
+ *   M, K       as tq2_matvec (M in 0..16, K % 256 == 0).
+ *   n_mats     1 .. TQ2_MAX_GROUP.
+ *   qs, d, N, y  HOST arrays of n_mats entries (read during the call, not
+ *              kept): device pointers to qs_j [N_j, K/4] (16-byte aligned),
+ *              d_j [N_j, K/256] fp16, y_j [M, N_j] (y_dtype; 4- or 2-byte
+ *              aligned), and the row counts N_j >= 0 (N_j = 0: y_j untouched).
+ *   y_dtype, act_scale, d_status, stream  as tq2_matvec (one act_scale for
+ *              the shared x).
+ *
+ * Results equal n_mats tq2_matvec calls with the same x; when M <= 2 and
+ * K <= 4096 they run as ONE kernel launch (the CTAs split between the
+ * matrices in proportion to their rows; x staged and the wait on the previous
+ * kernel paid once), otherwise as consecutive calls on the stream.  Errors:
+ * as tq2_matvec for every matrix (checked before anything is enqueued);
+ * TQ2_ERR_ARG for n_mats out of range; TQ2_ERR_NULL for a NULL array.
+ */
+TQ2_API tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats,
+                                      const uint8_t *const *qs, const uint16_t *const *d,
+                                      const int64_t *N, void *const *y, tq2_dtype y_dtype,
+                                      float act_scale, uint32_t *d_status, tq2_stream_t stream);
+
 /* Bytes of workspace tq2_matvec needs for this shape (0 for every shape today). */
 TQ2_API size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K);
 

@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "TQ2Error", "lib", "load", "declared_symbols",
-    "pack", "unpack", "from_dense", "matvec", "matvec_workspace_size",
+    "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "matvec_workspace_size",
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_TC05", "IMPL_PS", "IMPL_DP4",
@@ -62,6 +62,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_from_dense.argtypes = [P, I32, I64, I64, P, P, P, P]
         L.tq2_matvec.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P]
         L.tq2_matvec_impl.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P, I32]
+        L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P]
         L.tq2_matvec_workspace_size.argtypes = [I64, I64, I64]
         L.tq2_matvec_workspace_size.restype = SZ
         L.tq2_status_string.argtypes = [I32]
@@ -70,7 +71,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_last_cuda_error.argtypes = []
         L.tq2_last_cuda_error.restype = ctypes.c_char_p
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
-                   "tq2_version"):
+                   "tq2_matvec_grouped", "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
         return L
@@ -200,6 +201,38 @@ def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, statu
                                _stream_ptr(stream), int(impl))
     _check(st, "tq2_matvec")
     return y
+
+
+def matvec_grouped(x, qs_list, d_list, y_list=None, y_dtype=None, act_scale: float = 0.0,
+                   status=None, stream=None):
+    """[y_j] = ternary matvecs of one shared x [M,K] with several packed
+    matrices (tq2_matvec_grouped): one launch when the library can group them."""
+    torch = _torch()
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    M, K = x.shape
+    n = len(qs_list)
+    if n != len(d_list) or (y_list is not None and len(y_list) != n):
+        raise ValueError("qs_list, d_list and y_list must have the same length")
+    if x.dtype != torch.float16 or any(d.dtype != torch.float16 for d in d_list) or \
+            any(q.dtype != torch.uint8 for q in qs_list):
+        raise TypeError("x and d must be float16, qs uint8")
+    if y_list is None:
+        dt = torch.float32 if (y_dtype in (None, F32, torch.float32)) else torch.float16
+        y_list = [torch.empty((M, q.shape[0]), dtype=dt, device=q.device) for q in qs_list]
+    ycode = F32 if y_list[0].dtype == torch.float32 else F16
+    _need_cuda(x, *qs_list, *d_list, *y_list, status)
+    Pn = ctypes.c_void_p * n
+    qa = Pn(*[_ptr(q).value for q in qs_list])
+    da = Pn(*[_ptr(d).value for d in d_list])
+    ya = Pn(*[_ptr(y).value for y in y_list])
+    na = (ctypes.c_int64 * n)(*[q.shape[0] for q in qs_list])
+    st = load().tq2_matvec_grouped(_ptr(x), M, K, n, ctypes.cast(qa, ctypes.c_void_p),
+                                   ctypes.cast(da, ctypes.c_void_p), ctypes.cast(na, ctypes.c_void_p),
+                                   ctypes.cast(ya, ctypes.c_void_p), ycode, float(act_scale),
+                                   _ptr(status), _stream_ptr(stream))
+    _check(st, "tq2_matvec_grouped")
+    return y_list
 
 
 def matvec_workspace_size(M: int, N: int, K: int) -> int:

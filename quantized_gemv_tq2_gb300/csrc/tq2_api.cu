@@ -203,6 +203,74 @@ tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, cons
     return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, d_status, stream, impl);
 }
 
+tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
+                              const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
+                              float act_scale, uint32_t *d_status, tq2_stream_t stream)
+{
+    if (n_mats < 1 || n_mats > TQ2_MAX_GROUP) return TQ2_ERR_ARG;
+    if (qs == nullptr || d == nullptr || N == nullptr || y == nullptr) return TQ2_ERR_NULL;
+    // every matrix must pass the checks of a single call (no CUDA call yet)
+    int live = 0;
+    for (int j = 0; j < n_mats; ++j) {
+        tq2_status st = check_nk(N[j], K);
+        if (st != TQ2_OK) return st;
+        if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
+        if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
+        if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
+        if (M == 0 || N[j] == 0) continue;
+        if (y[j] == nullptr) return TQ2_ERR_NULL;
+        if (K > 0 && (x == nullptr || qs[j] == nullptr || d[j] == nullptr)) return TQ2_ERR_NULL;
+        if (!aligned(x, 16) || !aligned(qs[j], 16) || !aligned(d[j], 2)) return TQ2_ERR_ALIGN;
+        if (!aligned(y[j], y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
+        ++live;
+    }
+    if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    if (live == 0) return TQ2_OK;
+
+    const uint8_t *gq[TQ2_MAX_GROUP];
+    const uint16_t *gd[TQ2_MAX_GROUP];
+    void *gy[TQ2_MAX_GROUP];
+    int64_t gn[TQ2_MAX_GROUP];
+    int n = 0;
+    for (int j = 0; j < n_mats; ++j) {
+        if (M == 0 || N[j] == 0) continue;
+        gq[n] = qs[j];
+        gd[n] = d[j];
+        gy[n] = y[j];
+        gn[n] = N[j];
+        ++n;
+    }
+    int dev = 0;
+    tq2_status st = TQ2_OK;
+    if (K > 0 && n > 1) {
+        if ((st = current_device(&dev)) != TQ2_OK) return st;
+        if (tq2::mma_group_supported((int)M, n, gn, K, dev)) {
+            tq2::MatvecArgs a;
+            a.x = x;
+            a.qs = nullptr;
+            a.d = nullptr;
+            a.y = nullptr;
+            a.status = d_status;
+            a.N = 0;
+            a.K = K;
+            a.M = (int)M;
+            a.y_f16 = (y_dtype == TQ2_F16);
+            a.act_scale = act_scale;
+            a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;
+            a.stream = reinterpret_cast<cudaStream_t>(stream);
+            cudaError_t e = tq2::launch_matvec_mma_group(a, n, gq, gd, gy, gn, dev);
+            if (e == cudaSuccess) e = cudaGetLastError();
+            return from_cuda(e);
+        }
+    }
+    // otherwise one call per matrix, same x, same stream
+    for (int j = 0; j < n; ++j) {
+        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, d_status, stream, 0);
+        if (st != TQ2_OK) return st;
+    }
+    return TQ2_OK;
+}
+
 size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K)
 {
     (void)M;

@@ -32,6 +32,13 @@ struct MatvecArgs {
 bool mma_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_mma(const MatvecArgs &a, int device);
 
+// The same kernel over a group of up to 4 weight matrices that share x (and
+// K <= 4096): one launch, CTAs split in proportion to the rows.  qs/d/y/N
+// are host arrays of n device pointers / row counts.
+bool mma_group_supported(int M, int n, const int64_t *N, int64_t K, int device);
+cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                                    void *const *y, const int64_t *N, int device);
+
 // 5th-generation tensor-core path (tcgen05 MMA, A in tensor memory), M <= 2,
 // K a multiple of 512 with K / S <= 4096.  Returns false when unsupported.
 bool tc05_matvec_supported(int M, int64_t N, int64_t K, int device);

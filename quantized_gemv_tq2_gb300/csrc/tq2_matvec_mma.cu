@@ -47,6 +47,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "tq2_device.cuh"
@@ -61,10 +62,23 @@ using namespace dev;
 #define TQ2_MMA_WARPS 8
 #endif
 constexpr int kConsumerWarps = TQ2_MMA_WARPS;
+constexpr int kUpw = 16 / kConsumerWarps;           // fast path: 256-blocks per warp and stage
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kMmaThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kChunkBlocks = 16;                    // 256-blocks per stage row (4096 codes)
 constexpr int kTargetSmem = 112 * 1024;             // two CTAs per SM (PDL overlap)
+
+// One weight matrix of a launch.  A single call has one; a grouped call
+// (several matrices sharing x, K <= 4096) gives each matrix a contiguous range
+// of CTAs [g0, g0 + G) in proportion to its rows.
+constexpr int kMaxGroup = 4;
+struct GroupMat {
+    const uint8_t *qs;   // [N, K/4]
+    const uint16_t *d;   // [N, K/256]
+    void *y;             // [M, N]
+    int64_t N;
+    int g0, G;
+};
 
 struct MmaParams {
     // K > 4096 only: qs as a 2-D tensor of uint64 [N][K/32], boxes of
@@ -83,6 +97,8 @@ struct MmaParams {
     int max_rg;      // 16-row groups per CTA (max)
     int dstr;        // fp32 stride of the d slice rows (B + 1, odd)
     int off_bar, off_red, off_dsm, off_xsum, off_xs, off_ring, smem_total;
+    int n_mats;
+    GroupMat mats[kMaxGroup];
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -116,9 +132,16 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
     volatile int *abort_flag = &abort_shared;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t N = p.a.N, K = p.a.K;
-    const int64_t r0 = (int64_t)blockIdx.x * N / p.G;
-    const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / p.G;
+    // this CTA's matrix and rows
+    int mi = 0;
+    while (mi + 1 < p.n_mats && (int)blockIdx.x >= p.mats[mi + 1].g0) ++mi;
+    const uint8_t *const qs_g = p.mats[mi].qs;
+    const uint16_t *const d_g = p.mats[mi].d;
+    void *const y_g = p.mats[mi].y;
+    const int64_t N = p.mats[mi].N, K = p.a.K;
+    const int cta = (int)blockIdx.x - p.mats[mi].g0, G_m = p.mats[mi].G;
+    const int64_t r0 = (int64_t)cta * N / G_m;
+    const int64_t r1 = (int64_t)(cta + 1) * N / G_m;
     const int nrows = (int)(r1 - r0);
     const int nrg = (nrows + 15) >> 4;
     const int n_stages = ((nrg + p.rg_s - 1) / p.rg_s) * p.n_kc;
@@ -165,7 +188,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full, bytes);
-                    bulk_g2s(dst0, p.a.qs + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
+                    bulk_g2s(dst0, qs_g + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
                 }
             } else {
                 // 16 rows x 1024 bytes (columns past the row end read as zero);
@@ -219,7 +242,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
     // element i = tid + 256 j sits at (row, block) stepped without division.
     {
         const int nd = nrows * B;
-        const uint16_t *dsrc = p.a.d + r0 * B;
+        const uint16_t *dsrc = d_g + r0 * B;
         const int q_step = kConsumerThreads / B, r_step = kConsumerThreads - q_step * B;
         int r = tid / B, b = tid - (tid / B) * B;
         for (int base = 0; base < nd; base += kConsumerThreads * 8) {
@@ -252,7 +275,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
     {
         // 16-code words of x; a thread takes words L = base0 + j*256 + lane
         // (j < 4) and issues the loads of all four before using any.
-        constexpr int kXBatch = 4;
+        constexpr int kXBatch = (kConsumerWarps >= 16) ? 2 : 4;
         const int total = kM * B * 16;
         for (int base0 = warp * 32; base0 < total; base0 += kConsumerThreads * kXBatch) {
           uint4 xv[kXBatch][2];
@@ -383,10 +406,10 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
             const int kb0 = kc * p.nbk_full;
             const int nbk = min(p.nbk_full, B - kb0);
             const uint32_t st = a_thr + (uint32_t)(slot * p.stage_bytes);
-            if (kConsumerWarps == 8 && nrg_s == 1 && nbk == 2 * kConsumerWarps) {
-                // Full 16-row x 16-block stage: this warp takes blocks warp and
-                // warp + 8 of row group rg0, computed together (8 independent
-                // MMA chains), straight-line.
+            if (nrg_s == 1 && nbk == kUpw * kConsumerWarps) {
+                // Full 16-row x 16-block stage: this warp takes blocks
+                // warp + u * kConsumerWarps (u < kUpw) of row group rg0,
+                // computed together (4 * kUpw independent MMA chains).
                 const int rg = rg0;
                 if (rg != cur_rg) {
                     if (cur_rg >= 0) flush(cur_rg);
@@ -394,32 +417,31 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                     for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = 0.0f;
                     cur_rg = rg;
                 }
-                const int kbA = kb0 + warp, kbB = kbA + kConsumerWarps;
-                const uint32_t paA = st + (uint32_t)(warp * 64);
-                const uint32_t paB = paA + (uint32_t)(kConsumerWarps * 64);
-                const uint4 waA = lds128(paA), wbA = lds128(paA + a_half);
-                const uint4 waB = lds128(paB), wbB = lds128(paB + a_half);
-                const uint32_t pxA = x_thr + (uint32_t)kbA * x_blk, pxB = x_thr + (uint32_t)kbB * x_blk;
-                const uint4 xaA = lds128(pxA), xbA = lds128(pxA + x_half);
-                const uint4 xaB = lds128(pxB), xbB = lds128(pxB + x_half);
-                const uint32_t pdA = d_thr + (uint32_t)rg * rg_stride_d + (uint32_t)kbA * 4u;
-                const uint32_t pdB = pdA + (uint32_t)(kConsumerWarps * 4);
-                const float dgA = lds_f32(pdA), dg8A = lds_f32(pdA + d_half);
-                const float dgB = lds_f32(pdB), dg8B = lds_f32(pdB + d_half);
-                const float xiA = -lds_f32(xs_thr + (uint32_t)kbA * (4u * kM)) * 5.9604644775390625e-08f;
-                const float xiB = -lds_f32(xs_thr + (uint32_t)kbB * (4u * kM)) * 5.9604644775390625e-08f;
-                // Two units (blocks kbA, kbB), four class accumulators each,
-                // starting at zero; the "-1" of q - 1 is added below as
-                // d_b * (-X_b * 2^-24) to the class-0 sums.
-                const uint32_t W0[2][4] = {{waA.x, waA.y, waA.z, waA.w}, {waB.x, waB.y, waB.z, waB.w}};
-                const uint32_t W1[2][4] = {{wbA.x, wbA.y, wbA.z, wbA.w}, {wbB.x, wbB.y, wbB.z, wbB.w}};
-                const uint32_t BX[2][4][2] = {{{xaA.x, xaA.y}, {xaA.z, xaA.w}, {xbA.x, xbA.y}, {xbA.z, xbA.w}},
-                                              {{xaB.x, xaB.y}, {xaB.z, xaB.w}, {xbB.x, xbB.y}, {xbB.z, xbB.w}}};
-                float c[2][4][4];
+                uint32_t W0[kUpw][4], W1[kUpw][4], BX[kUpw][4][2];
+                float dg[kUpw], dg8[kUpw], xi[kUpw];
+#pragma unroll
+                for (int u = 0; u < kUpw; ++u) {
+                    const int kb = kb0 + warp + u * kConsumerWarps;
+                    const uint32_t pa = st + (uint32_t)((warp + u * kConsumerWarps) * 64);
+                    const uint4 wa = lds128(pa), wb = lds128(pa + a_half);
+                    const uint32_t px = x_thr + (uint32_t)kb * x_blk;
+                    const uint4 xa = lds128(px), xb = lds128(px + x_half);
+                    const uint32_t pd = d_thr + (uint32_t)rg * rg_stride_d + (uint32_t)kb * 4u;
+                    dg[u] = lds_f32(pd);
+                    dg8[u] = lds_f32(pd + d_half);
+                    xi[u] = -lds_f32(xs_thr + (uint32_t)kb * (4u * kM)) * 5.9604644775390625e-08f;
+                    W0[u][0] = wa.x; W0[u][1] = wa.y; W0[u][2] = wa.z; W0[u][3] = wa.w;
+                    W1[u][0] = wb.x; W1[u][1] = wb.y; W1[u][2] = wb.z; W1[u][3] = wb.w;
+                    BX[u][0][0] = xa.x; BX[u][0][1] = xa.y; BX[u][1][0] = xa.z; BX[u][1][1] = xa.w;
+                    BX[u][2][0] = xb.x; BX[u][2][1] = xb.y; BX[u][3][0] = xb.z; BX[u][3][1] = xb.w;
+                }
+                // four class accumulators per unit, starting at zero; the "-1"
+                // of q - 1 is added below as d_b * (-X_b * 2^-24) to class 0
+                float c[kUpw][4][4];
 #pragma unroll
                 for (int jw = 0; jw < 4; ++jw) {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
+                    for (int u = 0; u < kUpw; ++u) {
                         const uint32_t w0 = W0[u][jw], w1 = W1[u][jw], s0 = w0 >> 8, s1 = w1 >> 8;
 #pragma unroll
                         for (int cl = 0; cl < 4; ++cl) {
@@ -431,14 +453,17 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                         }
                     }
                 }
-                acc[0][0] = fmaf(dgB, c[1][0][0] + xiB, fmaf(dgA, c[0][0][0] + xiA, acc[0][0]));
-                acc[0][1] = fmaf(dg8B, c[1][0][2] + xiB, fmaf(dg8A, c[0][0][2] + xiA, acc[0][1]));
-                acc[1][0] = fmaf(dgB, c[1][1][1], fmaf(dgA, c[0][1][1], acc[1][0]));
-                acc[1][1] = fmaf(dg8B, c[1][1][3], fmaf(dg8A, c[0][1][3], acc[1][1]));
-                acc[2][0] = fmaf(dgB, c[1][2][0], fmaf(dgA, c[0][2][0], acc[2][0]));
-                acc[2][1] = fmaf(dg8B, c[1][2][2], fmaf(dg8A, c[0][2][2], acc[2][1]));
-                acc[3][0] = fmaf(dgB, c[1][3][1], fmaf(dgA, c[0][3][1], acc[3][0]));
-                acc[3][1] = fmaf(dg8B, c[1][3][3], fmaf(dg8A, c[0][3][3], acc[3][1]));
+#pragma unroll
+                for (int u = 0; u < kUpw; ++u) {
+                    acc[0][0] = fmaf(dg[u], c[u][0][0] + xi[u], acc[0][0]);
+                    acc[0][1] = fmaf(dg8[u], c[u][0][2] + xi[u], acc[0][1]);
+                    acc[1][0] = fmaf(dg[u], c[u][1][1], acc[1][0]);
+                    acc[1][1] = fmaf(dg8[u], c[u][1][3], acc[1][1]);
+                    acc[2][0] = fmaf(dg[u], c[u][2][0], acc[2][0]);
+                    acc[2][1] = fmaf(dg8[u], c[u][2][2], acc[2][1]);
+                    acc[3][0] = fmaf(dg[u], c[u][3][1], acc[3][0]);
+                    acc[3][1] = fmaf(dg8[u], c[u][3][3], acc[3][1]);
+                }
             } else {
             int j = 0, bl = warp;  // unit u = warp + 8 i  ->  (16-row group j, block bl)
             while (bl >= nbk) {
@@ -538,9 +563,9 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         if (prologue) s *= p.a.act_scale;
         const int64_t o = (int64_t)m * N + r0 + r;
         if (p.a.y_f16)
-            reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(s);
+            reinterpret_cast<__half *>(y_g)[o] = __float2half_rn(s);
         else
-            reinterpret_cast<float *>(p.a.y)[o] = s;
+            reinterpret_cast<float *>(y_g)[o] = s;
     }
 }
 
@@ -549,12 +574,11 @@ static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Shared-memory plan for G CTAs within max_dyn bytes of dynamic shared
 // memory; returns false if it cannot fit.
-bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaParams &p)
+bool make_plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, MmaParams &p)
 {
     const int kMaxSmem = max_dyn;
     const int64_t B = K / 256;
     if (B > (1 << 20)) return false;
-    p.G = G;
     p.B = (int)B;
     if (B > kChunkBlocks) {  // 16 rows x 4096 codes per stage, 2-D tensor boxes
         p.tma2d = 1;
@@ -567,7 +591,6 @@ bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaParams &p)
         p.n_kc = 1;
         p.rg_s = kChunkBlocks / (int)B;
     }
-    const int64_t max_rows = (N + G - 1) / G;
     p.max_rg = (int)((max_rows + 15) / 16);
     if (p.rg_s > p.max_rg) p.rg_s = p.max_rg;
     p.rb = p.nbk_full * 64;  // dense rows, as TMA writes them
@@ -597,6 +620,12 @@ bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaParams &p)
     p.stages = S;
     p.smem_total = fixed + S * p.stage_bytes;
     return p.smem_total <= kMaxSmem;
+}
+
+bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaParams &p)
+{
+    p.G = G;
+    return make_plan_rows(M, (N + G - 1) / G, K, max_dyn, p);
 }
 
 // Largest dynamic shared memory the kernel for kM may use on `device`
@@ -639,6 +668,56 @@ bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaParams &p
     return true;
 }
 
+// CTAs of a group in proportion to the matrices' rows (at least one each,
+// at most one per SM in total while that fits), then the shared-memory plan
+// for the largest per-CTA row count.
+bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, int max_dyn, MmaParams &p)
+{
+    if (max_dyn <= 0 || n < 1 || n > kMaxGroup || K > 256 * kChunkBlocks) return false;
+    int64_t total = 0;
+    for (int j = 0; j < n; ++j) {
+        if (N[j] < 1) return false;
+        total += N[j];
+    }
+    const int nsm = sm_count(device);
+    for (int cap = nsm; cap <= 64 * nsm; cap *= 2) {
+        int G[kMaxGroup], sum = 0;
+        for (int j = 0; j < n; ++j) {
+            int64_t g = (int64_t)cap * N[j] / total;
+            if (g < 1) g = 1;
+            if (g > N[j]) g = (int)N[j];
+            G[j] = (int)g;
+            sum += G[j];
+        }
+        // leftover CTAs to the matrix with the most rows per CTA
+        while (sum < cap) {
+            int best = -1;
+            double worst = 0.0;
+            for (int j = 0; j < n; ++j)
+                if (G[j] < N[j] && (double)N[j] / G[j] > worst) {
+                    worst = (double)N[j] / G[j];
+                    best = j;
+                }
+            if (best < 0) break;
+            ++G[best];
+            ++sum;
+        }
+        int64_t max_rows = 0;
+        int g0 = 0;
+        for (int j = 0; j < n; ++j) {
+            max_rows = std::max<int64_t>(max_rows, (N[j] + G[j] - 1) / G[j]);
+            p.mats[j].N = N[j];
+            p.mats[j].g0 = g0;
+            p.mats[j].G = G[j];
+            g0 += G[j];
+        }
+        p.n_mats = n;
+        p.G = g0;
+        if (make_plan_rows(M, max_rows, K, max_dyn, p)) return true;
+    }
+    return false;
+}
+
 // qs as uint64 [N][K/32]; boxes 128 x {16, 8, 4, 2, 1}
 cudaError_t encode_qs_maps(const MatvecArgs &a, MmaParams &p)
 {
@@ -664,6 +743,8 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
     p.a = a;
     if (!plan_for(kM, a.N, a.K, device, max_dynamic_smem<kM>(device), p))
         return cudaErrorInvalidConfiguration;
+    p.n_mats = 1;
+    p.mats[0] = GroupMat{a.qs, a.d, a.y, a.N, 0, p.G};
     if (p.tma2d) {
         cudaError_t e = encode_qs_maps(a, p);
         if (e != cudaSuccess) return e;
@@ -682,7 +763,48 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int kM>
+cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                              void *const *y, const int64_t *N, int device)
+{
+    MmaParams p{};
+    p.a = a;
+    if (!group_plan(kM, n, N, a.K, device, max_dynamic_smem<kM>(device), p)) return cudaErrorInvalidConfiguration;
+    for (int j = 0; j < n; ++j) {
+        p.mats[j].qs = qs[j];
+        p.mats[j].d = d[j];
+        p.mats[j].y = y[j];
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.G);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = (size_t)p.smem_total;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<kM>, p);
+}
+
 }  // namespace
+
+bool mma_group_supported(int M, int n, const int64_t *N, int64_t K, int device)
+{
+    if (M < 1 || M > 2 || K < 256) return false;
+    MmaParams p{};
+    const int max_dyn = (M == 1) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
+    return group_plan(M, n, N, K, device, max_dyn, p);
+}
+
+cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                                    void *const *y, const int64_t *N, int device)
+{
+    if (a.M == 1) return launch_group_impl<1>(a, n, qs, d, y, N, device);
+    if (a.M == 2) return launch_group_impl<2>(a, n, qs, d, y, N, device);
+    return cudaErrorInvalidValue;
+}
 
 bool mma_matvec_supported(int M, int64_t N, int64_t K, int device)
 {

@@ -22,7 +22,7 @@ def L():
 
 def test_every_declared_symbol_is_exported(L):
     names = tq2.declared_symbols()
-    assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec",
+    assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
                           "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
@@ -92,3 +92,28 @@ def test_layout_calls_reject_bad_arguments(L):
     assert L.tq2_from_dense(A16, 0, 4, 256, A16, NUL, NUL, S) == NULL
     assert L.tq2_from_dense(A2, 0, 4, 256, A16, A16, NUL, S) == ALIGN  # fp32 W needs 4 bytes
     assert L.tq2_from_dense(A16, 1, 0, 256, A16, A16, NUL, S) == OK
+
+
+def test_grouped_rejects_bad_arguments(L):
+    n = 3
+    Pn = ctypes.c_void_p * n
+    good = Pn(0x10000, 0x20000, 0x30000)
+    ys = Pn(0x40000, 0x50000, 0x60000)
+    Ns = (ctypes.c_int64 * n)(64, 32, 16)
+    cast = lambda a: ctypes.cast(a, ctypes.c_void_p)
+    G = lambda **k: L.tq2_matvec_grouped(k.get("x", A16), k.get("M", 1), k.get("K", 512), k.get("n", n),
+                                         cast(k.get("qs", good)), cast(k.get("d", good)), cast(k.get("N", Ns)),
+                                         cast(k.get("y", ys)), k.get("yd", 0), k.get("s", 0.0), NUL, S)
+    assert G(n=0) == ARG
+    assert G(n=5) == ARG                          # more than TQ2_MAX_GROUP
+    assert L.tq2_matvec_grouped(A16, 1, 512, n, NUL, cast(good), cast(Ns), cast(ys), 0, 0.0, NUL, S) == NULL
+    assert G(K=300) == SHAPE
+    assert G(M=17) == SHAPE
+    assert G(N=(ctypes.c_int64 * n)(64, -1, 16)) == SHAPE
+    assert G(yd=3) == DTYPE
+    assert G(s=-1.0) == ARG
+    assert G(qs=Pn(0x10000, 0x20002, 0x30000)) == ALIGN
+    assert G(y=Pn(0x40000, 0, 0x60000)) == NULL
+    assert G(x=A2) == ALIGN
+    assert G(M=0) == OK                           # nothing to do
+    assert G(N=(ctypes.c_int64 * n)(0, 0, 0)) == OK
