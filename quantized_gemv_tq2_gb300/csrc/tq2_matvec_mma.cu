@@ -383,6 +383,99 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
     const uint32_t xs_thr = smem_addr(xsum) + (uint32_t)mcol * 4u;
     const uint32_t rg_stride_d = (uint32_t)(16 * p.dstr) * 4u;
 
+    if (p.n_kc == 1 && p.rg_s == 1 && p.nbk_full == kUpw * kConsumerWarps) {
+        // K = 4096: every stage is one 16-row group, all 16 blocks.  This
+        // warp takes blocks warp + u * kConsumerWarps of every stage, so their
+        // x sums stay in registers.  The next stage's codes are read as soon
+        // as this stage's are in MMA operands: their latency overlaps the
+        // MMAs draining and the scaled sums.
+        float xi[kUpw];
+#pragma unroll
+        for (int u = 0; u < kUpw; ++u)
+            xi[u] = -lds_f32(xs_thr + (uint32_t)(warp + u * kConsumerWarps) * (4u * kM)) * 5.9604644775390625e-08f;
+        const uint32_t x_warp = x_thr + (uint32_t)warp * x_blk;
+        const uint32_t a_warp = a_thr + (uint32_t)(warp * 64);
+        const uint32_t d_warp = d_thr + (uint32_t)(warp * 4);
+        uint32_t W0[kUpw][4], W1[kUpw][4];
+        float dg[kUpw], dg8[kUpw];
+        auto load_codes = [&](int sl) {
+#pragma unroll
+            for (int u = 0; u < kUpw; ++u) {
+                const uint32_t pa = a_warp + (uint32_t)(sl * p.stage_bytes + u * kConsumerWarps * 64);
+                const uint4 wa = lds128(pa), wb = lds128(pa + a_half);
+                W0[u][0] = wa.x; W0[u][1] = wa.y; W0[u][2] = wa.z; W0[u][3] = wa.w;
+                W1[u][0] = wb.x; W1[u][1] = wb.y; W1[u][2] = wb.z; W1[u][3] = wb.w;
+            }
+        };
+        auto load_scales = [&](int rg) {
+#pragma unroll
+            for (int u = 0; u < kUpw; ++u) {
+                const uint32_t pd = d_warp + (uint32_t)rg * rg_stride_d + (uint32_t)(u * kConsumerWarps * 4);
+                dg[u] = lds_f32(pd);
+                dg8[u] = lds_f32(pd + d_half);
+            }
+        };
+        int sl = 0, ph = 0;
+        bool ok = n_stages > 0;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[0]), 0u))) {
+            if (lane == 0) report_timeout(p, abort_flag);
+            ok = false;
+        }
+        if (ok) {
+            load_codes(0);
+            load_scales(0);
+        }
+        for (int s = 0; ok && s < n_stages; ++s) {
+            // unit by unit: four class accumulators starting at zero, then
+            // their scaled sums (the "-1" of q - 1 enters as d_b * (-X_b *
+            // 2^-24) on class 0); the next stage's codes are read once this
+            // stage's are all in MMA operands
+            const int nsl = (sl + 1 == S) ? 0 : sl + 1;
+            const int nph = (sl + 1 == S) ? (ph ^ 1) : ph;
+#pragma unroll
+            for (int u = 0; u < kUpw; ++u) {
+                const uint32_t px = x_warp + (uint32_t)(u * kConsumerWarps) * x_blk;
+                const uint4 xa = lds128(px), xb = lds128(px + x_half);
+                const uint32_t BX[4][2] = {{xa.x, xa.y}, {xa.z, xa.w}, {xb.x, xb.y}, {xb.z, xb.w}};
+                float c[4][4];
+#pragma unroll
+                for (int jw = 0; jw < 4; ++jw) {
+                    const uint32_t w0 = W0[u][jw], w1 = W1[u][jw], s0 = w0 >> 8, s1 = w1 >> 8;
+#pragma unroll
+                    for (int cl = 0; cl < 4; ++cl) {
+                        const uint32_t m = 0x00030003u << (2 * cl);
+                        if (jw == 0)
+                            mma_16816_zero(c[cl], w0 & m, w1 & m, s0 & m, s1 & m, BX[jw][0], BX[jw][1]);
+                        else
+                            mma_16816(c[cl], w0 & m, w1 & m, s0 & m, s1 & m, BX[jw][0], BX[jw][1]);
+                    }
+                }
+                if (u + 1 == kUpw && s + 1 < n_stages) {
+                    if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[nsl]), (uint32_t)nph))) {
+                        load_codes(nsl);
+                    } else {
+                        if (lane == 0) report_timeout(p, abort_flag);
+                        ok = false;
+                    }
+                }
+                const float e = dg[u], e8 = dg8[u];
+                acc[0][0] = fmaf(e, c[0][0] + xi[u], u ? acc[0][0] : 0.0f);
+                acc[0][1] = fmaf(e8, c[0][2] + xi[u], u ? acc[0][1] : 0.0f);
+                acc[1][0] = fmaf(e, c[1][1], u ? acc[1][0] : 0.0f);
+                acc[1][1] = fmaf(e8, c[1][3], u ? acc[1][1] : 0.0f);
+                acc[2][0] = fmaf(e, c[2][0], u ? acc[2][0] : 0.0f);
+                acc[2][1] = fmaf(e8, c[2][2], u ? acc[2][1] : 0.0f);
+                acc[3][0] = fmaf(e, c[3][1], u ? acc[3][0] : 0.0f);
+                acc[3][1] = fmaf(e8, c[3][3], u ? acc[3][1] : 0.0f);
+            }
+            if (ok && s + 1 < n_stages) load_scales(s + 1);
+            flush(s);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[S + sl]));
+            sl = nsl;
+            ph = nph;
+        }
+    } else {
     int slot = 0, phase = 0, kc = 0, rg0 = 0;  // stage iterator (no divisions)
     bool alive = true;        // false after this warp's wait ran out: no more waits
     bool ready_lane = false;  // early, non-blocking test of this stage's barrier
@@ -549,6 +642,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         }
     }
     if (cur_rg >= 0) flush(cur_rg);
+    }
     consumer_barrier();
     if (*abort_flag) return;  // y is invalid; TQ2_FLAG_TIMEOUT was reported
 
