@@ -10,7 +10,8 @@ The C source cites the passages it follows:
   recovery of d and the codes from a dequantised W, the linear factoring of
   the matvec;
 * "gemma4 wNa8o8 requires int8 activations" page: the static int8
-  fake-quant of the activations and its reciprocal-multiply form.
+  fake-quant of the activations and its reciprocal-multiply form, and the
+  same fake-quant of a linear's output at store (requantisation).
 """
 
 from __future__ import annotations
@@ -76,6 +77,8 @@ def _load():
         lib.tq2o_fakequant_codes.restype = None
         lib.tq2o_fakequant.argtypes = [P, I64, F, ctypes.c_int, P]
         lib.tq2o_fakequant.restype = None
+        lib.tq2o_requant.argtypes = [P, I64, F, P, P]
+        lib.tq2o_requant.restype = None
         lib.tq2o_matvec_f64.argtypes = [P, I64, P, P, I64, I64, F, P, P]
         lib.tq2o_matvec_f64.restype = None
         lib.tq2o_matvec_rows_f64.argtypes = [P, I64, P, P, I64, I64, F, P, I64, P, P]
@@ -191,6 +194,16 @@ def fakequant(x: np.ndarray, s: float, mode: int = 0) -> np.ndarray:
     out = np.zeros(xb.shape, dtype=np.float64)
     _load().tq2o_fakequant(_ptr(xb), xb.size, float(np.float32(s)), int(mode), _ptr(out))
     return out
+
+
+def requant(y, s: float):
+    """Output requantisation at store: (codes int8, y' = code * s fp64) of
+    fp64 y, the decision taken as rint(fp32(y) * fp32(1/s)) in fp32."""
+    yv = np.ascontiguousarray(np.asarray(y, dtype=np.float64))
+    codes = np.zeros(yv.shape, dtype=np.int8)
+    out = np.zeros(yv.shape, dtype=np.float64)
+    _load().tq2o_requant(_ptr(yv), yv.size, float(np.float32(s)), _ptr(codes), _ptr(out))
+    return codes, out
 
 
 # ---------------------------------------------------------------- matvec

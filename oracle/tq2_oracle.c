@@ -292,6 +292,35 @@ void tq2o_fakequant(const uint16_t *x, int64_t n, float s, int mode, double *xq)
 }
 
 /* ---------------------------------------------------------------------- */
+/* Static int8 output requantisation at store [P3]: the fake-quant at a     */
+/* linear's output boundary ("Implemented": fake-quant at every linear      */
+/* boundary, input post-norm and output at store; the recipe's "requantize  */
+/* the result to int8 with output_activation_scale -> dequantize").  The    */
+/* same function as the activation fake-quant, applied to the fp32 result:  */
+/* code = clamp(rint(fp32(y) * fp32(1/s)), -128, 127) in fp32, y' = code*s. */
+/* NaN -> 0, +-Inf saturate (as for the activations).                       */
+/* ---------------------------------------------------------------------- */
+static int requant_code_f32(double y, float s)
+{
+    volatile float inv = 1.0f / s;
+    volatile float yf = (float)y;
+    volatile float t = yf * inv;
+    return clamp_i8((double)rintf(t));
+}
+
+/* codes[n] and y'[n] = code * s (fp64) of the requantisation of y[n]. */
+void tq2o_requant(const double *y, int64_t n, float s, int8_t *codes, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int q = requant_code_f32(y[i], s);
+        if (codes)
+            codes[i] = (int8_t)q;
+        if (out)
+            out[i] = (double)q * (double)s;
+    }
+}
+
+/* ---------------------------------------------------------------------- */
 /* The matvec [P1, linear factoring]:                                      */
 /*   y[m][n] = sum_b d[n][b] * sum_{k in b} x'[m][k] * (q[n][k] - 1)        */
 /* with x' = x (act_scale == 0: no prologue, cf. the checkpoint's "scale 0  */

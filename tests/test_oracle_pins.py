@@ -209,6 +209,56 @@ def test_fakequant_reciprocal_form_matches_definition_away_from_ties():
     assert mism < 50
 
 
+# --------------------------------------------------------------------- output requantisation
+def test_requant_golden_cases():
+    for line in _golden_lines("requant_cases.txt"):
+        ys, ss, cs, vs = line.split()
+        codes, out = oracle.requant(np.array([float(ys)]), float(ss))
+        assert int(codes[0]) == int(cs), line
+        assert out[0] == float(vs), line
+
+
+def test_requant_matches_definition_away_from_ties():
+    # numpy restatement of the definition: clamp(round(y / s)) in fp64 on the
+    # fp32 value of y, half to even; the reciprocal form may differ only
+    # within a few fp32 ulps of a .5 tie
+    rng = np.random.default_rng(11)
+    y = (rng.standard_normal(100000) * 10.0 ** rng.uniform(-3, 2, 100000)).astype(np.float32)
+    mism = 0
+    for s in (0.013, 0.05, 0.0917, 1.7):
+        codes, out = oracle.requant(y.astype(np.float64), s)
+        t = y.astype(np.float64) / np.float64(np.float32(s))
+        qd = np.clip(np.rint(t), -128, 127).astype(np.int64)
+        c = codes.astype(np.int64)
+        diff = c != qd
+        mism += int(diff.sum())
+        frac = np.abs(np.abs(t[diff]) - np.floor(np.abs(t[diff])) - 0.5)
+        assert np.all(frac <= 4 * 2.0 ** -23 * np.abs(t[diff]) + 1e-30)
+        assert np.all(np.abs(c[diff] - qd[diff]) == 1)
+        assert np.array_equal(out, c * np.float64(np.float32(s)))
+    assert mism < 50
+
+
+def test_requant_is_the_activation_fakequant_on_fp16_values():
+    # the same function at the other boundary: on values that are fp16 the
+    # codes equal those of the (pinned) activation fake-quant
+    x = syn.activations(5, 1, 20000, heavy=True)[0]
+    for s in (0.02, 0.07, 0.25):
+        codes, _ = oracle.requant(x.astype(np.float64), s)
+        assert np.array_equal(codes, oracle.fakequant_codes(x, s, 0))
+
+
+def test_requant_range_and_fixed_point():
+    rng = np.random.default_rng(12)
+    y = rng.standard_normal(5000) * 150.0
+    for s in (0.125, 0.5, 2.0):  # powers of two: code * s is exact in fp32
+        codes, out = oracle.requant(y, s)
+        assert codes.min() >= -128 and codes.max() <= 127
+        assert codes.min() == -128 and codes.max() == 127  # the clamp is reached
+        codes2, out2 = oracle.requant(out, s)
+        assert np.array_equal(codes2, codes) and np.array_equal(out2, out)
+
+
 # --------------------------------------------------------------------- matvec
 def _dense_from_codes(codes, d):
     return np.repeat(d.astype(np.float64), 256, axis=1) * (codes.astype(np.float64) - 1)
