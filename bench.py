@@ -163,31 +163,33 @@ def build_stack(torch, tq2, syn, dev, with_prologue_scales=True):
     Y = torch.zeros(yo, dtype=torch.float32, device=dev)
     y_host = torch.empty(yo, dtype=torch.float32).pin_memory()
     scales = [syn.act_scale(SEED, linear=L) for L, *_ in lin] if with_prologue_scales else None
+    out_scales = [syn.out_scale(SEED, linear=L) for L, *_ in lin] if with_prologue_scales else None
     torch.cuda.synchronize()
     return dict(lin=lin, qs=qs, d=ds, x_off=x_off, y_off=y_off, X=X, Y=Y, x_host=x_host,
-                y_host=y_host, scales=scales)
+                y_host=y_host, scales=scales, out_scales=out_scales)
 
 
 def capture(torch, tq2, st, calls, stream):
-    """calls: list of (x view, qs, d, y view, act_scale, impl) -> CUDA graph."""
+    """calls: list of (x view, qs, d, y view, act_scale, impl, out_scale) -> CUDA graph."""
     with torch.cuda.stream(stream):
-        for x, qs, d, y, s, impl in calls:  # eager warm-up (kernel attributes, module load)
-            tq2.matvec(x, qs, d, y=y, act_scale=s, impl=impl)
+        for x, qs, d, y, s, impl, so in calls:  # eager warm-up (kernel attributes, module load)
+            tq2.matvec(x, qs, d, y=y, act_scale=s, impl=impl, out_scale=so)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for x, qs, d, y, s, impl in calls:
-                tq2.matvec(x, qs, d, y=y, act_scale=s, impl=impl)
+            for x, qs, d, y, s, impl, so in calls:
+                tq2.matvec(x, qs, d, y=y, act_scale=s, impl=impl, out_scale=so)
     stream.synchronize()
     return g
 
 
-def stack_calls(st, prologue=False, impl=0):
+def stack_calls(st, prologue=False, impl=0, requant=False):
     calls = []
     for i, (L, name, N, K) in enumerate(st["lin"]):
         x = st["X"][st["x_off"][i]:st["x_off"][i] + K].view(1, K)
         y = st["Y"][st["y_off"][i]:st["y_off"][i] + N].view(1, N)
-        calls.append((x, st["qs"][i], st["d"][i], y, st["scales"][i] if prologue else 0.0, impl))
+        calls.append((x, st["qs"][i], st["d"][i], y, st["scales"][i] if prologue else 0.0, impl,
+                      st["out_scales"][i] if requant else 0.0))
     return calls
 
 
@@ -264,7 +266,7 @@ def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None):
             import tq2_synth as syn
             x = torch.from_numpy(syn.activations(SEED + 7, M, K, linear=0)).to(dev)
             ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in idx]
-            calls = [(x, st["qs"][i], st["d"][i], y, 0.0, impl) for i, y in zip(idx, ys)]
+            calls = [(x, st["qs"][i], st["d"][i], y, 0.0, impl, 0.0) for i, y in zip(idx, ys)]
             g = capture(torch, tq2, st, calls, stream)
             one = time_graph(torch, g, stream, 2, 1)
             reps = max(3, int(0.3 / max(one * 1e-3, 1e-6)))  # ~0.3 s of replays
@@ -389,6 +391,13 @@ def run_gpu(args):
         extras["stack_with_prologue"] = dict(ms_per_step=ms_p, gbs=STACK_BYTES / (ms_p * 1e-3) / 1e9,
                                              tok_s=1e3 / ms_p)
         del gp
+        gq = capture(torch, tq2, st, stack_calls(st, prologue=True, requant=True), stream)
+        ms_q = time_graph(torch, gq, stream, max(3, min(args.steps, 2000)), 5)
+        extras["stack_wna8o8"] = dict(
+            ms_per_step=ms_q, gbs=STACK_BYTES / (ms_q * 1e-3) / 1e9, tok_s=1e3 / ms_q,
+            how="int8 fake-quant of x on load (per-linear act_scale) and requantisation of y "
+                "at store (per-linear out_scale, tq2_matvec_requant), both U[0.01, 0.1]")
+        del gq
         gcalls, gbytes = grouped_stack(st)
         gg = capture_grouped(torch, tq2, gcalls, stream)
         ms_g = time_graph(torch, gg, stream, max(3, min(args.steps, 2000)), 5)

@@ -190,6 +190,31 @@ TQ2_API tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *
                            void *workspace, size_t workspace_bytes, uint32_t *d_status,
                            tq2_stream_t stream, int impl);
 
+/*
+ * tq2_matvec_requant -- tq2_matvec_impl followed by the static int8
+ * requantisation of the result at store ("gemma4 wNa8o8 requires int8
+ * activations" page, "Implemented": fake-quant at every linear boundary,
+ * input post-norm and output at store; the recipe's "requantize the result
+ * to int8 with output_activation_scale -> dequantize").  With act_scale > 0
+ * the block sums are exact integer sums of int8 codes times ternary weights
+ * (int8 x ternary -> exact accumulate), and the stored result is
+ *   y'[m][n] = out_scale * clamp(rint(y[m][n] * (1/out_scale)), -128, 127)
+ * where y[m][n] is the fp32 result tq2_matvec_impl would store before its
+ * dtype conversion, the integer decision is taken in fp32 with
+ * fp32(1/out_scale) (ties to even; NaN -> 0, +-Inf saturate), and the
+ * product code * out_scale is rounded once to fp32, then to y_dtype (RNE).
+ *   out_scale  >= 0 and finite, else TQ2_ERR_ARG; 0 stores y unchanged
+ *              (the call is then tq2_matvec_impl).
+ * Everything else (arguments, impl, errors, accuracy of y before the
+ * requantisation) as tq2_matvec_impl.  A code may differ by one from the
+ * one of the exact y only where y lies within the accuracy bound of a
+ * rounding boundary.
+ */
+TQ2_API tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                                      int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                                      float out_scale, void *workspace, size_t workspace_bytes,
+                                      uint32_t *d_status, tq2_stream_t stream, int impl);
+
 /* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
  * host thread ("no error" if none): name and description, static storage. */
 TQ2_API const char *tq2_last_cuda_error(void);

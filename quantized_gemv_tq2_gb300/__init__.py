@@ -62,6 +62,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_from_dense.argtypes = [P, I32, I64, I64, P, P, P, P]
         L.tq2_matvec.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P]
         L.tq2_matvec_impl.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P, I32]
+        L.tq2_matvec_requant.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
         L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P]
         L.tq2_matvec_workspace_size.argtypes = [I64, I64, I64]
         L.tq2_matvec_workspace_size.restype = SZ
@@ -71,7 +72,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_last_cuda_error.argtypes = []
         L.tq2_last_cuda_error.restype = ctypes.c_char_p
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
-                   "tq2_matvec_grouped", "tq2_version"):
+                   "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
         return L
@@ -173,8 +174,9 @@ def from_dense(W, qs=None, d=None, status=None, stream=None):
 
 
 def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, status=None,
-           stream=None, impl: int = IMPL_AUTO, workspace=None):
-    """y [M,N] = ternary matvec of x [M,K] fp16 with packed qs/d (tq2_matvec)."""
+           stream=None, impl: int = IMPL_AUTO, workspace=None, out_scale: float = 0.0):
+    """y [M,N] = ternary matvec of x [M,K] fp16 with packed qs/d (tq2_matvec);
+    out_scale > 0 requantises y to int8 at store (tq2_matvec_requant)."""
     torch = _torch()
     if x.dim() == 1:
         x = x.view(1, -1)
@@ -192,7 +194,11 @@ def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, statu
     ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) \
         if workspace is not None else (ctypes.c_void_p(0), 0)
     L = load()
-    if impl == IMPL_AUTO:
+    if out_scale != 0.0:
+        st = L.tq2_matvec_requant(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode,
+                                  float(act_scale), float(out_scale), ws_ptr, ws_bytes, _ptr(status),
+                                  _stream_ptr(stream), int(impl))
+    elif impl == IMPL_AUTO:
         st = L.tq2_matvec(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
                           ws_ptr, ws_bytes, _ptr(status), _stream_ptr(stream))
     else:

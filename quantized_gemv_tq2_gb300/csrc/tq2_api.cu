@@ -77,13 +77,14 @@ tq2_status current_device(int *dev)
 
 tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                          int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
-                         uint32_t *d_status, tq2_stream_t stream, int impl)
+                         float out_scale, uint32_t *d_status, tq2_stream_t stream, int impl)
 {
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
     if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
     if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
+    if (!(out_scale >= 0.0f) || !std::isfinite(out_scale)) return TQ2_ERR_ARG;
     if (impl < 0 || impl > 5) return TQ2_ERR_ARG;
     if ((impl == 1 || impl == 3) && M > 2) return TQ2_ERR_ARG;
     if (impl == 5 && M > 1) return TQ2_ERR_ARG;
@@ -96,7 +97,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t ybytes = (size_t)(M * N) * (y_dtype == TQ2_F32 ? 4 : 2);
-    if (K == 0)  // empty sums: y = 0 (all-zero bits are +0 in fp32 and fp16)
+    if (K == 0)  // empty sums: y = 0 (all-zero bits are +0 in fp32 and fp16; requantised, still 0)
         return from_cuda(cudaMemsetAsync(y, 0, ybytes, s));
 
     int dev = 0;
@@ -113,6 +114,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     a.y_f16 = (y_dtype == TQ2_F16);
     a.act_scale = act_scale;
     a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;  // IEEE-correct division
+    a.out_scale = out_scale;
+    a.inv_out = out_scale != 0.0f ? 1.0f / out_scale : 0.0f;
     a.stream = s;
 
     // impl 0: for M <= 2 the class-column mma.sync kernel, for larger M (or
@@ -190,7 +193,7 @@ tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uin
 {
     (void)workspace;
     (void)workspace_bytes;
-    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, d_status, stream, 0);
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, 0.0f, d_status, stream, 0);
 }
 
 tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
@@ -200,7 +203,17 @@ tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, cons
 {
     (void)workspace;
     (void)workspace_bytes;
-    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, d_status, stream, impl);
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, 0.0f, d_status, stream, impl);
+}
+
+tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                              int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
+                              float out_scale, void *workspace, size_t workspace_bytes,
+                              uint32_t *d_status, tq2_stream_t stream, int impl)
+{
+    (void)workspace;
+    (void)workspace_bytes;
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, d_status, stream, impl);
 }
 
 tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
@@ -257,6 +270,8 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
             a.y_f16 = (y_dtype == TQ2_F16);
             a.act_scale = act_scale;
             a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;
+            a.out_scale = 0.0f;
+            a.inv_out = 0.0f;
             a.stream = reinterpret_cast<cudaStream_t>(stream);
             cudaError_t e = tq2::launch_matvec_mma_group(a, n, gq, gd, gy, gn, dev);
             if (e == cudaSuccess) e = cudaGetLastError();
@@ -265,7 +280,7 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
     }
     // otherwise one call per matrix, same x, same stream
     for (int j = 0; j < n; ++j) {
-        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, d_status, stream, 0);
+        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, 0.0f, d_status, stream, 0);
         if (st != TQ2_OK) return st;
     }
     return TQ2_OK;

@@ -169,5 +169,13 @@ __device__ __forceinline__ float fq_code(float x, float inv_s)
     return fminf(fmaxf(rintf(t), -128.0f), 127.0f);
 }
 
+// Output requantisation at store (gemma4 wNa8o8 page, "Implemented": the
+// same fake-quant at a linear's output): y -> s * clamp(rint(y * (1/s)),
+// -128, 127) on the fp32 result; s == 0 leaves y as computed.
+__device__ __forceinline__ float requant_out(float y, float s, float inv_s)
+{
+    return (s != 0.0f) ? s * fq_code(y, inv_s) : y;
+}
+
 }  // namespace dev
 }  // namespace tq2

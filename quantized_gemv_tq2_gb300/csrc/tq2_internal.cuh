@@ -23,6 +23,8 @@ struct MatvecArgs {
     int y_f16;           // 0: fp32 y, 1: fp16 y
     float act_scale;     // 0: no prologue
     float inv_scale;     // fp32(1/act_scale), correctly rounded on the host
+    float out_scale;     // 0: y stored as computed; else requantised to int8 at store
+    float inv_out;       // fp32(1/out_scale), correctly rounded on the host
     cudaStream_t stream;
 };
 

@@ -618,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_dp4_kernel(const __grid_co
         float s = red[r * 2];
         if (p.ngrp == 2) s += red[r * 2 + 1];
         if (prologue) s *= p.a.act_scale;
+        s = requant_out(s, p.a.out_scale, p.a.inv_out);
         if (p.a.y_f16)
             reinterpret_cast<__half *>(p.a.y)[r0 + r] = __float2half_rn(s);
         else

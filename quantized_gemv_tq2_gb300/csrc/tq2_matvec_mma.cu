@@ -655,6 +655,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) s += red[((rg * kConsumerWarps + w) * kM + m) * 16 + ri];
         if (prologue) s *= p.a.act_scale;
+        s = requant_out(s, p.a.out_scale, p.a.inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(y_g)[o] = __float2half_rn(s);

@@ -477,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) s += red[((rg * kWarps + w) * 16 + ri) * M + m];
         if (prologue) s *= p.a.act_scale;
+        s = requant_out(s, p.a.out_scale, p.a.inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(s);

@@ -8,6 +8,7 @@
 // against.
 #include <cuda_fp16.h>
 
+#include "tq2_device.cuh"
 #include "tq2_internal.cuh"
 
 namespace tq2 {
@@ -15,15 +16,7 @@ namespace {
 
 constexpr int kSimtThreads = 256;
 
-// fake-quant integer code of one activation: rint(x * (1/s)) in fp32,
-// ties to even, clamped to [-128, 127]; NaN -> 0 (gemma4 wNa8o8 page,
-// "Implemented": s * clamp(rint(x * (1/s)), -128, 127)).
-__device__ __forceinline__ float fq_code(float x, float inv_s)
-{
-    float t = __fmul_rn(x, inv_s);
-    if (t != t) return 0.0f;
-    return fminf(fmaxf(rintf(t), -128.0f), 127.0f);
-}
+using dev::fq_code;  // rint(x * (1/s)) in fp32, clamped (gemma4 wNa8o8 page)
 
 template <int kM>
 __global__ void __launch_bounds__(kSimtThreads)
@@ -71,6 +64,7 @@ matvec_simt_kernel(MatvecArgs a)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
             if (prologue) s *= a.act_scale;
+            s = dev::requant_out(s, a.out_scale, a.inv_out);
             if (lane == 0) {
                 if (a.y_f16)
                     reinterpret_cast<__half *>(a.y)[(int64_t)m * a.N + n] = __float2half_rn(s);

@@ -51,6 +51,7 @@
 
 #include <atomic>
 
+#include "tq2_device.cuh"
 #include "tq2_internal.cuh"
 
 namespace tq2 {
@@ -537,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
         float v = 0.0f;
         for (int s = 0; s < S; ++s) v += red[(s * p.lanes_per_seg + r) * kM + m];
         if (prologue) v *= p.a.act_scale;
+        v = dev::requant_out(v, p.a.out_scale, p.a.inv_out);
         const int64_t o = (int64_t)m * N + row0 + r;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(v);

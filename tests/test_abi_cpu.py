@@ -23,6 +23,7 @@ def L():
 def test_every_declared_symbol_is_exported(L):
     names = tq2.declared_symbols()
     assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
+                          "tq2_matvec_impl", "tq2_matvec_requant",
                           "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
@@ -62,6 +63,26 @@ def test_matvec_rejects_bad_dtype_and_args(L):
     assert mv(L, impl=1, M=3) == ARG  # the class-column tensor-core kernels take M <= 2
     assert mv(L, impl=3, M=3) == ARG
     assert mv(L, impl=4, M=17) == SHAPE  # the pre-scaled kernel takes M <= 16, as the API
+
+
+def rq(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, so=0.5, st=NUL, impl=0):
+    return L.tq2_matvec_requant(x, M, qs, d, N, K, y, yd, s, so, NUL, 0, st, S, impl)
+
+
+def test_requant_rejects_bad_arguments(L):
+    assert rq(L, so=-0.5) == ARG
+    assert rq(L, so=float("nan")) == ARG
+    assert rq(L, so=float("inf")) == ARG
+    assert rq(L, s=-1.0) == ARG
+    assert rq(L, K=300) == SHAPE
+    assert rq(L, M=17) == SHAPE
+    assert rq(L, yd=3) == DTYPE
+    assert rq(L, impl=6) == ARG
+    assert rq(L, impl=1, M=3) == ARG
+    assert rq(L, x=NUL) == NULL
+    assert rq(L, y=A2) == ALIGN
+    assert rq(L, M=0, x=NUL, y=NUL) == OK
+    assert rq(L, N=0, qs=NUL, d=NUL, y=NUL, so=0.0) == OK
 
 
 def test_matvec_empty_shapes_are_noops(L):

@@ -36,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "SLOT_CODE_BITS", "SLOT_SCALES", "SLOT_X", "SLOT_HEAVY_SEL", "SLOT_HEAVY_Z",
-    "SLOT_ACT_SCALE", "SLOT_DENSE",
+    "SLOT_ACT_SCALE", "SLOT_DENSE", "SLOT_OUT_SCALE",
     "tensor_id", "words", "uniform", "normal",
     "code_bits", "codes_from_bits", "codes_from_bits_torch", "codes", "scales", "activations",
     "act_scale", "dense_normal",
@@ -54,6 +54,7 @@ SLOT_HEAVY_SEL = 3
 SLOT_HEAVY_Z = 4
 SLOT_ACT_SCALE = 5
 SLOT_DENSE = 6
+SLOT_OUT_SCALE = 7
 
 
 def tensor_id(linear: int, slot: int) -> int:
@@ -150,6 +151,12 @@ def activations(seed: int, m: int, k: int, linear: int = 0,
 def act_scale(seed: int, linear: int = 0) -> float:
     """Static per-linear activation scale s = fp32(U[0.01, 0.1])."""
     u = uniform(seed, tensor_id(linear, SLOT_ACT_SCALE), 1)[0]
+    return float(np.float32(0.01 + 0.09 * u))
+
+
+def out_scale(seed: int, linear: int = 0) -> float:
+    """Static per-linear output scale s_o = fp32(U[0.01, 0.1])."""
+    u = uniform(seed, tensor_id(linear, SLOT_OUT_SCALE), 1)[0]
     return float(np.float32(0.01 + 0.09 * u))
 
 
