@@ -104,8 +104,10 @@ __device__ __forceinline__ uint32_t frag_off(int bx, int nt, int jw, int h, int 
 }
 
 // Turn x (rows m, blocks [kb0, kb0 + nbx)) into B fragments and xinfo.
-// One warp per (block, row) pair; lane l takes the 8 codes' x values
-// 8l .. 8l+7 of the block.
+// A half-warp takes one (row, block) pair, lane wi of it the 16-code word wi
+// of the block (16 x values, two 16-byte loads): it writes that word's whole
+// B entry (both halves, all four classes), so no value crosses lanes; the
+// block sum and the "big" test are half-warp reductions.
 template <int NT>
 __device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uint32_t frag, float2 *xinfo,
                                         int warp, int lane)
@@ -113,17 +115,20 @@ __device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uin
     const int M = p.a.M;
     const int64_t K = p.a.K;
     const bool prologue = p.a.act_scale != 0.0f;
-    const int h = lane & 1, w = lane >> 1;
-    constexpr int kBatch = 4;
+    const int hw = lane >> 4, wi = lane & 15;
+    const int t = wi >> 2, jw = wi & 3;
+    const uint32_t half_mask = hw ? 0xFFFF0000u : 0x0000FFFFu;
+    constexpr int kBatch = 2;                 // pairs per half-warp per pass
+    constexpr int kStep = kWarps * 2;         // pairs per pass of all warps
     const int npairs = nbx * M;
     // pair index pr -> (m = pr / nbx, bx = pr - m * nbx), stepped without division
-    int m0 = 0, bx0 = warp;
+    int m0 = 0, bx0 = 2 * warp + hw;
     while (bx0 >= nbx && m0 < M) {
         bx0 -= nbx;
         ++m0;
     }
-    for (int pr0 = warp; pr0 < npairs; pr0 += kWarps * kBatch) {
-        uint4 v[kBatch];
+    for (int pr0 = 2 * warp; pr0 < npairs; pr0 += kStep * kBatch) {
+        uint4 v[kBatch][2];
         int mm[kBatch], bb[kBatch];
         int m = m0, bx = bx0;
 #pragma unroll
@@ -131,10 +136,11 @@ __device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uin
             mm[i] = m;
             bb[i] = bx;
             if (m < M) {
-                const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(kb0 + bx) * 256 + 8 * lane;
-                v[i] = *reinterpret_cast<const uint4 *>(src);
+                const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(kb0 + bx) * 256 + 16 * wi;
+                v[i][0] = *reinterpret_cast<const uint4 *>(src);
+                v[i][1] = *reinterpret_cast<const uint4 *>(src + 8);
             }
-            bx += kWarps;
+            bx += kStep;
             while (bx >= nbx && m < M) {
                 bx -= nbx;
                 ++m;
@@ -144,53 +150,61 @@ __device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uin
         bx0 = bx;
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-            if (mm[i] >= M) break;  // uniform over the warp
-            uint32_t r[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            const bool live = mm[i] < M;  // uniform over each half-warp
+            if (!__any_sync(0xffffffffu, live)) break;
+            uint32_t r[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w,
+                             v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w};
+            if (!live) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) r[q] = 0u;
+            }
             if (prologue) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r[q]));
                     const __half2 c2 = __floats2half2_rn(fq_code(f.x, p.a.inv_scale), fq_code(f.y, p.a.inv_scale));
                     r[q] = *reinterpret_cast<const uint32_t *>(&c2);
                 }
             }
-            float sum = 0.0f;
-            bool big = false;
+            float s2[2] = {0.0f, 0.0f};
+            uint32_t mx = 0u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
                 const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r[q]));
-                sum += f.x + f.y;
-                big |= ((r[q] & 0x7FFFu) >= 0x6400u) || (((r[q] >> 16) & 0x7FFFu) >= 0x6400u);
+                s2[q & 1] += f.x + f.y;
+                mx = __vmaxu2(mx, r[q] & 0x7FFF7FFFu);
             }
-            big = __any_sync(0xffffffffu, big);
-            // class scales: positions 8h + (0,1 | 2,3 | 4,5 | 6,7) have classes (0,1 | 2,3 | 0,1 | 2,3)
+            float sum = s2[0] + s2[1];
+            const bool big_lane = ((mx & 0xFFFFu) >= 0x6400u) || ((mx >> 16) >= 0x6400u);
+            const bool big = (__ballot_sync(0xffffffffu, big_lane) & half_mask) != 0u;
+            // class scales: r[q] holds positions (2q, 2q+1), classes (0,1) for even q, (2,3) for odd q
             const __half2 s01 = big ? __floats2half2_rn(1.0f, 0.25f) : __floats2half2_rn(64.0f, 16.0f);
             const __half2 s23 = big ? __floats2half2_rn(0.0625f, 0.015625f) : __floats2half2_rn(4.0f, 1.0f);
-            uint32_t sv[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
                 const __half2 prod = __hmul2(*reinterpret_cast<const __half2 *>(&r[q]), (q & 1) ? s23 : s01);
-                sv[q] = *reinterpret_cast<const uint32_t *>(&prod);
+                r[q] = *reinterpret_cast<const uint32_t *>(&prod);
             }
-            // this lane's two entries of each class: positions (8h + c, 8h + 4 + c)
-            uint32_t mine[4];
+            // class c: b0 = (x[c], x[8+c]), b1 = (x[4+c], x[12+c]) of the word
+            uint32_t e[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) mine[c] = __byte_perm(sv[c >> 1], sv[2 + (c >> 1)], (c & 1) ? 0x7632 : 0x5410);
-            // lane h = 0 writes classes 0, 1; lane h = 1 writes classes 2, 3
-            const uint32_t recv0 = __shfl_xor_sync(0xffffffffu, h ? mine[0] : mine[2], 1);
-            const uint32_t recv1 = __shfl_xor_sync(0xffffffffu, h ? mine[1] : mine[3], 1);
-            const uint32_t own0 = h ? mine[2] : mine[0], own1 = h ? mine[3] : mine[1];
-            const uint32_t lo0 = h ? recv0 : own0, hi0 = h ? own0 : recv0;
-            const uint32_t lo1 = h ? recv1 : own1, hi1 = h ? own1 : recv1;
-            const int mi = mm[i], nt = mi >> 3;
-            sts128(frag + frag_off(bb[i], nt, w & 3, h, w >> 2, mi & 7, M), __byte_perm(lo0, hi0, 0x5410),
-                   __byte_perm(lo0, hi0, 0x7632), __byte_perm(lo1, hi1, 0x5410), __byte_perm(lo1, hi1, 0x7632));
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+                e[2 * c] = __byte_perm(r[c >> 1], r[4 + (c >> 1)], sel);
+                e[2 * c + 1] = __byte_perm(r[2 + (c >> 1)], r[6 + (c >> 1)], sel);
+            }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (lane == 0) {
-                const float sc = big ? 5.9604644775390625e-08f : 3.814697265625e-06f;  // 2^-24, 2^-18
-                const float rs = big ? 16777216.0f : 262144.0f;
-                xinfo[bb[i] * 8 * NT + mi] = make_float2(-sum * sc, rs);
+            for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (live) {
+                const int mi = mm[i], nt = mi >> 3, Mt = min(8, M - 8 * nt);
+                const uint32_t dst = frag + frag_off(bb[i], nt, jw, 0, t, mi & 7, M);
+                sts128(dst, e[0], e[1], e[2], e[3]);                                // classes 0, 1
+                sts128(dst + (uint32_t)(64 * Mt), e[4], e[5], e[6], e[7]);        // classes 2, 3
+                if (wi == 0) {
+                    const float sc = big ? 5.9604644775390625e-08f : 3.814697265625e-06f;  // 2^-24, 2^-18
+                    const float rs = big ? 16777216.0f : 262144.0f;
+                    xinfo[bb[i] * 8 * NT + mi] = make_float2(-sum * sc, rs);
+                }
             }
         }
     }
