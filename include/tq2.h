@@ -215,6 +215,29 @@ TQ2_API tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_
                                       float out_scale, void *workspace, size_t workspace_bytes,
                                       uint32_t *d_status, tq2_stream_t stream, int impl);
 
+/*
+ * tq2_gemm -- the same product for any number of activation rows (prefill:
+ * a prompt's tokens at once), BitCPM ternary page, linear-factoring paragraph:
+ *   y[m][n] = sum_b d[n][b] * sum_{k in b} x'[m][k] * (q[n][k] - 1),
+ * m < M, with the optional prologue (act_scale) and output requantisation
+ * (out_scale) of tq2_matvec_requant.
+ *   x          device, fp16 [M, K] row-major, 16-byte aligned, read only.
+ *   M          >= 0 (up to 2^30); qs, d, N, K, y, y_dtype, act_scale,
+ *              out_scale, d_status, stream as tq2_matvec_requant (y [M, N]).
+ *   impl       0 = automatic, 1 = the tcgen05 GEMM (5th-generation tensor
+ *              cores: weights expanded once per 128-row tile into exact fp16
+ *              (q - 1) * d_b in tensor memory, x tiles by TMA, fp32
+ *              accumulation over all of K; no prologue: act_scale must be 0),
+ *              2 = the matvec kernels on 16-row slices of x.  Automatic takes
+ *              the GEMM for M > 16 without a prologue, the slices otherwise.
+ * Errors and accuracy as tq2_matvec (TQ2_ERR_SHAPE for M out of range;
+ * TQ2_ERR_ARG for impl out of range, impl 1 with act_scale != 0, or a shape
+ * impl 1 cannot plan).
+ */
+TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
+                            int64_t K, void *y, tq2_dtype y_dtype, float act_scale, float out_scale,
+                            uint32_t *d_status, tq2_stream_t stream, int impl);
+
 /* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
  * host thread ("no error" if none): name and description, static storage. */
 TQ2_API const char *tq2_last_cuda_error(void);

@@ -286,6 +286,65 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
     return TQ2_OK;
 }
 
+tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
+                    void *y, tq2_dtype y_dtype, float act_scale, float out_scale, uint32_t *d_status,
+                    tq2_stream_t stream, int impl)
+{
+    tq2_status st = check_nk(N, K);
+    if (st != TQ2_OK) return st;
+    if (M < 0 || M > ((int64_t)1 << 30)) return TQ2_ERR_SHAPE;
+    if (M > 0 && N > 0 && M > kMaxElems / (N > K ? N : (K > 0 ? K : 1))) return TQ2_ERR_SHAPE;
+    if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
+    if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
+    if (!(out_scale >= 0.0f) || !std::isfinite(out_scale)) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 2) return TQ2_ERR_ARG;
+    if (impl == 1 && act_scale != 0.0f) return TQ2_ERR_ARG;  // the tcgen05 GEMM has no prologue
+    if (M == 0 || N == 0) return TQ2_OK;
+    if (y == nullptr) return TQ2_ERR_NULL;
+    if (K > 0 && (x == nullptr || qs == nullptr || d == nullptr)) return TQ2_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(d, 2)) return TQ2_ERR_ALIGN;
+    if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
+    if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t ebytes = (y_dtype == TQ2_F32 ? 4 : 2);
+    if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * ebytes, s));
+
+    int dev = 0;
+    if ((st = current_device(&dev)) != TQ2_OK) return st;
+    // impl 0: the tcgen05 GEMM for M > 16 without a prologue, else the
+    // matvec kernels on 16-row slices of x (the same result contract)
+    bool gemm = (impl == 1);
+    if (impl == 0) gemm = M > 16 && act_scale == 0.0f && tq2::gemm_tc05_supported(M, N, K, dev);
+    if (gemm) {
+        if (!tq2::gemm_tc05_supported(M, N, K, dev)) return TQ2_ERR_ARG;
+        tq2::MatvecArgs a;
+        a.x = x;
+        a.qs = qs;
+        a.d = d;
+        a.y = y;
+        a.status = d_status;
+        a.N = N;
+        a.K = K;
+        a.M = (int)M;
+        a.y_f16 = (y_dtype == TQ2_F16);
+        a.act_scale = act_scale;
+        a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;
+        a.out_scale = out_scale;
+        a.inv_out = out_scale != 0.0f ? 1.0f / out_scale : 0.0f;
+        a.stream = s;
+        cudaError_t e = tq2::launch_gemm_tc05(a, dev);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        return from_cuda(e);
+    }
+    for (int64_t m0 = 0; m0 < M; m0 += 16) {
+        const int64_t mc = (M - m0 < 16) ? (M - m0) : 16;
+        st = matvec_common(x + m0 * K, mc, qs, d, N, K, static_cast<uint8_t *>(y) + (size_t)(m0 * N) * ebytes,
+                           y_dtype, act_scale, out_scale, d_status, stream, 0);
+        if (st != TQ2_OK) return st;
+    }
+    return TQ2_OK;
+}
+
 size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K)
 {
     (void)M;

@@ -1,0 +1,530 @@
+// tq2_gemm_tc05.cu -- ternary GEMM for prefill-sized M on the 5th-generation
+// tensor cores (sm_103a): tcgen05.mma with the weights in tensor memory, x
+// tiles brought by TMA, one fp32 accumulator in tensor memory.
+//
+// What it computes (BitCPM ternary page, linear-factoring paragraph), for any
+// number M of activation rows:
+//   y[m][n] = sum_b d[n][b] * sum_{k in b} x[m][k] * (q[n][k] - 1)
+// Each (q - 1) * d_b is one of -d_b, 0, +d_b and therefore exact in fp16, and
+// an fp16 x fp16 product is exact in fp32, so with many activation rows the
+// matvec becomes a plain dense contraction W' x^T with W'[n][k] = (q - 1) d_b:
+// the weights are expanded once per tile and the tensor cores accumulate over
+// all of K with no per-block epilogue (the d_b and the "-1" live in W').
+//
+// Tile: 128 weight rows (the MMA's M, one TMEM lane each) x BN activation rows
+// (the MMA's N, 128 or 256), all of K; tcgen05.mma.cta_group::1.kind::f16,
+// K = 16 per instruction.
+//   * warp 0 streams the packed codes: 2-D TMA boxes of 128 rows x 128 bytes
+//     (512 codes), 128-byte swizzle, before griddepcontrol.wait (weights never
+//     depend on earlier kernels);
+//   * warp 1 streams x after griddepcontrol.wait: per stage one TMA box of
+//     64 values (4 k-steps) x BN rows, 128 bytes per row with the 128-byte
+//     swizzle, which is the K-major SWIZZLE_128B operand layout the MMA reads
+//     (8-row groups 1024 bytes apart; k-step j of the stage starts 32 bytes
+//     into the row); rows past M read as 0;
+//   * warp 2 allocates the 512 TMEM columns (after the wait, so the previous
+//     kernel's tensor memory is free) and one lane issues the MMAs;
+//   * warps 3..10 (two per TMEM lane quadrant) stage d, then expand 8 k-steps
+//     at a time: for code pair (2j, 2j+1) of a 16-code word, the fp16 pair
+//     (1024 + q) - 1025 = q - 1 (exact) times d_b, written with tcgen05.st
+//     into a 4-slot ring of 64 TMEM columns; at the end they read D (one
+//     column per activation row) and store y, with the optional int8
+//     requantisation at store.
+// Every mbarrier wait is bounded; a wait that runs out sets TQ2_FLAG_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "tq2_device.cuh"
+#include "tq2_internal.cuh"
+
+namespace tq2 {
+namespace {
+
+using namespace dev;
+
+constexpr int kWProducerWarp = 0;
+constexpr int kBProducerWarp = 1;
+constexpr int kMmaWarp = 2;
+constexpr int kFirstUnpackWarp = 3;
+constexpr int kUnpackWarps = 8;
+constexpr int kThreads = (kFirstUnpackWarp + kUnpackWarps) * 32;  // 352
+constexpr int kTmemThreads = (kUnpackWarps + 1) * 32;            // MMA warp + unpack warps
+constexpr int kRows = 128;               // weight rows per tile (MMA M, TMEM lanes)
+constexpr int kKs = 4;                   // k-steps (16 codes) per x stage
+constexpr int kWStageBytes = 16384;      // 128 rows x 128 bytes of codes (32 k-steps)
+constexpr int kASlots = 4;               // TMEM A ring
+constexpr int kAColsPerSlot = 64;        // 8 k-steps x 8 columns
+constexpr int kDCol = 256;               // D (fp32, BN columns) starts here
+constexpr int kTmemCols = 512;
+constexpr int kMaxStages = 8;
+
+struct GemmParams {
+    CUtensorMap wmap;  // qs as uint64 [N][K/32]; box {16, 128}; 128-byte swizzle
+    CUtensorMap xmap;  // x as fp16 [M][K]; box {64, BN}; 128-byte swizzle
+    MatvecArgs a;
+    int n_tiles;       // weight-row tiles (ceil(N / 128)); blockIdx = m_tile * n_tiles + n_tile
+    int B;             // 256-blocks per row
+    int sw, sb;        // ring depths: codes, x
+    int off_bar, off_dsm, off_w, off_b, smem_total;
+};
+
+__device__ __forceinline__ uint64_t evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this warp's lane quadrant
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// D[d_taddr] (+)= A[a_taddr] * B(desc), M = 128, N from idesc, K = 16, f16 x f16 -> f32
+__device__ __forceinline__ void umma_f16(uint32_t d_taddr, uint32_t a_taddr, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+                 "r"(a_taddr), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void report_timeout(const GemmParams &p, volatile int *flag)
+{
+    *flag = 1;
+    if (p.a.status) atomicOr(p.a.status, TQ2_FLAG_TIMEOUT);
+}
+
+// The 8 TMEM columns of one k-step for one weight row: column j holds the
+// fp16 pair ((q[2j] - 1) d, (q[2j+1] - 1) d) of the 16-code word w.
+__device__ __forceinline__ void expand_word(uint32_t w, __half2 dd, uint32_t *o)
+{
+    const uint32_t src[4] = {w, w >> 2, w >> 4, w >> 6};  // code pairs at bits 0-1 of each byte
+    const __half2 bias = __float2half2_rn(-1025.0f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t byte = (uint32_t)(j >> 1), odd = (uint32_t)(j & 1);
+        // q[2j] -> bits 0-1 of lane 0, q[2j+1] -> bits 16-17 of lane 1
+        const uint32_t t = __byte_perm(src[2 * odd], src[2 * odd + 1], byte | ((4u + byte) << 8));
+        const uint32_t f = (t & 0x00030003u) | 0x64006400u;  // fp16 (1024 + q, 1024 + q')
+        const __half2 h = __hmul2(__hadd2(*reinterpret_cast<const __half2 *>(&f), bias), dd);
+        o[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_constant__ GemmParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+    volatile int *abort_flag = &abort_sh;
+    constexpr uint32_t kBStageBytes = (uint32_t)BN * 128u;  // 64 values (kKs k-steps) per row
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t N = p.a.N, K = p.a.K;
+    const int M = p.a.M;
+    const int ntile = (int)(blockIdx.x % (unsigned)p.n_tiles), mtile = (int)(blockIdx.x / (unsigned)p.n_tiles);
+    const int64_t n0 = (int64_t)ntile * kRows;
+    const int m0 = mtile * BN;
+    const int nks = (int)(K / 16);               // k-steps
+    const int ngroups = nks / 8;                 // TMEM A fills (8 k-steps each)
+    const int nwst = (int)((K + 511) / 512);     // code stages (128 bytes of codes per row)
+    const int nbst = nks / kKs;                  // x stages
+    const int SW = p.sw, SB = p.sb;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    const uint32_t wfull0 = smem_addr(bars), wempty0 = wfull0 + 8u * SW;
+    const uint32_t bfull0 = wempty0 + 8u * SW, bempty0 = bfull0 + 8u * SB;
+    const uint32_t afull0 = bempty0 + 8u * SB, aempty0 = afull0 + 8u * kASlots;
+    const uint32_t dfull = aempty0 + 8u * kASlots;
+    // both rings must be 1024-byte aligned for the 128-byte swizzle (the plan
+    // reserves the slack)
+    const uint32_t wring = (smem_addr(smem + p.off_w) + 1023u) & ~1023u;
+    const uint32_t bring = (smem_addr(smem + p.off_b) + 1023u) & ~1023u;
+
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (tid == 0) {
+        for (int i = 0; i < SW; ++i) {
+            mbar_init(wfull0 + 8u * i, 1);
+            mbar_init(wempty0 + 8u * i, kUnpackWarps);
+        }
+        for (int i = 0; i < SB; ++i) {
+            mbar_init(bfull0 + 8u * i, 1);
+            mbar_init(bempty0 + 8u * i, 1);
+        }
+        for (int i = 0; i < kASlots; ++i) {
+            mbar_init(afull0 + 8u * i, 4);
+            mbar_init(aempty0 + 8u * i, 1);
+        }
+        mbar_init(dfull, 1);
+        abort_sh = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kWProducerWarp) {
+        // -------------------------------------------------- codes -> shared memory
+        const uint64_t pol = evict_first_policy();
+        int issued = 0;
+        for (int s = 0; s < nwst; ++s) {
+            const int slot = s % SW, round = s / SW;
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(wempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
+                if (lane == 0) report_timeout(p, abort_flag);
+                break;
+            }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            if (lane == 0) {
+                const uint32_t full = wfull0 + 8u * slot;
+                mbar_arrive_expect_tx(full, (uint32_t)kWStageBytes);
+                tensor2d_g2s(wring + (uint32_t)(slot * kWStageBytes), &p.wmap, 16 * s, (int)n0, full, pol);
+            }
+            __syncwarp();
+            issued = s + 1;
+        }
+        for (int slot = 0; slot < SW && slot < issued; ++slot) {  // no copy in flight at exit
+            const int last = slot + ((issued - 1 - slot) / SW) * SW;
+            if (!mbar_wait(wfull0 + 8u * slot, (uint32_t)((last / SW) & 1)) && lane == 0) report_timeout(p, abort_flag);
+        }
+        return;
+    }
+
+    if (warp == kBProducerWarp) {
+        // -------------------------------------------------- x -> shared memory
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+        const uint64_t pol = evict_last_policy();           // every weight tile reads it again
+        int issued = 0;
+        for (int s = 0; s < nbst; ++s) {
+            const int slot = s % SB, round = s / SB;
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(bempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
+                if (lane == 0) report_timeout(p, abort_flag);
+                break;
+            }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            const uint32_t full = bfull0 + 8u * slot;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full, kBStageBytes);
+                tensor2d_g2s(bring + (uint32_t)slot * kBStageBytes, &p.xmap, 16 * kKs * s, m0, full, pol);
+            }
+            __syncwarp();
+            issued = s + 1;
+        }
+        for (int slot = 0; slot < SB && slot < issued; ++slot) {
+            const int last = slot + ((issued - 1 - slot) / SB) * SB;
+            if (!mbar_wait(bfull0 + 8u * slot, (uint32_t)((last / SB) & 1)) && lane == 0) report_timeout(p, abort_flag);
+        }
+        return;
+    }
+
+    if (warp == kMmaWarp) {
+        // -------------------------------------------------- TMEM + MMA issue
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&tmem_base_sh)),
+                     "n"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+        named_barrier(1, kTmemThreads);  // (a) TMEM address published
+        tc_fence_after();
+        const uint32_t tbase = tmem_base_sh;
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((128u >> 4) << 24);
+            // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart (the
+            // leading offset is unused in this mode), layout type 2
+            const uint64_t desc_hi = ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+                                     ((uint64_t)2 << 61);
+            for (int ks = 0; ks < nks; ++ks) {
+                const int g = ks >> 3, a = g & (kASlots - 1), i = ks & 7;
+                const int s = ks / kKs, j = ks - s * kKs, bslot = s % SB;
+                if (i == 0 && !mbar_wait(afull0 + 8u * a, (uint32_t)((g / kASlots) & 1))) {
+                    report_timeout(p, abort_flag);
+                    break;
+                }
+                if (j == 0 && !mbar_wait(bfull0 + 8u * bslot, (uint32_t)((s / SB) & 1))) {
+                    report_timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t baddr = bring + (uint32_t)bslot * kBStageBytes + (uint32_t)(32 * j);
+                const uint64_t desc = desc_hi | (uint64_t)((baddr & 0x3FFFFu) >> 4);
+                umma_f16(tbase + kDCol, tbase + (uint32_t)(a * kAColsPerSlot + 8 * i), desc, idesc,
+                         (uint32_t)(ks != 0));
+                if (i == 7) umma_commit(aempty0 + 8u * a);        // A slot free once these MMAs completed
+                if (j == kKs - 1) umma_commit(bempty0 + 8u * bslot);  // x stage free likewise
+            }
+            umma_commit(dfull);  // every MMA issued above has completed
+        }
+        __syncwarp();
+        named_barrier(2, kTmemThreads);  // (b) the epilogue has read D
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(kTmemCols));
+        return;
+    }
+
+    // ------------------------------------------------------ expand / epilogue warps
+    const int uw = warp - kFirstUnpackWarp;  // 0..7
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int half = uw >> 2;                // expands the groups g with g % 2 == half
+    const int row = q * 32 + lane;           // weight row in the tile = TMEM lane
+    const int64_t n = n0 + row;
+    const int B = p.B;
+    uint16_t *dsm = reinterpret_cast<uint16_t *>(smem + p.off_dsm);  // [B][128] fp16, 0 past N
+
+    for (int i = uw * 32 + lane; i < kRows * B; i += kUnpackWarps * 32) {
+        const int r = i / B, b = i - r * B;  // row-major reads of d
+        dsm[b * kRows + r] = (n0 + r < N) ? p.a.d[(n0 + r) * (int64_t)B + b] : (uint16_t)0;
+    }
+    named_barrier(3, kUnpackWarps * 32);  // d staged
+    named_barrier(1, kTmemThreads);       // (a)
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+    const uint32_t tlane = tbase + ((uint32_t)(q * 32) << 16);
+
+    {
+        bool alive = true;
+        int cur_w = -1;
+        for (int g = half; g < ngroups; g += 2) {
+            const int ws = g >> 2;           // code stage (4 groups)
+            const int u0 = (g & 3) * 2;      // first 16-byte unit of the group in the row
+            const int slot = ws % SW;
+            if (ws != cur_w) {
+                if (cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
+                cur_w = ws;
+                if (alive && !__all_sync(0xffffffffu, mbar_wait(wfull0 + 8u * slot, (uint32_t)((ws / SW) & 1)))) {
+                    if (lane == 0) report_timeout(p, abort_flag);
+                    alive = false;
+                }
+            }
+            const int a = g & (kASlots - 1);
+            if (alive && g >= kASlots &&
+                !__all_sync(0xffffffffu, mbar_wait(aempty0 + 8u * a, (uint32_t)(((g / kASlots) - 1) & 1)))) {
+                if (lane == 0) report_timeout(p, abort_flag);
+                alive = false;
+            }
+            uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+            if (alive) {
+                const uint32_t lbase = wring + (uint32_t)(slot * kWStageBytes + row * 128);
+                c0 = lds128(lbase + ((uint32_t)(u0 ^ (row & 7)) << 4));
+                c1 = lds128(lbase + ((uint32_t)((u0 + 1) ^ (row & 7)) << 4));
+            }
+            const __half hd = __ushort_as_half(dsm[(g >> 1) * kRows + row]);  // block of the group
+            const __half2 dd = __halves2half2(hd, hd);
+            const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t v[32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) expand_word(wd[4 * h2 + i], dd, &v[8 * i]);
+                if (alive) tmem_st32(tlane + (uint32_t)(a * kAColsPerSlot + 32 * h2), v);
+            }
+            if (alive) {
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull0 + 8u * a);
+        }
+        if (cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
+    }
+
+    // epilogue: D column c is activation row m0 + c; this warp takes half of them
+    const bool dok = __all_sync(0xffffffffu, mbar_wait(dfull, 0u));
+    if (!dok && lane == 0) report_timeout(p, abort_flag);
+    tc_fence_after();
+    const bool prologue = p.a.act_scale != 0.0f;
+    const bool store = (*abort_flag == 0) && n < N;
+#pragma unroll 1
+    for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int m = m0 + c0 + j;
+                if (m < M) {
+                    float v = __uint_as_float(r[j]);
+                    if (prologue) v *= p.a.act_scale;
+                    v = requant_out(v, p.a.out_scale, p.a.inv_out);
+                    const int64_t o = (int64_t)m * N + n;
+                    if (p.a.y_f16)
+                        reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(v);
+                    else
+                        reinterpret_cast<float *>(p.a.y)[o] = v;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    named_barrier(2, kTmemThreads);  // (b)
+}
+
+// ------------------------------------------------------------------ host side
+int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+bool make_plan(int BN, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams &p)
+{
+    if (M < 1 || N < 1 || K < 256 || K % 256 != 0 || M > (int64_t)1 << 30) return false;
+    if (K > (int64_t)1 << 24) return false;  // d slice and k-step counts stay small
+    p.B = (int)(K / 256);
+    p.n_tiles = (int)((N + kRows - 1) / kRows);
+    const int64_t tiles = (int64_t)p.n_tiles * ((M + BN - 1) / BN);
+    if (tiles > 0x7FFFFFFF) return false;
+    const int bstage = BN * 128;
+    int off = 0;
+    p.off_bar = off;
+    off += 8 * (4 * kMaxStages + 2 * kASlots + 1);
+    off = align_up(off, 128);
+    p.off_dsm = off;
+    off += align_up(p.B * kRows * 2, 128);
+    p.off_b = off;
+    const int fixed = off + 2048 + 2 * kWStageBytes;  // + alignment slack of both rings
+    int sb = (max_dyn - fixed - 1 * kWStageBytes) / bstage;  // leave room for a third code stage
+    if (sb > kMaxStages) sb = kMaxStages;
+    if (sb < 2) sb = (max_dyn - fixed) / bstage;
+    if (sb < 2) return false;
+    p.sb = sb;
+    off += 1024 + sb * bstage;
+    p.off_w = off;
+    int sw = (max_dyn - off - 1024) / kWStageBytes;
+    if (sw > 3) sw = 3;
+    if (sw < 2) return false;
+    p.sw = sw;
+    p.smem_total = off + 1024 + sw * kWStageBytes;
+    return p.smem_total <= max_dyn;
+}
+
+std::atomic<int> g_gemm_dyn[2][64];
+
+template <int BN>
+int gemm_max_dyn(int device)
+{
+    if (device < 0 || device >= 64) return 0;
+    const int bi = (BN == 256) ? 1 : 0;
+    int v = g_gemm_dyn[bi][device].load();
+    if (v > 0) return v;
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, gemm_tc05_kernel<BN>) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    v = optin - (int)fa.sharedSizeBytes;
+    if (cudaFuncSetAttribute(gemm_tc05_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_gemm_dyn[bi][device].store(v);
+    return v;
+}
+
+// BN = 256 (full tensor-core rate) when that still gives every SM a tile,
+// else 128 (twice the tiles).
+int pick_bn(int64_t M, int64_t N, int device)
+{
+    const int64_t nt = (N + kRows - 1) / kRows;
+    return (nt * ((M + 255) / 256) >= (int64_t)sm_count(device)) ? 256 : 128;
+}
+
+template <int BN>
+cudaError_t launch_gemm(const MatvecArgs &a, int device)
+{
+    GemmParams p{};
+    p.a = a;
+    if (!make_plan(BN, a.M, a.N, a.K, gemm_max_dyn<BN>(device), p)) return cudaErrorInvalidConfiguration;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
+        const cuuint32_t box[2] = {16, (cuuint32_t)kRows};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.qs), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)(a.K * 2)};
+        const cuuint32_t box[2] = {64, (cuuint32_t)BN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(a.x), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const int64_t G = (int64_t)p.n_tiles * ((a.M + BN - 1) / BN);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)p.smem_total;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, p);
+}
+
+}  // namespace
+
+bool gemm_tc05_supported(int64_t M, int64_t N, int64_t K, int device)
+{
+    GemmParams p{};
+    const int bn = pick_bn(M, N, device);
+    const int dyn = (bn == 256) ? gemm_max_dyn<256>(device) : gemm_max_dyn<128>(device);
+    return dyn > 0 && make_plan(bn, M, N, K, dyn, p);
+}
+
+cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device)
+{
+    return (pick_bn(a.M, a.N, device) == 256) ? launch_gemm<256>(a, device) : launch_gemm<128>(a, device);
+}
+
+}  // namespace tq2

@@ -46,6 +46,13 @@ cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *c
 bool tc05_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_tc05(const MatvecArgs &a, int device);
 
+// Ternary GEMM for many activation rows (any M): tcgen05 MMAs over weights
+// expanded to (q - 1) * d in tensor memory, x tiles by TMA.  No prologue
+// (act_scale is applied to the result only; callers with a prologue take the
+// matvec kernels).
+bool gemm_tc05_supported(int64_t M, int64_t N, int64_t K, int device);
+cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device);
+
 // Tensor-core path with pre-scaled x (all four code classes in one
 // accumulator, 8 activation rows per n-tile), M in 1..16.  Returns false
 // when the shape does not fit.

@@ -23,7 +23,7 @@ def L():
 def test_every_declared_symbol_is_exported(L):
     names = tq2.declared_symbols()
     assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
-                          "tq2_matvec_impl", "tq2_matvec_requant",
+                          "tq2_matvec_impl", "tq2_matvec_requant", "tq2_gemm",
                           "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
@@ -83,6 +83,27 @@ def test_requant_rejects_bad_arguments(L):
     assert rq(L, y=A2) == ALIGN
     assert rq(L, M=0, x=NUL, y=NUL) == OK
     assert rq(L, N=0, qs=NUL, d=NUL, y=NUL, so=0.0) == OK
+
+
+def gm(L, x=A16, M=64, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, so=0.0, st=NUL, impl=0):
+    return L.tq2_gemm(x, M, qs, d, N, K, y, yd, s, so, st, S, impl)
+
+
+def test_gemm_rejects_bad_arguments(L):
+    assert gm(L, K=300) == SHAPE
+    assert gm(L, M=-1) == SHAPE
+    assert gm(L, M=2 ** 31) == SHAPE
+    assert gm(L, yd=2) == DTYPE
+    assert gm(L, s=-1.0) == ARG
+    assert gm(L, so=float("nan")) == ARG
+    assert gm(L, impl=3) == ARG
+    assert gm(L, impl=-1) == ARG
+    assert gm(L, impl=1, s=0.05) == ARG  # the tcgen05 GEMM takes no prologue
+    assert gm(L, x=NUL) == NULL
+    assert gm(L, y=NUL) == NULL
+    assert gm(L, x=A2) == ALIGN
+    assert gm(L, M=0, x=NUL, y=NUL) == OK
+    assert gm(L, N=0, qs=NUL, d=NUL, y=NUL) == OK
 
 
 def test_matvec_empty_shapes_are_noops(L):
