@@ -17,17 +17,20 @@
 //   * warp 0 streams the packed codes: 2-D TMA boxes of 128 rows x 128 bytes
 //     (512 codes), 128-byte swizzle, before griddepcontrol.wait (weights never
 //     depend on earlier kernels);
-//   * warp 1 streams x after griddepcontrol.wait: per stage one TMA box of
-//     64 values (4 k-steps) x BN rows, 128 bytes per row with the 128-byte
+//   * warp 1 streams x after griddepcontrol.wait: per stage (8 k-steps) two
+//     TMA boxes of 64 values x BN rows, 128 bytes per row with the 128-byte
 //     swizzle, which is the K-major SWIZZLE_128B operand layout the MMA reads
-//     (8-row groups 1024 bytes apart; k-step j of the stage starts 32 bytes
+//     (8-row groups 1024 bytes apart; k-step j of a box starts 32 j bytes
 //     into the row); rows past M read as 0;
 //   * warp 2 allocates the 512 TMEM columns (after the wait, so the previous
-//     kernel's tensor memory is free) and one lane issues the MMAs;
+//     kernel's tensor memory is free) and one lane issues the MMAs, 8 per
+//     stage, then releases the stage's A slot and x buffer with one commit
+//     (a commit stalls the issuing thread for hundreds of cycles on this
+//     part, so there is one per 8 MMAs);
 //   * warps 3..10 (two per TMEM lane quadrant) stage d, then expand 8 k-steps
 //     at a time: for code pair (2j, 2j+1) of a 16-code word, the fp16 pair
 //     (1024 + q) - 1025 = q - 1 (exact) times d_b, written with tcgen05.st
-//     into a 4-slot ring of 64 TMEM columns; at the end they read D (one
+//     into a ring of 64-column TMEM slots (one per stage); at the end they read D (one
 //     column per activation row) and store y, with the optional int8
 //     requantisation at store.
 // Every mbarrier wait is bounded; a wait that runs out sets TQ2_FLAG_TIMEOUT.
@@ -54,7 +57,7 @@ constexpr int kUnpackWarps = 8;
 constexpr int kThreads = (kFirstUnpackWarp + kUnpackWarps) * 32;  // 352
 constexpr int kTmemThreads = (kUnpackWarps + 1) * 32;            // MMA warp + unpack warps
 constexpr int kRows = 128;               // weight rows per tile (MMA M, TMEM lanes)
-constexpr int kKs = 4;                   // k-steps (16 codes) per x stage
+constexpr int kKs = 8;                   // k-steps (16 codes) per stage: one A slot, two x boxes
 constexpr int kWStageBytes = 16384;      // 128 rows x 128 bytes of codes (32 k-steps)
 constexpr int kASlots = 4;               // TMEM A ring
 constexpr int kAColsPerSlot = 64;        // 8 k-steps x 8 columns
@@ -68,7 +71,7 @@ struct GemmParams {
     MatvecArgs a;
     int n_tiles;       // weight-row tiles (ceil(N / 128)); blockIdx = m_tile * n_tiles + n_tile
     int B;             // 256-blocks per row
-    int sw, sb;        // ring depths: codes, x
+    int sw, sb;        // ring depths: codes; stages (A slots and x buffers, <= 4)
     int off_bar, off_dsm, off_w, off_b, smem_total;
 };
 
@@ -162,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     volatile int *abort_flag = &abort_sh;
-    constexpr uint32_t kBStageBytes = (uint32_t)BN * 128u;  // 64 values (kKs k-steps) per row
+    constexpr uint32_t kBoxBytes = (uint32_t)BN * 128u;     // 64 values per row
+    constexpr uint32_t kBStageBytes = 2u * kBoxBytes;       // kKs = 8 k-steps
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t N = p.a.N, K = p.a.K;
@@ -173,14 +177,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const int nks = (int)(K / 16);               // k-steps
     const int ngroups = nks / 8;                 // TMEM A fills (8 k-steps each)
     const int nwst = (int)((K + 511) / 512);     // code stages (128 bytes of codes per row)
-    const int nbst = nks / kKs;                  // x stages
+    const int nbst = nks / kKs;                  // stages (= ngroups)
     const int SW = p.sw, SB = p.sb;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     const uint32_t wfull0 = smem_addr(bars), wempty0 = wfull0 + 8u * SW;
-    const uint32_t bfull0 = wempty0 + 8u * SW, bempty0 = bfull0 + 8u * SB;
-    const uint32_t afull0 = bempty0 + 8u * SB, aempty0 = afull0 + 8u * kASlots;
-    const uint32_t dfull = aempty0 + 8u * kASlots;
+    // stage slot r: bfull (x landed), afull (A slot written), sempty (the
+    // MMAs of the stage completed: both the A slot and the x buffer are free)
+    const uint32_t bfull0 = wempty0 + 8u * SW, afull0 = bfull0 + 8u * SB;
+    const uint32_t sempty0 = afull0 + 8u * SB;
+    const uint32_t dfull = sempty0 + 8u * SB;
     // both rings must be 1024-byte aligned for the 128-byte swizzle (the plan
     // reserves the slack)
     const uint32_t wring = (smem_addr(smem + p.off_w) + 1023u) & ~1023u;
@@ -194,11 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(bfull0 + 8u * i, 1);
-            mbar_init(bempty0 + 8u * i, 1);
-        }
-        for (int i = 0; i < kASlots; ++i) {
             mbar_init(afull0 + 8u * i, 4);
-            mbar_init(aempty0 + 8u * i, 1);
+            mbar_init(sempty0 + 8u * i, 1);
         }
         mbar_init(dfull, 1);
         abort_sh = 0;
@@ -239,16 +242,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         int issued = 0;
         for (int s = 0; s < nbst; ++s) {
             const int slot = s % SB, round = s / SB;
-            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(bempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(sempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             const uint32_t full = bfull0 + 8u * slot;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full, kBStageBytes);
-                tensor2d_g2s(bring + (uint32_t)slot * kBStageBytes, &p.xmap, 16 * kKs * s, m0, full, pol);
-            }
+            if (lane == 0) mbar_arrive_expect_tx(full, kBStageBytes);
+            __syncwarp();
+            if (lane < 2)
+                tensor2d_g2s(bring + (uint32_t)slot * kBStageBytes + (uint32_t)lane * kBoxBytes, &p.xmap,
+                             16 * kKs * s + 64 * lane, m0, full, pol);
             __syncwarp();
             issued = s + 1;
         }
@@ -276,24 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             // leading offset is unused in this mode), layout type 2
             const uint64_t desc_hi = ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
                                      ((uint64_t)2 << 61);
-            for (int ks = 0; ks < nks; ++ks) {
-                const int g = ks >> 3, a = g & (kASlots - 1), i = ks & 7;
-                const int s = ks / kKs, j = ks - s * kKs, bslot = s % SB;
-                if (i == 0 && !mbar_wait(afull0 + 8u * a, (uint32_t)((g / kASlots) & 1))) {
-                    report_timeout(p, abort_flag);
-                    break;
-                }
-                if (j == 0 && !mbar_wait(bfull0 + 8u * bslot, (uint32_t)((s / SB) & 1))) {
+            for (int g = 0; g < ngroups; ++g) {
+                const int r = g % SB;
+                const uint32_t par = (uint32_t)((g / SB) & 1);
+                if (!mbar_wait(afull0 + 8u * r, par) || !mbar_wait(bfull0 + 8u * r, par)) {
                     report_timeout(p, abort_flag);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t baddr = bring + (uint32_t)bslot * kBStageBytes + (uint32_t)(32 * j);
-                const uint64_t desc = desc_hi | (uint64_t)((baddr & 0x3FFFFu) >> 4);
-                umma_f16(tbase + kDCol, tbase + (uint32_t)(a * kAColsPerSlot + 8 * i), desc, idesc,
-                         (uint32_t)(ks != 0));
-                if (i == 7) umma_commit(aempty0 + 8u * a);        // A slot free once these MMAs completed
-                if (j == kKs - 1) umma_commit(bempty0 + 8u * bslot);  // x stage free likewise
+                const uint32_t b0 = bring + (uint32_t)r * kBStageBytes;
+#pragma unroll
+                for (int i = 0; i < kKs; ++i) {
+                    const uint32_t baddr = b0 + (uint32_t)(i >> 2) * kBoxBytes + (uint32_t)(32 * (i & 3));
+                    const uint64_t desc = desc_hi | (uint64_t)((baddr & 0x3FFFFu) >> 4);
+                    umma_f16(tbase + kDCol, tbase + (uint32_t)(r * kAColsPerSlot + 8 * i), desc, idesc,
+                             (uint32_t)(g != 0 || i != 0));
+                }
+                umma_commit(sempty0 + 8u * r);  // A slot and x buffer free once these MMAs completed
             }
             umma_commit(dfull);  // every MMA issued above has completed
         }
@@ -338,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                     alive = false;
                 }
             }
-            const int a = g & (kASlots - 1);
-            if (alive && g >= kASlots &&
-                !__all_sync(0xffffffffu, mbar_wait(aempty0 + 8u * a, (uint32_t)(((g / kASlots) - 1) & 1)))) {
+            const int a = g % SB;  // stage slot: TMEM A slot a
+            if (alive && g >= SB &&
+                !__all_sync(0xffffffffu, mbar_wait(sempty0 + 8u * a, (uint32_t)(((g / SB) - 1) & 1)))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 alive = false;
             }
@@ -413,7 +416,7 @@ bool make_plan(int BN, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams 
     p.n_tiles = (int)((N + kRows - 1) / kRows);
     const int64_t tiles = (int64_t)p.n_tiles * ((M + BN - 1) / BN);
     if (tiles > 0x7FFFFFFF) return false;
-    const int bstage = BN * 128;
+    const int bstage = 2 * BN * 128;
     int off = 0;
     p.off_bar = off;
     off += 8 * (4 * kMaxStages + 2 * kASlots + 1);
@@ -423,7 +426,7 @@ bool make_plan(int BN, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams 
     p.off_b = off;
     const int fixed = off + 2048 + 2 * kWStageBytes;  // + alignment slack of both rings
     int sb = (max_dyn - fixed - 1 * kWStageBytes) / bstage;  // leave room for a third code stage
-    if (sb > kMaxStages) sb = kMaxStages;
+    if (sb > kASlots) sb = kASlots;                              // one TMEM A slot per stage
     if (sb < 2) sb = (max_dyn - fixed) / bstage;
     if (sb < 2) return false;
     p.sb = sb;
