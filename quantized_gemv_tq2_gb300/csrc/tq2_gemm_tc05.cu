@@ -14,9 +14,9 @@
 // Tile: 128 weight rows (the MMA's M, one TMEM lane each) x BN activation rows
 // (the MMA's N, 128 or 256), all of K; tcgen05.mma.cta_group::1.kind::f16,
 // K = 16 per instruction.
-//   * warp 0 streams the packed codes: 2-D TMA boxes of 128 rows x 128 bytes
-//     (512 codes), 128-byte swizzle, before griddepcontrol.wait (weights never
-//     depend on earlier kernels);
+//   * warp 0 streams the packed codes: 2-D TMA boxes of 128 rows x 64 bytes
+//     (one 256-block), before griddepcontrol.wait (weights never depend on
+//     earlier kernels);
 //   * warp 1 streams x after griddepcontrol.wait: per stage (8 k-steps) two
 //     TMA boxes of 64 values x BN rows, 128 bytes per row with the 128-byte
 //     swizzle, which is the K-major SWIZZLE_128B operand layout the MMA reads
@@ -58,7 +58,7 @@ constexpr int kThreads = (kFirstUnpackWarp + kUnpackWarps) * 32;  // 352
 constexpr int kTmemThreads = (kUnpackWarps + 1) * 32;            // MMA warp + unpack warps
 constexpr int kRows = 128;               // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kKs = 8;                   // k-steps (16 codes) per stage: one A slot, two x boxes
-constexpr int kWStageBytes = 16384;      // 128 rows x 128 bytes of codes (32 k-steps)
+constexpr int kWStageBytes = 8192;       // 128 rows x 64 bytes of codes (16 k-steps, one 256-block)
 constexpr int kASlots = 4;               // TMEM A ring
 constexpr int kAColsPerSlot = 64;        // 8 k-steps x 8 columns
 constexpr int kDCol = 256;               // D (fp32, BN columns) starts here
@@ -66,7 +66,7 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxStages = 8;
 
 struct GemmParams {
-    CUtensorMap wmap;  // qs as uint64 [N][K/32]; box {16, 128}; 128-byte swizzle
+    CUtensorMap wmap;  // qs as uint64 [N][K/32]; box {8, 128}; no swizzle
     CUtensorMap xmap;  // x as fp16 [M][K]; box {64, BN}; 128-byte swizzle
     MatvecArgs a;
     int n_tiles;       // weight-row tiles (ceil(N / 128)); blockIdx = m_tile * n_tiles + n_tile
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const int m0 = mtile * BN;
     const int nks = (int)(K / 16);               // k-steps
     const int ngroups = nks / 8;                 // TMEM A fills (8 k-steps each)
-    const int nwst = (int)((K + 511) / 512);     // code stages (128 bytes of codes per row)
+    const int nwst = (int)(K / 256);             // code stages (64 bytes of codes per row)
     const int nbst = nks / kKs;                  // stages (= ngroups)
     const int SW = p.sw, SB = p.sb;
 
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const uint32_t bfull0 = wempty0 + 8u * SW, afull0 = bfull0 + 8u * SB;
     const uint32_t sempty0 = afull0 + 8u * SB;
     const uint32_t dfull = sempty0 + 8u * SB;
-    // both rings must be 1024-byte aligned for the 128-byte swizzle (the plan
-    // reserves the slack)
+    // the x ring must be 1024-byte aligned for the 128-byte swizzle (the plan
+    // reserves the slack; both rings move together)
     const uint32_t wring = (smem_addr(smem + p.off_w) + 1023u) & ~1023u;
     const uint32_t bring = (smem_addr(smem + p.off_b) + 1023u) & ~1023u;
 
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             if (lane == 0) {
                 const uint32_t full = wfull0 + 8u * slot;
                 mbar_arrive_expect_tx(full, (uint32_t)kWStageBytes);
-                tensor2d_g2s(wring + (uint32_t)(slot * kWStageBytes), &p.wmap, 16 * s, (int)n0, full, pol);
+                tensor2d_g2s(wring + (uint32_t)(slot * kWStageBytes), &p.wmap, 8 * s, (int)n0, full, pol);
             }
             __syncwarp();
             issued = s + 1;
@@ -330,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         bool alive = true;
         int cur_w = -1;
         for (int g = half; g < ngroups; g += 2) {
-            const int ws = g >> 2;           // code stage (4 groups)
-            const int u0 = (g & 3) * 2;      // first 16-byte unit of the group in the row
+            const int ws = g >> 1;           // code stage (2 groups)
+            const int u0 = (g & 1) * 2;      // first 16-byte unit of the group in the row
             const int slot = ws % SW;
             if (ws != cur_w) {
                 if (cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
@@ -349,9 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             }
             uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
             if (alive) {
-                const uint32_t lbase = wring + (uint32_t)(slot * kWStageBytes + row * 128);
-                c0 = lds128(lbase + ((uint32_t)(u0 ^ (row & 7)) << 4));
-                c1 = lds128(lbase + ((uint32_t)((u0 + 1) ^ (row & 7)) << 4));
+                const uint32_t lbase = wring + (uint32_t)(slot * kWStageBytes + row * 64);
+                c0 = lds128(lbase + (uint32_t)(u0 << 4));
+                c1 = lds128(lbase + (uint32_t)((u0 + 1) << 4));
             }
             const __half hd = __ushort_as_half(dsm[(g >> 1) * kRows + row]);  // block of the group
             const __half2 dd = __halves2half2(hd, hd);
@@ -422,21 +422,22 @@ bool make_plan(int BN, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams 
     off += 8 * (4 * kMaxStages + 2 * kASlots + 1);
     off = align_up(off, 128);
     p.off_dsm = off;
-    off += align_up(p.B * kRows * 2, 128);
+    off += p.B * kRows * 2;
+    // both rings at multiples of 1024 from the base: the runtime rounding of
+    // the base then shifts them alike, and one 1024-byte slack covers it
+    off = align_up(off, 1024);
     p.off_b = off;
-    const int fixed = off + 2048 + 2 * kWStageBytes;  // + alignment slack of both rings
-    int sb = (max_dyn - fixed - 1 * kWStageBytes) / bstage;  // leave room for a third code stage
-    if (sb > kASlots) sb = kASlots;                              // one TMEM A slot per stage
-    if (sb < 2) sb = (max_dyn - fixed) / bstage;
+    int sb = (max_dyn - off - 1024 - 2 * kWStageBytes) / bstage;
+    if (sb > kASlots) sb = kASlots;  // one TMEM A slot per stage
     if (sb < 2) return false;
     p.sb = sb;
-    off += 1024 + sb * bstage;
+    off += sb * bstage;
     p.off_w = off;
     int sw = (max_dyn - off - 1024) / kWStageBytes;
-    if (sw > 3) sw = 3;
+    if (sw > 4) sw = 4;
     if (sw < 2) return false;
     p.sw = sw;
-    p.smem_total = off + 1024 + sw * kWStageBytes;
+    p.smem_total = off + sw * kWStageBytes + 1024;
     return p.smem_total <= max_dyn;
 }
 
@@ -484,10 +485,10 @@ cudaError_t launch_gemm(const MatvecArgs &a, int device)
     {
         const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
         const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
-        const cuuint32_t box[2] = {16, (cuuint32_t)kRows};
+        const cuuint32_t box[2] = {8, (cuuint32_t)kRows};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.qs), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
