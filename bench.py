@@ -280,6 +280,47 @@ def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None):
     return out
 
 
+def _bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS bf16, burst)"
+    except Exception:
+        return 1900.0, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
+
+
+def prefill_gemm(torch, tq2, st, stream, M_list=(512, 2048)):
+    """tq2_gemm (tcgen05) on the layer shapes with M activation rows (a prompt
+    chunk): us per call and TFLOP/s (2 M N K), against the measured dense
+    bf16 tensor peak (fp16 runs at the same rate)."""
+    import tq2_synth as syn
+    peak, src = _bf16_peak()
+    out = {"peak_tflops": peak, "peak_source": src}
+    dev = st["X"].device
+    for gname, names in SHAPE_GROUPS.items():
+        i = [j for j, (L, n, N, K) in enumerate(st["lin"]) if n in names][0]
+        N, K = st["lin"][i][2], st["lin"][i][3]
+        for M in M_list:
+            x = torch.from_numpy(syn.activations(SEED + 11, M, K, linear=0)).to(dev)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    tq2.gemm(x, st["qs"][i], st["d"][i], y=y)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                reps = 20
+                e0.record(stream)
+                for _ in range(reps):
+                    tq2.gemm(x, st["qs"][i], st["d"][i], y=y)
+                e1.record(stream)
+            stream.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+            out[f"{gname}_M{M}"] = dict(us_per_call=us, tflops=tf, frac_of_peak=tf / peak)
+            del x, y
+    return out
+
+
 def cpu_baseline_oracle(budget_s=10.0):
     """The CPU oracle (fp64, one thread, as it stands) on layer 0 of the stack."""
     import numpy as np
@@ -416,6 +457,7 @@ def run_gpu(args):
         sweep = shape_graphs(torch, tq2, st, stream, M_list=(2, 4, 8, 16),
                              groups=("gateup_16384x4096", "down_4096x16384"))
         extras["m_sweep"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep.items()}
+        extras["prefill_gemm"] = prefill_gemm(torch, tq2, st, stream)
 
     peak, peak_src = _peak()
     value = job_gbs(world, STACK_BYTES, ms)
@@ -487,7 +529,7 @@ CASES = {"gateup": (16384, 4096), "down": (4096, 16384), "qo": (4096, 4096), "kv
 def run_case(args):
     """A small case for ncu: `copies` distinct weight sets of one shape (more
     than L2 in total for the big shapes), `launches` eager tq2_matvec calls
-    round-robin over them.  Prints the mean wall time per call (not a bench
+    (tq2_gemm when M > 16) round-robin over them.  Prints the mean wall time per call (not a bench
     value: the calls are eager and may run under a profiler)."""
     import torch
     import quantized_gemv_tq2_gb300 as tq2
@@ -507,7 +549,10 @@ def run_case(args):
     t0 = time.perf_counter()
     for i in range(args.launches):
         qs, d = ws[i % len(ws)]
-        tq2.matvec(x, qs, d, y=y, impl=args.case_impl)
+        if args.M > 16:  # prefill-sized M: tq2_gemm
+            tq2.gemm(x, qs, d, y=y)
+        else:
+            tq2.matvec(x, qs, d, y=y, impl=args.case_impl)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / args.launches
     print(json.dumps({"case": args.case, "N": N, "K": K, "M": args.M, "copies": args.copies,
