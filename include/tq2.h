@@ -227,12 +227,12 @@ TQ2_API tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_
  *   impl       0 = automatic, 1 = the tcgen05 GEMM (5th-generation tensor
  *              cores: weights expanded once per 128-row tile into exact fp16
  *              (q - 1) * d_b in tensor memory, x tiles by TMA, fp32
- *              accumulation over all of K; no prologue: act_scale must be 0),
- *              2 = the matvec kernels on 16-row slices of x.  Automatic takes
- *              the GEMM for M > 16 without a prologue, the slices otherwise.
+ *              accumulation over all of K; the prologue fake-quantises each
+ *              x tile in shared memory), 2 = the matvec kernels on 16-row
+ *              slices of x.  Automatic takes the GEMM for M > 16, the slices
+ *              otherwise.
  * Errors and accuracy as tq2_matvec (TQ2_ERR_SHAPE for M out of range;
- * TQ2_ERR_ARG for impl out of range, impl 1 with act_scale != 0, or a shape
- * impl 1 cannot plan).
+ * TQ2_ERR_ARG for impl out of range or a shape impl 1 cannot plan).
  */
 TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
                             int64_t K, void *y, tq2_dtype y_dtype, float act_scale, float out_scale,

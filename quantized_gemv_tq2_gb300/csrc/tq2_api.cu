@@ -298,7 +298,6 @@ tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint1
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
     if (!(out_scale >= 0.0f) || !std::isfinite(out_scale)) return TQ2_ERR_ARG;
     if (impl < 0 || impl > 2) return TQ2_ERR_ARG;
-    if (impl == 1 && act_scale != 0.0f) return TQ2_ERR_ARG;  // the tcgen05 GEMM has no prologue
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
     if (K > 0 && (x == nullptr || qs == nullptr || d == nullptr)) return TQ2_ERR_NULL;
@@ -311,10 +310,10 @@ tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint1
 
     int dev = 0;
     if ((st = current_device(&dev)) != TQ2_OK) return st;
-    // impl 0: the tcgen05 GEMM for M > 16 without a prologue, else the
-    // matvec kernels on 16-row slices of x (the same result contract)
+    // impl 0: the tcgen05 GEMM for M > 16, else the matvec kernels on 16-row
+    // slices of x (the same result contract)
     bool gemm = (impl == 1);
-    if (impl == 0) gemm = M > 16 && act_scale == 0.0f && tq2::gemm_tc05_supported(M, N, K, dev);
+    if (impl == 0) gemm = M > 16 && tq2::gemm_tc05_supported(M, N, K, dev);
     if (gemm) {
         if (!tq2::gemm_tc05_supported(M, N, K, dev)) return TQ2_ERR_ARG;
         tq2::MatvecArgs a;

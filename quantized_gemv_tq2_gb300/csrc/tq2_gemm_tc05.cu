@@ -30,7 +30,11 @@
 //   * warps 3..10 (two per TMEM lane quadrant) stage d, then expand 8 k-steps
 //     at a time: for code pair (2j, 2j+1) of a 16-code word, the fp16 pair
 //     (1024 + q) - 1025 = q - 1 (exact) times d_b, written with tcgen05.st
-//     into a ring of 64-column TMEM slots (one per stage); at the end they read D (one
+//     into a ring of 64-column TMEM slots (one per stage); with the int8
+//     prologue they also fake-quantise each x stage in shared memory first
+//     (element-wise, 1/8 of the stage per warp) and release it to the MMA
+//     issuer (a generic-to-async proxy fence, then an mbarrier); at the end
+//     they read D (one
 //     column per activation row) and store y, with the optional int8
 //     requantisation at store.
 // Every mbarrier wait is bounded; a wait that runs out sets TQ2_FLAG_TIMEOUT.
@@ -182,11 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     const uint32_t wfull0 = smem_addr(bars), wempty0 = wfull0 + 8u * SW;
-    // stage slot r: bfull (x landed), afull (A slot written), sempty (the
-    // MMAs of the stage completed: both the A slot and the x buffer are free)
-    const uint32_t bfull0 = wempty0 + 8u * SW, afull0 = bfull0 + 8u * SB;
+    // stage slot r: bfull (x landed), bconv (x fake-quantised, prologue
+    // only), afull (A slot written), sempty (the MMAs of the stage completed:
+    // both the A slot and the x buffer are free)
+    const uint32_t bfull0 = wempty0 + 8u * SW, bconv0 = bfull0 + 8u * SB, afull0 = bconv0 + 8u * SB;
     const uint32_t sempty0 = afull0 + 8u * SB;
     const uint32_t dfull = sempty0 + 8u * SB;
+    const bool prologue = p.a.act_scale != 0.0f;
     // the x ring must be 1024-byte aligned for the 128-byte swizzle (the plan
     // reserves the slack; both rings move together)
     const uint32_t wring = (smem_addr(smem + p.off_w) + 1023u) & ~1023u;
@@ -200,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(bfull0 + 8u * i, 1);
+            mbar_init(bconv0 + 8u * i, kUnpackWarps);
             mbar_init(afull0 + 8u * i, 4);
             mbar_init(sempty0 + 8u * i, 1);
         }
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             for (int g = 0; g < ngroups; ++g) {
                 const int r = g % SB;
                 const uint32_t par = (uint32_t)((g / SB) & 1);
-                if (!mbar_wait(afull0 + 8u * r, par) || !mbar_wait(bfull0 + 8u * r, par)) {
+                if (!mbar_wait(afull0 + 8u * r, par) || !mbar_wait((prologue ? bconv0 : bfull0) + 8u * r, par)) {
                     report_timeout(p, abort_flag);
                     break;
                 }
@@ -329,7 +336,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     {
         bool alive = true;
         int cur_w = -1;
-        for (int g = half; g < ngroups; g += 2) {
+        for (int g = prologue ? 0 : half; g < ngroups; g += prologue ? 1 : 2) {
+            if (prologue) {
+                // x' = clamp(rint(x * (1/s)), -128, 127) (times s at the store),
+                // this warp's 1/8 of stage g, in place
+                const int r = g % SB;
+                if (alive &&
+                    !__all_sync(0xffffffffu, mbar_wait(bfull0 + 8u * (uint32_t)r, (uint32_t)((g / SB) & 1)))) {
+                    if (lane == 0) report_timeout(p, abort_flag);
+                    alive = false;
+                }
+                if (alive) {
+                    const uint32_t xb = bring + (uint32_t)r * (2u * BN * 128u);
+                    for (int c = uw * 32 + lane; c < 2 * BN * 8; c += kUnpackWarps * 32) {
+                        const uint4 v = lds128(xb + (uint32_t)c * 16u);
+                        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                            const __half2 h = __floats2half2_rn(fq_code(f.x, p.a.inv_scale), fq_code(f.y, p.a.inv_scale));
+                            w[e] = *reinterpret_cast<const uint32_t *>(&h);
+                        }
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xb + (uint32_t)c * 16u),
+                                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                     : "memory");
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA reads
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bconv0 + 8u * (uint32_t)r);
+                if ((g & 1) != half) continue;  // the other half expands this group's A
+            }
             const int ws = g >> 1;           // code stage (2 groups)
             const int u0 = (g & 1) * 2;      // first 16-byte unit of the group in the row
             const int slot = ws % SW;
@@ -377,7 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const bool dok = __all_sync(0xffffffffu, mbar_wait(dfull, 0u));
     if (!dok && lane == 0) report_timeout(p, abort_flag);
     tc_fence_after();
-    const bool prologue = p.a.act_scale != 0.0f;
     const bool store = (*abort_flag == 0) && n < N;
 #pragma unroll 1
     for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
@@ -419,7 +455,7 @@ bool make_plan(int BN, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams 
     const int bstage = 2 * BN * 128;
     int off = 0;
     p.off_bar = off;
-    off += 8 * (4 * kMaxStages + 2 * kASlots + 1);
+    off += 8 * (2 * kMaxStages + 4 * kASlots + 1);  // code ring 2 x sw, stage ring 4 x sb, dfull
     off = align_up(off, 128);
     p.off_dsm = off;
     off += p.B * kRows * 2;

@@ -47,9 +47,8 @@ bool tc05_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_tc05(const MatvecArgs &a, int device);
 
 // Ternary GEMM for many activation rows (any M): tcgen05 MMAs over weights
-// expanded to (q - 1) * d in tensor memory, x tiles by TMA.  No prologue
-// (act_scale is applied to the result only; callers with a prologue take the
-// matvec kernels).
+// expanded to (q - 1) * d in tensor memory, x tiles by TMA (fake-quantised in
+// shared memory when act_scale != 0).
 bool gemm_tc05_supported(int64_t M, int64_t N, int64_t K, int device);
 cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device);
 

@@ -98,7 +98,6 @@ def test_gemm_rejects_bad_arguments(L):
     assert gm(L, so=float("nan")) == ARG
     assert gm(L, impl=3) == ARG
     assert gm(L, impl=-1) == ARG
-    assert gm(L, impl=1, s=0.05) == ARG  # the tcgen05 GEMM takes no prologue
     assert gm(L, x=NUL) == NULL
     assert gm(L, y=NUL) == NULL
     assert gm(L, x=A2) == ALIGN

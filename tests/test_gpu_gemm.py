@@ -1,8 +1,9 @@
 """GPU parity of tq2_gemm (any number of activation rows: prefill) against the
 CPU oracle: element by element within |dy| <= 1e-3 * sum_k |d_b x'_k| + 1e-6,
-bit-exact on one-hot x (every product and sum exact), ragged tiles in both
-dimensions, the 16-row-slice path with the prologue, requantisation at store,
-determinism, and sampled rows at a prefill-sized layer shape."""
+bit-exact on one-hot x (every product and sum exact, with and without the
+int8 prologue), ragged tiles in both dimensions, the prologue and the
+requantisation at store on both paths (tcgen05 GEMM and 16-row slices),
+determinism, and sampled rows at prefill-sized layer shapes."""
 import numpy as np
 import pytest
 
@@ -67,28 +68,35 @@ def test_gemm_one_hot_is_exact(T):
         assert np.array_equal(y, ye), f"impl={impl}: {int((y != ye).sum())} elements differ"
 
 
-def test_gemm_prologue_and_requant(T):
-    case = Case(seed=9, M=40, N=200, K=2048, heavy=True, prologue=True)
-    y_ref, tol = case.reference()
-    y = _gemm(T, case, 0)  # a prologue takes the 16-row slices
-    assert_within_tolerance(y, y_ref, tol, "prologue")
+@pytest.mark.parametrize("M,N,K", [(40, 200, 2048), (130, 257, 768), (300, 128, 4096)])
+def test_gemm_prologue_and_requant(T, M, N, K):
+    """The fused int8 prologue (x fake-quantised in shared memory on the
+    tcgen05 path) and the requantisation at store, both paths."""
     from test_gpu_requant import check_requant
+    case = Case(seed=9 + M, M=M, N=N, K=K, heavy=True, prologue=True)
+    y_ref, tol = case.reference()
     s_o = float(np.float32(np.abs(y_ref).max() / 100.0))
-    for impl, c in ((2, case), (1, Case(seed=9, M=40, N=200, K=2048, heavy=True))):
-        yr, tr = c.reference()
-        if impl == 1:
-            s_o = float(np.float32(np.abs(yr).max() / 100.0))
+    for impl in (1, 0, 2):
+        y = _gemm(T, case, impl)
+        assert_within_tolerance(y, y_ref, tol, f"prologue impl={impl}")
         for yd in (0, 1):
-            yq = _gemm(T, c, impl, y_dtype=yd, out_scale=s_o)
-            check_requant(yq.astype(np.float32 if yd == 0 else np.float16), yr, tr, s_o, yd, f"requant impl={impl}")
+            yq = _gemm(T, case, impl, y_dtype=yd, out_scale=s_o)
+            check_requant(yq.astype(np.float32 if yd == 0 else np.float16), y_ref, tol, s_o, yd,
+                          f"prologue+requant impl={impl} yd={yd}")
 
 
-def test_gemm_rejects_prologue_on_tcgen05(T):
-    import quantized_gemv_tq2_gb300 as tq2
-    case = Case(seed=1, M=32, N=64, K=256, prologue=True)
-    x, qs, d = case.device()
-    with pytest.raises(tq2.TQ2Error):
-        tq2.gemm(x, qs, d, act_scale=case.s, impl=1)
+def test_gemm_prologue_one_hot_is_exact(T):
+    """With the prologue, x' = s * code: one-hot x of value 3 s gives
+    y = s * 3 * (q - 1) * d exactly (codes, products and the sum are exact)."""
+    M, N, K = 64, 128, 512
+    case = Case(seed=6, M=M, N=N, K=K, prologue=True)
+    ks = (np.arange(M) * 53 + 5) % K
+    x = np.zeros((M, K), dtype=np.float16)
+    x[np.arange(M), ks] = np.float16(3.0 * case.s)
+    case.x = x
+    ye = oracle.matvec_exact(x, case.qs, case.d, K, case.s)
+    y = _gemm(T, case, 1)
+    assert np.array_equal(y.astype(np.float32), ye.astype(np.float32))
 
 
 def test_gemm_is_deterministic(T):
