@@ -82,6 +82,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
 }
 
+// For short producer/consumer hand-offs: spin on the non-blocking test
+// first; only a long wait falls back to the suspending try_wait.  Gives up
+// after kTimeoutNs like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
+{
+#pragma unroll 1
+    for (int i = 0; i < 2048; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity);
+}
+
+__device__ __forceinline__ uint64_t evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy()
 {
     uint64_t pol;
@@ -107,6 +125,21 @@ __device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap *ma
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
         : "memory");
+}
+
+__device__ __forceinline__ void tensor3d_g2s(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                             uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // D = A * B + D
@@ -151,6 +184,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 __device__ __forceinline__ float lds_f32(uint32_t addr)

@@ -84,11 +84,6 @@ __device__ __forceinline__ void report_timeout(const PsParams &p, volatile int *
     if (p.a.status) atomicOr(p.a.status, TQ2_FLAG_TIMEOUT);
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
 
 // Byte offsets of one block's B fragments and per-column scalars.
 //   frag:  block bx (within the x chunk) holds 512*M bytes; n-tile nt starts

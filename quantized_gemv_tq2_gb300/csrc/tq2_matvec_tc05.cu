@@ -53,6 +53,7 @@
 
 #include "tq2_device.cuh"
 #include "tq2_internal.cuh"
+#include "tq2_tcgen05.cuh"
 
 namespace tq2 {
 namespace {
@@ -67,7 +68,6 @@ constexpr int kAColsPerSlot = 64;  // 8 k-steps x 8 columns (32 bytes of codes p
 constexpr int kASlots = 4;
 constexpr int kDCol = 256;          // D regions start here (16 columns per 256-block)
 constexpr int kTargetSmem = 112 * 1024;
-constexpr unsigned long long kTimeoutNs = 200ull * 1000 * 1000;
 
 struct Tc05Params {
     CUtensorMap wmap;  // qs as uint64 [K/512 chunks][N rows][16]; box {16, R, C}; 128B swizzle
@@ -86,132 +86,8 @@ struct Tc05Params {
     uint32_t b_lbo;    // byte distance from the B0 to the B1 array
 };
 
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity), "n"(20000) : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Wait for the phase with the given parity; false after kTimeoutNs.  The
-// producer/consumer hand-offs here are short, so spin on the non-blocking
-// test first; only a long wait falls back to the suspending try_wait.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-#pragma unroll 1
-    for (int i = 0; i < 2048; ++i)
-        if (mbar_test_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
-    }
-}
-__device__ __forceinline__ uint64_t evict_first_policy()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void tensor3d_g2s(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
-                                             uint32_t bar, uint64_t pol)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol)
-        : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void named_barrier(int id, int threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive TMEM columns of this warp's lane quadrant
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr)
-{
-    uint32_t v;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// D[taddr] (+)= A[a_taddr] * B(desc), M = 128, N = 16, K = 16, f16 x f16 -> f32
-__device__ __forceinline__ void umma_f16(uint32_t d_taddr, uint32_t a_taddr, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
-                 "r"(a_taddr), "l"(bdesc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Static int8 fake-quant code (gemma4 wNa8o8 page, "Implemented"):
-// rint(x * (1/s)) in fp32, ties to even, clamped to [-128, 127]; NaN -> 0.
-__device__ __forceinline__ float fq_code(float x, float inv_s)
-{
-    float t = __fmul_rn(x, inv_s);
-    if (t != t) return 0.0f;
-    return fminf(fmaxf(rintf(t), -128.0f), 127.0f);
-}
+// ------------------------------------------------------------------ helpers
+using namespace dev;
 
 __device__ __forceinline__ void report_timeout(const Tc05Params &p, volatile int *flag)
 {
@@ -269,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
         int issued = 0;
         for (int st = 0; st < p.n_stages; ++st) {
             const int slot = st % SW, round = st / SW;
-            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(wempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait_spin(wempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 break;
             }
@@ -285,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
         }
         for (int slot = 0; slot < SW && slot < issued; ++slot) {  // no copy in flight at exit
             const int last = slot + ((issued - 1 - slot) / SW) * SW;
-            if (!mbar_wait(wfull0 + 8u * slot, (uint32_t)((last / SW) & 1)) && lane == 0) report_timeout(p, abort_flag);
+            if (!mbar_wait_spin(wfull0 + 8u * slot, (uint32_t)((last / SW) & 1)) && lane == 0) report_timeout(p, abort_flag);
         }
         return;
     }
@@ -310,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
             bool ok = true;
             for (int g = 0; g < kgroups && ok; ++g) {
                 const int a = g & (kASlots - 1);
-                if (!mbar_wait(afull0 + 8u * a, (uint32_t)((g / kASlots) & 1))) {
+                if (!mbar_wait_spin(afull0 + 8u * a, (uint32_t)((g / kASlots) & 1))) {
                     report_timeout(p, abort_flag);
                     ok = false;
                     break;
@@ -462,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
             if (sid != cur_stage) {
                 if (cur_stage >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_stage % SW));
                 cur_stage = sid;
-                if (alive && !__all_sync(0xffffffffu, mbar_wait(wfull0 + 8u * slot, (uint32_t)((sid / SW) & 1)))) {
+                if (alive && !__all_sync(0xffffffffu, mbar_wait_spin(wfull0 + 8u * slot, (uint32_t)((sid / SW) & 1)))) {
                     if (lane == 0) report_timeout(p, abort_flag);
                     alive = false;
                 }
             }
             const int a = g & (kASlots - 1);
             if (alive && g >= kASlots &&
-                !__all_sync(0xffffffffu, mbar_wait(aempty0 + 8u * a, (uint32_t)(((g / kASlots) - 1) & 1)))) {
+                !__all_sync(0xffffffffu, mbar_wait_spin(aempty0 + 8u * a, (uint32_t)(((g / kASlots) - 1) & 1)))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 alive = false;
             }
@@ -509,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
     }
 
     // epilogue: D -> per-lane partial -> per-row sum over the K segments
-    const bool dok = __all_sync(0xffffffffu, mbar_wait(dfull, 0u));
+    const bool dok = __all_sync(0xffffffffu, mbar_wait_spin(dfull, 0u));
     if (!dok && lane == 0) report_timeout(p, abort_flag);
     tc_fence_after();
     if (half == 0) {
@@ -538,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_tc05_kernel(const __grid_c
         float v = 0.0f;
         for (int s = 0; s < S; ++s) v += red[(s * p.lanes_per_seg + r) * kM + m];
         if (prologue) v *= p.a.act_scale;
-        v = dev::requant_out(v, p.a.out_scale, p.a.inv_out);
+        v = requant_out(v, p.a.out_scale, p.a.inv_out);
         const int64_t o = (int64_t)m * N + row0 + r;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(v);
