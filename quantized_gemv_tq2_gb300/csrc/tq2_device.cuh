@@ -82,6 +82,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
 }
 
+// The same wait with cluster-scope acquire: for barriers that CTAs of a
+// thread-block cluster arrive on remotely (their earlier shared-memory writes
+// are then visible to the waiter).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(20000)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer() - t0 > kTimeoutNs) return false;
+    }
+}
+
 // For short producer/consumer hand-offs: spin on the non-blocking test
 // first; only a long wait falls back to the suspending try_wait.  Gives up
 // after kTimeoutNs like mbar_wait.

@@ -37,6 +37,12 @@
 //     they read D (one
 //     column per activation row) and store y, with the optional int8
 //     requantisation at store.
+// Split K: when the tiles alone would leave SMs idle, a thread-block cluster
+// of S CTAs shares a tile, CTA r taking 256-blocks [r B / S, (r+1) B / S).
+// Each writes its fp32 partial tile to its own shared memory; CTA r then sums
+// its 1/S of the columns over the S partials (distributed shared memory, a
+// fixed order, so the result is the same on every run) and stores them.  The
+// cross-CTA hand-offs are mbarriers with remote arrivals and bounded waits.
 // Every mbarrier wait is bounded; a wait that runs out sets TQ2_FLAG_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -74,10 +80,11 @@ struct GemmParams {
     CUtensorMap wmap;  // qs as uint64 [N][K/32]; box {8, 128}; no swizzle
     CUtensorMap xmap;  // x as fp16 [M][K]; box {64, BN}; 128-byte swizzle
     MatvecArgs a;
-    int n_tiles;       // weight-row tiles (ceil(N / 128)); blockIdx = m_tile * n_tiles + n_tile
+    int n_tiles;       // weight-row tiles (ceil(N / 128)); tile = m_tile * n_tiles + n_tile
+    int S;             // CTAs per tile (cluster size; split of K), blockIdx = tile * S + rank
     int B;             // 256-blocks per row
     int sw, sb;        // ring depths: codes; stages (A slots and x buffers, <= 4)
-    int off_bar, off_dsm, off_w, off_b, smem_total;
+    int off_bar, off_dsm, off_w, off_b, smem_total;  // the x ring also holds the partial tile when S > 1
 };
 
 __device__ __forceinline__ void report_timeout(const GemmParams &p, volatile int *flag)
@@ -117,13 +124,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t N = p.a.N, K = p.a.K;
     const int M = p.a.M;
-    const int ntile = (int)(blockIdx.x % (unsigned)p.n_tiles), mtile = (int)(blockIdx.x / (unsigned)p.n_tiles);
+    const int S = p.S;
+    const int rank = (int)(blockIdx.x % (unsigned)S), tile = (int)(blockIdx.x / (unsigned)S);
+    const int ntile = tile % p.n_tiles, mtile = tile / p.n_tiles;
     const int64_t n0 = (int64_t)ntile * kRows;
     const int m0 = mtile * BN;
-    const int nks = (int)(K / 16);               // k-steps
-    const int ngroups = nks / 8;                 // TMEM A fills (8 k-steps each)
-    const int nwst = (int)(K / 256);             // code stages (64 bytes of codes per row)
-    const int nbst = nks / kKs;                  // stages (= ngroups)
+    // this CTA's 256-blocks [w0, w1) of K; all indices below are local to it
+    const int w0 = (int)((int64_t)rank * p.B / S), w1 = (int)((int64_t)(rank + 1) * p.B / S);
+    const int nwst = w1 - w0;                    // code stages (one 256-block each)
+    const int ngroups = 2 * nwst;                // stages of 8 k-steps (TMEM A fills, x buffers)
+    const int nbst = ngroups;
     const int SW = p.sw, SB = p.sb;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);
@@ -134,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const uint32_t bfull0 = wempty0 + 8u * SW, bconv0 = bfull0 + 8u * SB, afull0 = bconv0 + 8u * SB;
     const uint32_t sempty0 = afull0 + 8u * SB;
     const uint32_t dfull = sempty0 + 8u * SB;
+    const uint32_t pready = dfull + 8u, pdone = pready + 8u;  // split K: peers' partials written / read
     const bool prologue = p.a.act_scale != 0.0f;
     // the x ring must be 1024-byte aligned for the 128-byte swizzle (the plan
     // reserves the slack; both rings move together)
@@ -153,10 +164,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             mbar_init(sempty0 + 8u * i, 1);
         }
         mbar_init(dfull, 1);
+        if (S > 1) {
+            mbar_init(pready, (uint32_t)(S - 1));
+            mbar_init(pdone, (uint32_t)(S - 1));
+        }
         abort_sh = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (S > 1) {  // every CTA's barriers exist before any peer arrives on them
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
 
     if (warp == kWProducerWarp) {
         // -------------------------------------------------- codes -> shared memory
@@ -172,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             if (lane == 0) {
                 const uint32_t full = wfull0 + 8u * slot;
                 mbar_arrive_expect_tx(full, (uint32_t)kWStageBytes);
-                tensor2d_g2s(wring + (uint32_t)(slot * kWStageBytes), &p.wmap, 8 * s, (int)n0, full, pol);
+                tensor2d_g2s(wring + (uint32_t)(slot * kWStageBytes), &p.wmap, 8 * (w0 + s), (int)n0, full, pol);
             }
             __syncwarp();
             issued = s + 1;
@@ -201,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             __syncwarp();
             if (lane < 2)
                 tensor2d_g2s(bring + (uint32_t)slot * kBStageBytes + (uint32_t)lane * kBoxBytes, &p.xmap,
-                             16 * kKs * s + 64 * lane, m0, full, pol);
+                             256 * w0 + 16 * kKs * s + 64 * lane, m0, full, pol);
             __syncwarp();
             issued = s + 1;
         }
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 c0 = lds128(lbase + (uint32_t)(u0 << 4));
                 c1 = lds128(lbase + (uint32_t)((u0 + 1) << 4));
             }
-            const __half hd = __ushort_as_half(dsm[(g >> 1) * kRows + row]);  // block of the group
+            const __half hd = __ushort_as_half(dsm[(w0 + (g >> 1)) * kRows + row]);  // block of the group
             const __half2 dd = __halves2half2(hd, hd);
             const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
@@ -356,48 +374,103 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const bool dok = __all_sync(0xffffffffu, mbar_wait(dfull, 0u));
     if (!dok && lane == 0) report_timeout(p, abort_flag);
     tc_fence_after();
-    const bool store = (*abort_flag == 0) && n < N;
+    auto store_y = [&](int m, int64_t nn, float v) {
+        if (prologue) v *= p.a.act_scale;
+        v = requant_out(v, p.a.out_scale, p.a.inv_out);
+        const int64_t o = (int64_t)m * N + nn;
+        if (p.a.y_f16)
+            reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(v);
+        else
+            reinterpret_cast<float *>(p.a.y)[o] = v;
+    };
+    if (S == 1) {
+        const bool store = (*abort_flag == 0) && n < N;
+#pragma unroll 1
+        for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
+            tmem_ld_wait();
+            if (store) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (m0 + c0 + j < M) store_y(m0 + c0 + j, n, __uint_as_float(r[j]));
+            }
+        }
+        tc_fence_before();
+        named_barrier(2, kTmemThreads);  // (b)
+        return;
+    }
+
+    // split K: partial tile -> own shared memory (the x ring, idle now),
+    // column-major [BN][128] fp32
+    float *part = reinterpret_cast<float *>(smem + p.off_b);
 #pragma unroll 1
     for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
         tmem_ld_wait();
-        if (store) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int m = m0 + c0 + j;
-                if (m < M) {
-                    float v = __uint_as_float(r[j]);
-                    if (prologue) v *= p.a.act_scale;
-                    v = requant_out(v, p.a.out_scale, p.a.inv_out);
-                    const int64_t o = (int64_t)m * N + n;
-                    if (p.a.y_f16)
-                        reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(v);
-                    else
-                        reinterpret_cast<float *>(p.a.y)[o] = v;
-                }
-            }
-        }
+        for (int j = 0; j < 32; ++j) part[(c0 + j) * kRows + row] = __uint_as_float(r[j]);
     }
     tc_fence_before();
-    named_barrier(2, kTmemThreads);  // (b)
+    named_barrier(2, kTmemThreads);       // (b): TMEM read, the MMA warp may free it
+    named_barrier(3, kUnpackWarps * 32);  // every partial of this CTA written
+    const uint32_t part_s = smem_addr(part);
+    if (uw == 0 && lane < S && lane != rank) {  // tell every peer: my partial is ready
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(pready), "r"(lane));
+        asm volatile("fence.acq_rel.cluster;\n\tmbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                     ::"r"(remote) : "memory");
+    }
+    bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(pready, 0u));
+    if (!ok && lane == 0) report_timeout(p, abort_flag);
+    // this CTA's columns [rank BN/S, (rank+1) BN/S), summed over the S partials in rank order
+    const int cols = BN / S, c_lo = rank * cols;
+    const int tid_u = uw * 32 + lane;
+    if (ok) {
+        for (int i = tid_u; i < cols * kRows; i += kUnpackWarps * 32) {
+            const int c = c_lo + i / kRows, rr = i % kRows;
+            const uint32_t off = (uint32_t)((c * kRows + rr) * 4);
+            float v = 0.0f;
+            for (int q2 = 0; q2 < S; ++q2) {
+                uint32_t ra;
+                float t;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(part_s + off), "r"(q2));
+                asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(t) : "r"(ra) : "memory");
+                v += t;
+            }
+            const int m = m0 + c;
+            const int64_t nn = n0 + rr;
+            if (*abort_flag == 0 && m < M && nn < N) store_y(m, nn, v);
+        }
+    }
+    named_barrier(3, kUnpackWarps * 32);  // this CTA has read every peer's partial
+    if (uw == 0 && lane < S && lane != rank) {  // tell every peer: done reading yours
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(pdone), "r"(lane));
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+    }
+    // keep this CTA's shared memory alive until every peer has read it
+    if (!__all_sync(0xffffffffu, mbar_wait_cluster(pdone, 0u)) && lane == 0) report_timeout(p, abort_flag);
 }
 
 // ------------------------------------------------------------------ host side
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-bool make_plan(int BN, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams &p)
+bool make_plan(int BN, int S, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams &p)
 {
     if (M < 1 || N < 1 || K < 256 || K % 256 != 0 || M > (int64_t)1 << 30) return false;
     if (K > (int64_t)1 << 24) return false;  // d slice and k-step counts stay small
     p.B = (int)(K / 256);
+    if (S < 1 || S > 8 || S > p.B || BN % S != 0) return false;
+    p.S = S;
     p.n_tiles = (int)((N + kRows - 1) / kRows);
     const int64_t tiles = (int64_t)p.n_tiles * ((M + BN - 1) / BN);
-    if (tiles > 0x7FFFFFFF) return false;
+    if (tiles * S > 0x7FFFFFFF) return false;
     const int bstage = 2 * BN * 128;
     int off = 0;
     p.off_bar = off;
-    off += 8 * (2 * kMaxStages + 4 * kASlots + 1);  // code ring 2 x sw, stage ring 4 x sb, dfull
+    off += 8 * (2 * kMaxStages + 4 * kASlots + 3);  // code ring 2 x sw, stage ring 4 x sb, dfull, pready, pdone
     off = align_up(off, 128);
     p.off_dsm = off;
     off += p.B * kRows * 2;
@@ -452,12 +525,24 @@ int pick_bn(int64_t M, int64_t N, int device)
     return (nt * ((M + 255) / 256) >= (int64_t)sm_count(device)) ? 256 : 128;
 }
 
+// Split of K (cluster size): the largest power of two up to 8 with which the
+// tiles still fit on the SMs at once, and at least one 256-block per CTA.
+int pick_split(int BN, int64_t M, int64_t N, int64_t K, int device)
+{
+    const int64_t tiles = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
+    const int64_t nsm = sm_count(device);
+    int S = 1;
+    while (S < 8 && tiles * (2 * S) <= nsm && 2 * S <= K / 256) S *= 2;
+    return S;
+}
+
 template <int BN>
 cudaError_t launch_gemm(const MatvecArgs &a, int device)
 {
     GemmParams p{};
     p.a = a;
-    if (!make_plan(BN, a.M, a.N, a.K, gemm_max_dyn<BN>(device), p)) return cudaErrorInvalidConfiguration;
+    const int S = pick_split(BN, a.M, a.N, a.K, device);
+    if (!make_plan(BN, S, a.M, a.N, a.K, gemm_max_dyn<BN>(device), p)) return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     {
@@ -480,17 +565,21 @@ cudaError_t launch_gemm(const MatvecArgs &a, int device)
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const int64_t G = (int64_t)p.n_tiles * ((a.M + BN - 1) / BN);
+    const int64_t G = (int64_t)p.n_tiles * ((a.M + BN - 1) / BN) * S;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)p.smem_total;
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, p);
 }
 
@@ -501,7 +590,7 @@ bool gemm_tc05_supported(int64_t M, int64_t N, int64_t K, int device)
     GemmParams p{};
     const int bn = pick_bn(M, N, device);
     const int dyn = (bn == 256) ? gemm_max_dyn<256>(device) : gemm_max_dyn<128>(device);
-    return dyn > 0 && make_plan(bn, M, N, K, dyn, p);
+    return dyn > 0 && make_plan(bn, pick_split(bn, M, N, K, device), M, N, K, dyn, p);
 }
 
 cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device)
