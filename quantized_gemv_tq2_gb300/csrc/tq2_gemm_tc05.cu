@@ -579,7 +579,7 @@ cudaError_t launch_gemm(const MatvecArgs &a, int device)
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = (S > 1) ? 2 : 1;  // a cluster launch only when K is split
     return cudaLaunchKernelEx(&cfg, gemm_tc05_kernel<BN>, p);
 }
 
