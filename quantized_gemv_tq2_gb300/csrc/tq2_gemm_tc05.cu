@@ -12,8 +12,9 @@
 // all of K with no per-block epilogue (the d_b and the "-1" live in W').
 //
 // Tile: 128 weight rows (the MMA's M, one TMEM lane each) x BN activation rows
-// (the MMA's N, 128 or 256), all of K; tcgen05.mma.cta_group::1.kind::f16,
-// K = 16 per instruction.
+// (the MMA's N: 16, 32 or 64 for up to 64 rows -- an MMA with N <= 64 costs
+// about the same as with N = 16 -- else 128 or 256), all of K;
+// tcgen05.mma.cta_group::1.kind::f16, K = 16 per instruction.
 //   * warp 0 streams the packed codes: 2-D TMA boxes of 128 rows x 64 bytes
 //     (one 256-block), before griddepcontrol.wait (weights never depend on
 //     earlier kernels);
@@ -383,17 +384,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         else
             reinterpret_cast<float *>(p.a.y)[o] = v;
     };
+    // each half of the warps reads BN / 2 columns, 32 at a time (the load of
+    // a narrow tile's last chunk runs past BN into unused columns: masked)
+    const int c_beg = half * (BN / 2), c_end = c_beg + BN / 2;
     if (S == 1) {
         const bool store = (*abort_flag == 0) && n < N;
 #pragma unroll 1
-        for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+        for (int c0 = c_beg; c0 < c_end; c0 += 32) {
             uint32_t r[32];
             tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
             tmem_ld_wait();
             if (store) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (m0 + c0 + j < M) store_y(m0 + c0 + j, n, __uint_as_float(r[j]));
+                    if (c0 + j < c_end && m0 + c0 + j < M) store_y(m0 + c0 + j, n, __uint_as_float(r[j]));
             }
         }
         tc_fence_before();
@@ -405,12 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     // column-major [BN][128] fp32
     float *part = reinterpret_cast<float *>(smem + p.off_b);
 #pragma unroll 1
-    for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+    for (int c0 = c_beg; c0 < c_end; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) part[(c0 + j) * kRows + row] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j)
+            if (c0 + j < c_end) part[(c0 + j) * kRows + row] = __uint_as_float(r[j]);
     }
     tc_fence_before();
     named_barrier(2, kTmemThreads);       // (b): TMEM read, the MMA warp may free it
@@ -492,13 +497,15 @@ bool make_plan(int BN, int S, int64_t M, int64_t N, int64_t K, int max_dyn, Gemm
     return p.smem_total <= max_dyn;
 }
 
-std::atomic<int> g_gemm_dyn[2][64];
+std::atomic<int> g_gemm_dyn[5][64];
+
+constexpr int bn_index(int BN) { return BN == 16 ? 0 : BN == 32 ? 1 : BN == 64 ? 2 : BN == 128 ? 3 : 4; }
 
 template <int BN>
 int gemm_max_dyn(int device)
 {
     if (device < 0 || device >= 64) return 0;
-    const int bi = (BN == 256) ? 1 : 0;
+    const int bi = bn_index(BN);
     int v = g_gemm_dyn[bi][device].load();
     if (v > 0) return v;
     int optin = 0;
@@ -517,10 +524,14 @@ int gemm_max_dyn(int device)
     return v;
 }
 
-// BN = 256 (full tensor-core rate) when that still gives every SM a tile,
-// else 128 (twice the tiles).
+// Up to 64 activation rows: the narrowest tile that holds them (an MMA with
+// N <= 64 costs about the same as one with N = 16).  Beyond: BN = 256 (full
+// tensor-core rate) when that still gives every SM a tile, else 128.
 int pick_bn(int64_t M, int64_t N, int device)
 {
+    if (M <= 16) return 16;
+    if (M <= 32) return 32;
+    if (M <= 64) return 64;
     const int64_t nt = (N + kRows - 1) / kRows;
     return (nt * ((M + 255) / 256) >= (int64_t)sm_count(device)) ? 256 : 128;
 }
@@ -589,13 +600,21 @@ bool gemm_tc05_supported(int64_t M, int64_t N, int64_t K, int device)
 {
     GemmParams p{};
     const int bn = pick_bn(M, N, device);
-    const int dyn = (bn == 256) ? gemm_max_dyn<256>(device) : gemm_max_dyn<128>(device);
+    const int dyn = bn == 16 ? gemm_max_dyn<16>(device) : bn == 32 ? gemm_max_dyn<32>(device)
+                  : bn == 64 ? gemm_max_dyn<64>(device) : bn == 128 ? gemm_max_dyn<128>(device)
+                  : gemm_max_dyn<256>(device);
     return dyn > 0 && make_plan(bn, pick_split(bn, M, N, K, device), M, N, K, dyn, p);
 }
 
 cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device)
 {
-    return (pick_bn(a.M, a.N, device) == 256) ? launch_gemm<256>(a, device) : launch_gemm<128>(a, device);
+    switch (pick_bn(a.M, a.N, device)) {
+    case 16: return launch_gemm<16>(a, device);
+    case 32: return launch_gemm<32>(a, device);
+    case 64: return launch_gemm<64>(a, device);
+    case 128: return launch_gemm<128>(a, device);
+    default: return launch_gemm<256>(a, device);
+    }
 }
 
 }  // namespace tq2
