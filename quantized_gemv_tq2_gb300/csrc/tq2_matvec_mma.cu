@@ -751,15 +751,11 @@ int max_dynamic_smem(int device)
     return v;
 }
 
-// Grid and plan: one CTA per SM (at most one per 16 rows) while the per-CTA
-// share fits, more CTAs otherwise.
+// Grid and plan: one CTA per SM while the per-CTA share fits, more CTAs otherwise.
 bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaParams &p)
 {
     if (max_dyn <= 0) return false;
-    // at least one full 16-row group per CTA: a small matrix (k/v) is
-    // latency-bound, and CTAs of 1-2 rows only multiply the x staging
-    const int64_t gmax = (N + 15) / 16;
-    int G = (int)((gmax < (int64_t)sm_count(device)) ? gmax : sm_count(device));
+    int G = (int)((N < (int64_t)sm_count(device)) ? N : sm_count(device));
     while (!make_plan(M, N, K, G, max_dyn, p)) {
         if (G >= N) return false;
         G = (int)((2 * (int64_t)G < N) ? 2 * G : N);
