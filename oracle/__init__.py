@@ -9,6 +9,9 @@ The C source cites the passages it follows:
 * "BitCPM-CANN-8B -> Core AI, ternary 1.58-bit" page: the TQ2_0 format, the
   recovery of d and the codes from a dequantised W, the linear factoring of
   the matvec;
+* "Custom Metal kernels" page, the note on asymmetric (zero-point) int4:
+  the affine-int4 matvec with the zero point factored out,
+  acc += s * (dot - z * sum x);
 * "gemma4 wNa8o8 requires int8 activations" page: the static int8
   fake-quant of the activations and its reciprocal-multiply form, and the
   same fake-quant of a linear's output at store (requantisation).
@@ -85,6 +88,12 @@ def _load():
         lib.tq2o_matvec_rows_f64.restype = None
         lib.tq2o_matvec_exact.argtypes = [P, I64, P, P, I64, I64, F, P]
         lib.tq2o_matvec_exact.restype = ctypes.c_int64
+        lib.tq2o_affine4_f64.argtypes = [P, I64, P, P, P, I64, I64, I64, P, P]
+        lib.tq2o_affine4_f64.restype = None
+        lib.tq2o_affine4_rows_f64.argtypes = [P, I64, P, P, P, I64, I64, I64, P, I64, P, P]
+        lib.tq2o_affine4_rows_f64.restype = None
+        lib.tq2o_affine4_exact.argtypes = [P, I64, P, P, P, I64, I64, I64, P]
+        lib.tq2o_affine4_exact.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -262,3 +271,50 @@ def matvec_exact(x, qs, d, K, act_scale: float = 0.0) -> np.ndarray:
 def tolerance(tol_sum: np.ndarray) -> np.ndarray:
     """Per-element parity bound: 1e-3 * sum_k |d_b x_k| + 1e-6."""
     return 1e-3 * tol_sum + 1e-6
+
+
+# ---------------------------------------------------------------- affine int4
+def _affine4_args(x, qs, s, z, K, G):
+    xb = _bits16(x)
+    if xb.ndim == 1:
+        xb = xb.reshape(1, -1)
+    q = _c(qs, np.uint8)
+    sb, zb = _bits16(s), _bits16(z)
+    N = q.shape[0]
+    if G < 1 or K % G or q.shape[1] * 2 != K or sb.shape != (N, K // G) or zb.shape != (N, K // G):
+        raise ValueError("affine int4: qs [N, K/2], s and z [N, K/G], G | K")
+    return xb, q, sb, zb, N
+
+
+def affine4(x, qs, s, z, K: int, G: int):
+    """fp64 affine-int4 matvec, zero point factored per group:
+    (y [M,N], tol_sum [M,N]) with tol_sum = sum_g |s_g| sum_k |x_k| (q_k + |z_g|)."""
+    xb, q, sb, zb, N = _affine4_args(x, qs, s, z, K, G)
+    M = xb.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    t = np.zeros((M, N), dtype=np.float64)
+    _load().tq2o_affine4_f64(_ptr(xb), M, _ptr(q), _ptr(sb), _ptr(zb), N, K, G, _ptr(y), _ptr(t))
+    return y, t
+
+
+def affine4_rows(x, qs, s, z, K: int, G: int, rows):
+    """fp64 affine-int4 matvec for the output rows ``rows`` only."""
+    xb, q, sb, zb, N = _affine4_args(x, qs, s, z, K, G)
+    M = xb.shape[0]
+    r = _c(rows, np.int64)
+    assert r.size == 0 or (r.min() >= 0 and r.max() < N)
+    y = np.zeros((M, r.size), dtype=np.float64)
+    t = np.zeros((M, r.size), dtype=np.float64)
+    _load().tq2o_affine4_rows_f64(_ptr(xb), M, _ptr(q), _ptr(sb), _ptr(zb), N, K, G, _ptr(r), r.size,
+                                  _ptr(y), _ptr(t))
+    return y, t
+
+
+def affine4_exact(x, qs, s, z, K: int, G: int) -> np.ndarray:
+    """Exact dense-form affine-int4 matvec (sum_k s(q - z) x_k in __int128),
+    rounded once to fp64; NaN where a term could overflow the exact sum."""
+    xb, q, sb, zb, N = _affine4_args(x, qs, s, z, K, G)
+    M = xb.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    _load().tq2o_affine4_exact(_ptr(xb), M, _ptr(q), _ptr(sb), _ptr(zb), N, K, G, _ptr(y))
+    return y

@@ -1,5 +1,6 @@
 /*
- * tq2_oracle.c -- plain, slow CPU oracle for the TQ2_0-style ternary matvec.
+ * tq2_oracle.c -- plain, slow CPU oracle for the TQ2_0-style ternary matvec
+ * (and its affine-int4 sibling).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may load this library.  The product (the CUDA
@@ -14,6 +15,10 @@
  *        block along K), the recovery paragraph (d = max|W| in the block,
  *        code = round(W/d)+1), and the linear-factoring identity
  *        sum_k x_k d_b (q_k-1) = sum_b d_b sum_{k in b} x_k (q_k-1).
+ *   [P2] "Custom Metal kernels" (coreai-model-zoo knowledge page
+ *        custom-metal-kernels): the note on asymmetric (zero-point) int4,
+ *        whose fused matvec factors the zero point out,
+ *        acc += s * (dot - z * sum x).
  *   [P3] "gemma4 wNa8o8 requires int8 activations" (coreai-model-zoo
  *        knowledge page): the static fake-quant clamp(round(x/s),-128,127)*s,
  *        its implemented form s*clamp(rint(x*(1/s)),-128,127) ("Implemented"
@@ -435,6 +440,117 @@ int64_t tq2o_matvec_exact(const uint16_t *x, int64_t M, const uint8_t *qs, const
                 v = ldexp((double)acc, -24 + sexp);
             }
             y[m * N + n] = v;
+        }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Affine int4 matvec (zero-point factoring).                              */
+/* [P2] "Custom Metal kernels" (coreai-model-zoo knowledge page             */
+/* custom-metal-kernels), the note on asymmetric (zero-point) int4: a fused */
+/* affine-int4 matvec factors the zero point out of the dot product,        */
+/* acc += s * (dot - z * sum x), per group of the reduction axis.           */
+/* Readings (the note gives the identity only): W[n][k] = s[n][g] *         */
+/* (q[n][k] - z[n][g]) with a 4-bit unsigned code q in [0, 15] and g = k/G; */
+/* code k sits at bits 4*(k%2) of byte k/2 of row n (low nibble first);     */
+/* s and z are fp16 arrays [N][K/G]; z is a real zero point in code units.  */
+/* ---------------------------------------------------------------------- */
+static int nibble_at(const uint8_t *qs, int64_t K, int64_t n, int64_t k)
+{
+    return (qs[n * (K / 2) + k / 2] >> (4 * (k % 2))) & 15;
+}
+
+/* y[m][n] = sum_g s_g * (sum_{k in g} x_k q_k - z_g * sum_{k in g} x_k),  */
+/* fp64, the groups and the terms in order.  tol_sum[m][n] =                */
+/* sum_g |s_g| sum_{k in g} |x_k| (q_k + |z_g|): the magnitude of the two   */
+/* factored sums, which is what their rounding error scales with.           */
+static void affine4_row(const uint16_t *x, int64_t m, const uint8_t *qs, const uint16_t *s,
+                        const uint16_t *z, int64_t n, int64_t K, int64_t G, double *y, double *t)
+{
+    int64_t ng = K / G;
+    double acc = 0.0, bound = 0.0;
+    for (int64_t g = 0; g < ng; ++g) {
+        double sg = tq2o_half_to_double(s[n * ng + g]);
+        double zg = tq2o_half_to_double(z[n * ng + g]);
+        double dot = 0.0, sx = 0.0, ab = 0.0;
+        for (int64_t k = g * G; k < (g + 1) * G; ++k) {
+            double xv = tq2o_half_to_double(x[m * K + k]);
+            int q = nibble_at(qs, K, n, k);
+            dot += xv * (double)q;
+            sx += xv;
+            ab += fabs(xv) * ((double)q + fabs(zg));
+        }
+        acc += sg * (dot - zg * sx);
+        bound += fabs(sg) * ab;
+    }
+    *y = acc;
+    if (t)
+        *t = bound;
+}
+
+void tq2o_affine4_f64(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,
+                      const uint16_t *z, int64_t N, int64_t K, int64_t G, double *y, double *tol_sum)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            affine4_row(x, m, qs, s, z, n, K, G, &y[m * N + n], tol_sum ? &tol_sum[m * N + n] : 0);
+}
+
+/* The same for the output rows rows[0..nrows): y, tol_sum are [M, nrows]. */
+void tq2o_affine4_rows_f64(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,
+                           const uint16_t *z, int64_t N, int64_t K, int64_t G, const int64_t *rows,
+                           int64_t nrows, double *y, double *tol_sum)
+{
+    (void)N;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t i = 0; i < nrows; ++i)
+            affine4_row(x, m, qs, s, z, rows[i], K, G, &y[m * nrows + i],
+                        tol_sum ? &tol_sum[m * nrows + i] : 0);
+}
+
+/* Exact dense form, the oracle's own check: sum_k W[n][k] x_k with W =     */
+/* s * (q - z) taken element by element (no factoring).  In units of 2^-24  */
+/* every fp16 value is an integer, so each term is s_u * (q * 2^24 - z_u) * */
+/* x_u * 2^-72, summed in __int128.  A term that could push the sum past    */
+/* 2^126 (|term| >= 2^112 with K <= 2^14) marks the output NaN instead;     */
+/* returns the number of such (or non-finite) outputs.                      */
+static int bitlen128(__int128 v)
+{
+    unsigned __int128 u = v < 0 ? (unsigned __int128)(-v) : (unsigned __int128)v;
+    int b = 0;
+    while (u) {
+        u >>= 1;
+        ++b;
+    }
+    return b;
+}
+
+int64_t tq2o_affine4_exact(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,
+                           const uint16_t *z, int64_t N, int64_t K, int64_t G, double *y)
+{
+    int64_t ng = K / G, bad = 0;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            __int128 acc = 0;
+            int ok = K <= (1 << 14);
+            for (int64_t k = 0; k < K && ok; ++k) {
+                int64_t g = k / G;
+                int64_t su = half_to_units(s[n * ng + g], &ok);
+                int64_t zu = half_to_units(z[n * ng + g], &ok);
+                int64_t xu = half_to_units(x[m * K + k], &ok);
+                __int128 w = (__int128)su * ((__int128)nibble_at(qs, K, n, k) * ((__int128)1 << 24) - zu);
+                if (bitlen128(w) + bitlen128(xu) >= 112) {
+                    ok = 0;
+                    break;
+                }
+                acc += w * xu;
+            }
+            if (!ok) {
+                y[m * N + n] = NAN;
+                ++bad;
+            } else {
+                y[m * N + n] = ldexp((double)acc, -72);
+            }
         }
     return bad;
 }

@@ -460,3 +460,130 @@ def test_generator_torch_code_expansion_matches_numpy():
     b = syn.codes_from_bits_torch(torch.from_numpy(bits), 64, 512).numpy()
     assert np.array_equal(a, b)
     assert np.array_equal(a, syn.codes(3, 64, 512, linear=2))
+
+
+# ------------------------------------------------------------- affine int4
+def _nibbles(qs):
+    """Codes [N, K] from packed bytes, written independently of the oracle:
+    byte j holds code 2j in its low nibble and code 2j+1 in its high one."""
+    q = np.asarray(qs, dtype=np.uint8)
+    out = np.empty((q.shape[0], q.shape[1] * 2), dtype=np.int64)
+    out[:, 0::2] = q & 15
+    out[:, 1::2] = q >> 4
+    return out
+
+
+def _affine4_case(seed, M, N, K, G, heavy=False):
+    qs, s, z = syn.affine4_weights(seed, N, K, G)
+    x = syn.activations(seed, M, K, heavy=heavy)
+    return x, qs, s, z
+
+
+@pytest.mark.parametrize("seed,M,N,K,G", [(1, 1, 7, 256, 64), (2, 2, 33, 1024, 128),
+                                          (3, 3, 16, 768, 256), (4, 1, 9, 4096, 64)])
+def test_affine4_against_numpy_dense(seed, M, N, K, G):
+    """The factored form equals the dense product W x with W = s (q - z)
+    materialised element by element (numpy, fp64): pins the nibble order,
+    the group index, the zero point's sign and the scale."""
+    x, qs, s, z = _affine4_case(seed, M, N, K, G, heavy=(seed % 2 == 0))
+    y, tol = oracle.affine4(x, qs, s, z, K, G)
+    gi = np.arange(K) // G
+    W = s.astype(np.float64)[:, gi] * (_nibbles(qs) - z.astype(np.float64)[:, gi])
+    ref = x.astype(np.float64) @ W.T
+    assert np.all(np.abs(y - ref) <= 1e-12 * tol + 1e-300)
+    # the tolerance sum's closed form
+    t_ref = np.abs(x.astype(np.float64)) @ (np.abs(s.astype(np.float64))[:, gi]
+                                            * (_nibbles(qs) + np.abs(z.astype(np.float64))[:, gi])).T
+    assert np.allclose(tol, t_ref, rtol=1e-12, atol=0)
+
+
+def test_affine4_one_hot_is_exact():
+    """x = e_k gives y[n] = s[n][k/G] * (q[n][k] - z[n][k/G]) exactly."""
+    N, K, G = 12, 512, 64
+    _, qs, s, z = _affine4_case(5, 1, N, K, G)
+    q = _nibbles(qs)
+    for k in (0, 1, 63, 64, 127, 200, 511):
+        x = np.zeros((1, K), dtype=np.float16)
+        x[0, k] = 1.0
+        want = s.astype(np.float64)[:, k // G] * (q[:, k] - z.astype(np.float64)[:, k // G])
+        y, _ = oracle.affine4(x, qs, s, z, K, G)
+        assert np.array_equal(y[0], want), k
+        assert np.array_equal(oracle.affine4_exact(x, qs, s, z, K, G)[0], want), k
+
+
+def test_affine4_every_byte_value_in_both_nibble_positions():
+    """Row v holds the byte v everywhere: x = e_0 reads its low nibble,
+    x = e_1 its high nibble (brute force over all 256 byte values)."""
+    N, K, G = 256, 256, 256
+    qs = np.repeat(np.arange(256, dtype=np.uint8)[:, None], K // 2, axis=1)
+    s = np.full((N, 1), 0.5, dtype=np.float16)
+    z = np.full((N, 1), 3.0, dtype=np.float16)
+    for k, nib in ((0, np.arange(256) & 15), (1, np.arange(256) >> 4), (255, np.arange(256) >> 4)):
+        x = np.zeros((1, K), dtype=np.float16)
+        x[0, k] = 1.0
+        y, _ = oracle.affine4(x, qs, s, z, K, G)
+        assert np.array_equal(y[0], 0.5 * (nib - 3.0)), k
+
+
+def test_affine4_unit_scale_zero_point_zero_is_integer_dot():
+    """s = 1, z = 0: y = sum_k q_k x_k, the textbook dot product (numpy)."""
+    M, N, K, G = 2, 10, 512, 128
+    x, qs, _, _ = _affine4_case(6, M, N, K, G)
+    s = np.ones((N, K // G), dtype=np.float16)
+    z = np.zeros((N, K // G), dtype=np.float16)
+    y, _ = oracle.affine4(x, qs, s, z, K, G)
+    ref = x.astype(np.float64) @ _nibbles(qs).T.astype(np.float64)
+    assert np.array_equal(y, ref)  # every partial sum is exact in fp64
+
+
+def test_affine4_code_equal_to_integer_zero_point_gives_zero():
+    """Every code equal to an integer zero point: W = 0, so y = 0 exactly,
+    whatever x and s are."""
+    N, K, G = 6, 512, 64
+    x = syn.activations(7, 2, K, heavy=True)
+    v = np.arange(N) % 16
+    qs = np.repeat((v | (v << 4)).astype(np.uint8)[:, None], K // 2, axis=1)
+    s = syn.scales(7, N, K // G)
+    z = np.repeat(v.astype(np.float16)[:, None], K // G, axis=1)
+    y, _ = oracle.affine4(x, qs, s, z, K, G)
+    assert np.all(y == 0.0)
+    assert np.all(oracle.affine4_exact(x, qs, s, z, K, G) == 0.0)
+
+
+def test_affine4_exact_against_fractions_and_f64_within_rounding():
+    """The exact dense form equals rational arithmetic (Python fractions) on
+    a tiny case, and the fp64 factored form is within K * 2^-52 * tol of it."""
+    from fractions import Fraction
+    M, N, K, G = 1, 3, 256, 64
+    x, qs, s, z = _affine4_case(8, M, N, K, G, heavy=True)
+    q = _nibbles(qs)
+    ye = oracle.affine4_exact(x, qs, s, z, K, G)
+    for n in range(N):
+        acc = Fraction(0)
+        for k in range(K):
+            acc += (Fraction(float(s[n, k // G])) * (q[n, k] - Fraction(float(z[n, k // G])))
+                    * Fraction(float(x[0, k])))
+        assert ye[0, n] == float(acc)
+    x, qs, s, z = _affine4_case(9, 2, 40, 4096, 128, heavy=True)
+    y, tol = oracle.affine4(x, qs, s, z, 4096, 128)
+    ye = oracle.affine4_exact(x, qs, s, z, 4096, 128)
+    assert np.all(np.isfinite(ye))
+    assert np.all(np.abs(y - ye) <= 4096 * 2.0 ** -52 * tol)
+
+
+def test_affine4_rows_matches_full():
+    x, qs, s, z = _affine4_case(10, 2, 50, 1024, 64)
+    y, t = oracle.affine4(x, qs, s, z, 1024, 64)
+    rows = np.array([0, 7, 49, 23])
+    yr, tr = oracle.affine4_rows(x, qs, s, z, 1024, 64, rows)
+    assert np.array_equal(yr, y[:, rows]) and np.array_equal(tr, t[:, rows])
+
+
+def test_affine4_generator_distribution():
+    qs, s, z = syn.affine4_weights(1, 64, 4096, 128)
+    q = _nibbles(qs)
+    counts = np.bincount(q.reshape(-1), minlength=16) / q.size
+    assert np.all(np.abs(counts - 1 / 16) < 0.005)
+    assert s.dtype == np.float16 and z.dtype == np.float16
+    assert 0.0 <= float(z.min()) and float(z.max()) <= 15.0 and float(z.std()) > 3.0
+    assert np.array_equal(syn.affine4_weights(1, 64, 4096, 128)[0], qs)

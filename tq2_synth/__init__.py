@@ -55,6 +55,7 @@ SLOT_HEAVY_Z = 4
 SLOT_ACT_SCALE = 5
 SLOT_DENSE = 6
 SLOT_OUT_SCALE = 7
+SLOT_ZERO_POINT = 8
 
 
 def tensor_id(linear: int, slot: int) -> int:
@@ -165,3 +166,16 @@ def dense_normal(seed: int, n: int, k: int, linear: int = 0,
     """A generic (not ternary) dense weight [n, k] fp32 ~ N(0, sigma^2)."""
     z = normal(seed, tensor_id(linear, SLOT_DENSE), n * k)
     return (sigma * z).astype(np.float32).reshape(n, k)
+
+
+# ---------------------------------------------------------------- affine int4
+def affine4_weights(seed: int, n: int, k: int, g: int, linear: int = 0):
+    """Affine-int4 weights for one linear: (qs [n, k/2] uint8, s [n, k/g] fp16,
+    z [n, k/g] fp16).  Every byte is random, so the 4-bit codes are i.i.d.
+    uniform on 0..15; s = fp16(U[0.005, 0.05]) as the ternary block scales;
+    z = fp16(U[0, 15]), a real zero point anywhere in the code range."""
+    qs = code_bits(seed, tensor_id(linear, SLOT_CODE_BITS), n * k // 2).reshape(n, k // 2)
+    sc = scales(seed, n, k // g, linear=linear)
+    u = uniform(seed, tensor_id(linear, SLOT_ZERO_POINT), n * (k // g))
+    z = (15.0 * u).astype(np.float16).reshape(n, k // g)
+    return qs, sc, z
