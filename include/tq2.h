@@ -239,6 +239,40 @@ TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, con
                             int64_t K, void *y, tq2_dtype y_dtype, float act_scale, float out_scale,
                             uint32_t *d_status, tq2_stream_t stream, int impl);
 
+/*
+ * tq2_affine4_matvec -- the affine-int4 sibling on the same skeleton
+ * ("Custom Metal kernels" page, the note on asymmetric (zero-point) int4: a
+ * fused affine-int4 matvec factors the zero point out, acc += s * (dot -
+ * z * sum x)):
+ *   y[m][n] = sum_g s[n][g] * (sum_{k in g} x[m][k] q[n][k]
+ *                              - z[n][g] * sum_{k in g} x[m][k]),
+ * i.e. y = W x with W[n][k] = s[n][k/G] * (q[n][k] - z[n][k/G]).
+ *   x          device, fp16 [M, K] row-major, 16-byte aligned, read only.
+ *   M          0 .. 16 activation rows (two per kernel launch).
+ *   qs         device, uint8 [N, K/2]: 4-bit codes q in 0..15, code k of a
+ *              row in byte k/2 at bits 4*(k%2) (low nibble first); 16-byte
+ *              aligned, read only.
+ *   s, z       device, fp16 [N, K/G]: the scale and the zero point (in code
+ *              units, any fp16 value) of each group of G codes; 2-byte
+ *              aligned, read only.
+ *   N, K       N >= 0, K >= 0 with K % 256 == 0 (K % G == 0 follows).
+ *   G          64, 128 or 256, else TQ2_ERR_ARG.
+ *   y, y_dtype device [M, N] fp32 (TQ2_F32) or fp16 (TQ2_F16, round to
+ *              nearest even), 4- or 2-byte aligned, written.
+ *   d_status   optional device word; TQ2_FLAG_TIMEOUT if a bounded wait ran
+ *              out (y is then invalid).
+ *   stream     caller's CUDA stream; the call enqueues and returns.
+ * Accuracy: |y - exact| <= 1e-3 * sum_g |s_g| sum_{k in g} |x_k| (q_k +
+ * |z_g|) + 1e-6 per element (the magnitude of the two factored sums, which
+ * the fp32 accumulation error scales with).  Deterministic run to run.
+ * Errors: as tq2_matvec (TQ2_ERR_SHAPE, _NULL, _ALIGN, _DTYPE, _CUDA);
+ * TQ2_ERR_ARG for G, or a K too long for the x staging to fit in shared
+ * memory.  M = 0 or N = 0: nothing is done; K = 0: y = 0.
+ */
+TQ2_API tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,
+                                      const uint16_t *z, int64_t N, int64_t K, int64_t G, void *y,
+                                      tq2_dtype y_dtype, uint32_t *d_status, tq2_stream_t stream);
+
 /* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
  * host thread ("no error" if none): name and description, static storage. */
 TQ2_API const char *tq2_last_cuda_error(void);

@@ -19,7 +19,8 @@ from . import build as _build
 
 __all__ = [
     "TQ2Error", "lib", "load", "declared_symbols",
-    "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "gemm", "matvec_workspace_size",
+    "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "gemm", "affine4_matvec",
+    "matvec_workspace_size",
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_TC05", "IMPL_PS", "IMPL_DP4", "IMPL_GEMM",
@@ -65,6 +66,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_matvec_requant.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
         L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P]
         L.tq2_gemm.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, P, I32]
+        L.tq2_affine4_matvec.argtypes = [P, I64, P, P, P, I64, I64, I64, P, I32, P, P]
         L.tq2_matvec_workspace_size.argtypes = [I64, I64, I64]
         L.tq2_matvec_workspace_size.restype = SZ
         L.tq2_status_string.argtypes = [I32]
@@ -73,7 +75,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_last_cuda_error.argtypes = []
         L.tq2_last_cuda_error.restype = ctypes.c_char_p
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
-                   "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_gemm", "tq2_version"):
+                   "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_gemm", "tq2_affine4_matvec",
+                   "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
         return L
@@ -258,6 +261,26 @@ def gemm(x, qs, d, y=None, y_dtype=None, act_scale: float = 0.0, out_scale: floa
     _need_cuda(x, qs, d, y, status)
     _check(load().tq2_gemm(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
                            float(out_scale), _ptr(status), _stream_ptr(stream), int(impl)), "tq2_gemm")
+    return y
+
+
+def affine4_matvec(x, qs, s, z, G: int, y=None, y_dtype=None, status=None, stream=None):
+    """Affine-int4 matvec y [M,N] = W x with W = s (q - z) per group of G codes
+    (tq2_affine4_matvec): qs uint8 [N, K/2] (low nibble first), s and z fp16
+    [N, K/G], x fp16 [M, K] with M <= 16."""
+    torch = _torch()
+    M, K = x.shape
+    N = qs.shape[0]
+    if (x.dtype != torch.float16 or s.dtype != torch.float16 or z.dtype != torch.float16
+            or qs.dtype != torch.uint8):
+        raise TypeError("x, s and z must be float16, qs uint8")
+    if y is None:
+        dt = torch.float32 if (y_dtype in (None, F32, torch.float32)) else torch.float16
+        y = torch.empty((M, N), dtype=dt, device=qs.device)
+    ycode = F32 if y.dtype == torch.float32 else F16
+    _need_cuda(x, qs, s, z, y, status)
+    _check(load().tq2_affine4_matvec(_ptr(x), M, _ptr(qs), _ptr(s), _ptr(z), N, K, int(G), _ptr(y), ycode,
+                                     _ptr(status), _stream_ptr(stream)), "tq2_affine4_matvec")
     return y
 
 

@@ -350,6 +350,45 @@ tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint1
     return TQ2_OK;
 }
 
+tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,
+                              const uint16_t *z, int64_t N, int64_t K, int64_t G, void *y, tq2_dtype y_dtype,
+                              uint32_t *d_status, tq2_stream_t stream)
+{
+    tq2_status st = check_nk(N, K);
+    if (st != TQ2_OK) return st;
+    if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
+    if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
+    if (G != 64 && G != 128 && G != 256) return TQ2_ERR_ARG;
+    if (M == 0 || N == 0) return TQ2_OK;
+    if (y == nullptr) return TQ2_ERR_NULL;
+    if (K > 0 && (x == nullptr || qs == nullptr || s == nullptr || z == nullptr)) return TQ2_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(s, 2) || !aligned(z, 2)) return TQ2_ERR_ALIGN;
+    if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
+    if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * (y_dtype == TQ2_F32 ? 4 : 2), cs));
+
+    int dev = 0;
+    if ((st = current_device(&dev)) != TQ2_OK) return st;
+    if (!tq2::affine4_supported(N, K, G, dev)) return TQ2_ERR_ARG;
+    tq2::Affine4Args a;
+    a.x = x;
+    a.qs = qs;
+    a.s = s;
+    a.z = z;
+    a.y = y;
+    a.status = d_status;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.G = G;
+    a.y_f16 = (y_dtype == TQ2_F16);
+    a.stream = cs;
+    cudaError_t e = tq2::launch_affine4(a, dev);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return from_cuda(e);
+}
+
 size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K)
 {
     (void)M;

@@ -63,6 +63,23 @@ cudaError_t launch_matvec_ps(const MatvecArgs &a, int device);
 bool dp4_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_dp4(const MatvecArgs &a, int device);
 
+// Affine-int4 matvec (zero point factored out per group of G codes): codes
+// [N][K/2] (two per byte, low nibble first), s and z fp16 [N][K/G], G in
+// {64, 128, 256}; activation rows two per launch.
+struct Affine4Args {
+    const uint16_t *x;   // [M, K] fp16 bits
+    const uint8_t *qs;   // [N, K/2]
+    const uint16_t *s;   // [N, K/G] fp16 bits
+    const uint16_t *z;   // [N, K/G] fp16 bits
+    void *y;             // [M, N] fp32 or fp16
+    uint32_t *status;    // optional device flag word
+    int64_t M, N, K, G;
+    int y_f16;
+    cudaStream_t stream;
+};
+bool affine4_supported(int64_t N, int64_t K, int64_t G, int device);
+cudaError_t launch_affine4(const Affine4Args &a, int device);
+
 // CUDA-core path (fp32 FMA per code), any M in 1..16.
 cudaError_t launch_matvec_simt(const MatvecArgs &a, int device);
 

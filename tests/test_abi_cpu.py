@@ -24,7 +24,7 @@ def test_every_declared_symbol_is_exported(L):
     names = tq2.declared_symbols()
     assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
                           "tq2_matvec_impl", "tq2_matvec_requant", "tq2_gemm",
-                          "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version"}
+                          "tq2_affine4_matvec", "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
 
@@ -158,3 +158,30 @@ def test_grouped_rejects_bad_arguments(L):
     assert G(x=A2) == ALIGN
     assert G(M=0) == OK                           # nothing to do
     assert G(N=(ctypes.c_int64 * n)(0, 0, 0)) == OK
+
+
+def a4(L, x=A16, M=1, qs=A16, s=A16, z=A16, N=64, K=512, G=128, y=A16, yd=0, st=NUL):
+    return L.tq2_affine4_matvec(x, M, qs, s, z, N, K, G, y, yd, st, S)
+
+
+def test_affine4_rejects_bad_arguments(L):
+    assert a4(L, K=300) == SHAPE
+    assert a4(L, K=-256) == SHAPE
+    assert a4(L, M=17) == SHAPE
+    assert a4(L, M=-1) == SHAPE
+    assert a4(L, yd=2) == DTYPE
+    for g in (0, 32, 100, 512, -64):
+        assert a4(L, G=g) == ARG
+    assert a4(L, x=NUL) == NULL
+    assert a4(L, qs=NUL) == NULL
+    assert a4(L, s=NUL) == NULL
+    assert a4(L, z=NUL) == NULL
+    assert a4(L, y=NUL) == NULL
+    assert a4(L, x=A2) == ALIGN
+    assert a4(L, qs=A2) == ALIGN
+    assert a4(L, s=P(0x10001)) == ALIGN
+    assert a4(L, z=P(0x10001)) == ALIGN
+    assert a4(L, y=A2, yd=0) == ALIGN
+    assert a4(L, st=P(0x10002)) == ALIGN
+    assert a4(L, M=0, x=NUL, y=NUL) == OK
+    assert a4(L, N=0, qs=NUL, s=NUL, z=NUL, y=NUL) == OK
