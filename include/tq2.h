@@ -253,7 +253,7 @@ TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, con
  *              row in byte k/2 at bits 4*(k%2) (low nibble first); 16-byte
  *              aligned, read only.
  *   s, z       device, fp16 [N, K/G]: the scale and the zero point (in code
- *              units, any fp16 value) of each group of G codes; 2-byte
+ *              units, any fp16 value) of each group of G codes; 16-byte
  *              aligned, read only.
  *   N, K       N >= 0, K >= 0 with K % 256 == 0 (K % G == 0 follows).
  *   G          64, 128 or 256, else TQ2_ERR_ARG.

@@ -362,7 +362,7 @@ tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, c
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
     if (K > 0 && (x == nullptr || qs == nullptr || s == nullptr || z == nullptr)) return TQ2_ERR_NULL;
-    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(s, 2) || !aligned(z, 2)) return TQ2_ERR_ALIGN;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(s, 16) || !aligned(z, 16)) return TQ2_ERR_ALIGN;
     if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
     if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -11,8 +11,10 @@
 //
 // How (the ternary mma.sync kernel's skeleton, re-cut for nibbles):
 //   * a producer warp streams 16-row x 2048-code chunks of the codes with
-//     TMA (eight 16 x 128-byte boxes per stage, 128-byte swizzle, rows past
-//     N read as zero) into a ring of 16 KB stages, before the PDL wait;
+//     TMA into a ring of 16 KB stages, before the PDL wait: one copy per
+//     stage through a 3-D view of the codes (16 words of a 256-code block,
+//     rows, blocks), laid out block-major, 128 bytes per row, with the
+//     128-byte swizzle (rows past N and blocks past K read as zero);
 //   * the (s, z) pairs of the CTA's rows are staged once as half2;
 //   * x is staged once per CTA in mma B-fragment order, plus the group sums
 //     sum_{k in g} x_k for the zero-point term (fixed-order shuffle trees);
@@ -50,7 +52,7 @@ constexpr int kMaxStages = 8;
 constexpr int kTwoPerSm = 112 * 1024;
 
 struct A4Params {
-    CUtensorMap tq;       // codes as uint64 [N][K/16], box 16 x 16, 128-byte swizzle
+    CUtensorMap tq;       // codes as uint64 {16 per block, N rows, K/256 blocks}, box 16 x 16 x 8, 128-byte swizzle
     const uint16_t *x;    // [M][K] fp16 bits (this launch's first activation row)
     const uint16_t *s;    // [N][K/G] fp16 bits
     const uint16_t *z;    // [N][K/G] fp16 bits
@@ -148,13 +150,13 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            const int nb = min(8, p.B - kc * 8);  // 256-code blocks in this chunk
+            // one 16 KB copy: 8 blocks x 16 rows x 128 bytes (blocks past K
+            // and rows past N read as zero and count in full)
             const uint32_t full = smem_addr(&bars[slot]);
-            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nb * 2048u);
-            __syncwarp();
-            if (lane < nb)
-                tensor2d_g2s(ring + (uint32_t)(slot * kStageBytes + lane * 2048), &p.tq, (kc * 8 + lane) * 16,
-                             (int)(r0 + rg * 16), full, pol);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full, (uint32_t)kStageBytes);
+                tensor3d_g2s(ring + (uint32_t)(slot * kStageBytes), &p.tq, 0, (int)(r0 + rg * 16), kc * 8, full, pol);
+            }
             __syncwarp();
             issued = s + 1;
             if (++kc == p.nkc) {
@@ -178,31 +180,47 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
     float *xg = reinterpret_cast<float *>(smem + p.off_xg);  // [kM][ng] group sums of x
     float *red = reinterpret_cast<float *>(smem + p.off_red);
 
-    // (s, z) of this CTA's rows as half2 (rows past N: zero, so they add
-    // nothing).  All loads of a batch are issued before the first store.
+    // (s, z) of this CTA's rows as half2, rows padded to ng + 1 words.  The
+    // rows' slices of s and z are contiguous (and 16-byte aligned: s, z are,
+    // and r0 is a multiple of 16), so they are read as 16-byte vectors, all
+    // of a thread's loads in flight together; rows past N get s = 0 (no
+    // contribution).
     {
-        const int ne = nrg * 16 * ng;
-        for (int base = 0; base < ne; base += kConsumers * 4) {
-            uint16_t sv[4], zv[4];
+        constexpr int kSzBatch = 4;
+        const int ne = nrows * ng;
+        const int nvec = ne >> 3;
+        const uint4 *sv4 = reinterpret_cast<const uint4 *>(p.s + r0 * ng);
+        const uint4 *zv4 = reinterpret_cast<const uint4 *>(p.z + r0 * ng);
+        auto put = [&](int e, uint16_t sh, uint16_t zh) {
+            const int r = e / ng;
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(szs + (uint32_t)(r * szstr + (e - r * ng)) * 4u),
+                         "r"(pack_h2(sh, zh))
+                         : "memory");
+        };
+        for (int base = 0; base < nvec; base += kConsumers * kSzBatch) {
+            uint4 a[kSzBatch], b[kSzBatch];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = base + j * kConsumers + tid;
-                const int r = i / ng;
-                const bool v = i < ne && r0 + r < N;
-                const int64_t o = (r0 + r) * ng + (i - r * ng);
-                sv[j] = v ? p.s[o] : (uint16_t)0;
-                zv[j] = v ? p.z[o] : (uint16_t)0;
+            for (int j = 0; j < kSzBatch; ++j) {
+                const int v = base + j * kConsumers + tid;
+                a[j] = v < nvec ? sv4[v] : make_uint4(0, 0, 0, 0);
+                b[j] = v < nvec ? zv4[v] : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = base + j * kConsumers + tid;
-                const int r = i / ng;
-                if (i < ne)
-                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(szs + (uint32_t)(r * szstr + (i - r * ng)) * 4u),
-                                 "r"(pack_h2(sv[j], zv[j]))
-                                 : "memory");
+            for (int j = 0; j < kSzBatch; ++j) {
+                const int v = base + j * kConsumers + tid;
+                if (v < nvec) {
+                    const uint32_t aw[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
+                    const uint32_t bw[4] = {b[j].x, b[j].y, b[j].z, b[j].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        put(v * 8 + 2 * i, (uint16_t)(aw[i] & 0xffffu), (uint16_t)(bw[i] & 0xffffu));
+                        put(v * 8 + 2 * i + 1, (uint16_t)(aw[i] >> 16), (uint16_t)(bw[i] >> 16));
+                    }
+                }
             }
         }
+        for (int e = nvec * 8 + tid; e < ne; e += kConsumers) put(e, p.s[r0 * ng + e], p.z[r0 * ng + e]);
+        for (int e = ne + tid; e < nrg * 16 * ng; e += kConsumers) put(e, 0, 0);
     }
 
     // x depends on the previous kernel in the stream.
@@ -214,43 +232,56 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
     // x[12 + c]).  The 4 lanes of a slice, then the kG / 64 slices of a
     // group, are summed by a fixed shuffle tree into the group sum of x.
     {
+        constexpr int kXBatch = 4;  // tasks per thread whose loads are in flight together
         const int ntask = kM * p.B * 16;
-        for (int base = warp * 32; base < ntask; base += kConsumers) {
-            const int task = base + lane;
-            const bool valid = task < ntask;
-            const int t = task & 3, j = (task >> 2) & 3, mb = task >> 4;
-            const int m = (kM == 2 && mb >= p.B) ? 1 : 0;
-            const int b = mb - m * p.B;
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-            if (valid) {
-                const uint16_t *src = p.x + (int64_t)m * K + (int64_t)b * 256 + j * 64 + t * 16;
-                lo = *reinterpret_cast<const uint4 *>(src);
-                hi = *reinterpret_cast<const uint4 *>(src + 8);
-            }
-            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            uint16_t h[16];
-            float sum = 0.0f;
+        for (int base0 = warp * 32; base0 < ntask; base0 += kConsumers * kXBatch) {
+            uint4 lo[kXBatch], hi[kXBatch];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                h[2 * i] = (uint16_t)(w[i] & 0xffffu);
-                h[2 * i + 1] = (uint16_t)(w[i] >> 16);
-                sum += h2f(h[2 * i]) + h2f(h[2 * i + 1]);
-            }
-            if (valid) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t e = (uint32_t)((4 * m + c) * 4 + t);
-                    const uint32_t dst = xf + ((uint32_t)((b * 4 + j) * 16 * kM) + e) * 8u;
-                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(pack_h2(h[c], h[c + 4])),
-                                 "r"(pack_h2(h[8 + c], h[12 + c]))
-                                 : "memory");
+            for (int u = 0; u < kXBatch; ++u) {
+                const int task = base0 + u * kConsumers + lane;
+                lo[u] = hi[u] = make_uint4(0, 0, 0, 0);
+                if (task < ntask) {
+                    const int t = task & 3, j = (task >> 2) & 3, mb = task >> 4;
+                    const int m = (kM == 2 && mb >= p.B) ? 1 : 0;
+                    const int b = mb - m * p.B;
+                    const uint16_t *src = p.x + (int64_t)m * K + (int64_t)b * 256 + j * 64 + t * 16;
+                    lo[u] = *reinterpret_cast<const uint4 *>(src);
+                    hi[u] = *reinterpret_cast<const uint4 *>(src + 8);
                 }
             }
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if (kJpg >= 2) sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (kJpg >= 4) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-            if (valid && t == 0 && j % kJpg == 0) xg[m * ng + (b * 256 + j * 64) / kG] = sum;
+#pragma unroll
+            for (int u = 0; u < kXBatch; ++u) {
+                const int task = base0 + u * kConsumers + lane;
+                if (base0 + u * kConsumers >= ntask) break;  // warp-uniform
+                const bool valid = task < ntask;
+                const int t = task & 3, j = (task >> 2) & 3, mb = task >> 4;
+                const int m = (kM == 2 && mb >= p.B) ? 1 : 0;
+                const int b = mb - m * p.B;
+                const uint32_t w[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w, hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+                uint16_t h[16];
+                float sum = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    h[2 * i] = (uint16_t)(w[i] & 0xffffu);
+                    h[2 * i + 1] = (uint16_t)(w[i] >> 16);
+                    sum += h2f(h[2 * i]) + h2f(h[2 * i + 1]);
+                }
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t e = (uint32_t)((4 * m + c) * 4 + t);
+                        const uint32_t dst = xf + ((uint32_t)((b * 4 + j) * 16 * kM) + e) * 8u;
+                        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(pack_h2(h[c], h[c + 4])),
+                                     "r"(pack_h2(h[8 + c], h[12 + c]))
+                                     : "memory");
+                    }
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if (kJpg >= 2) sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                if (kJpg >= 4) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+                if (valid && t == 0 && j % kJpg == 0) xg[m * ng + (b * 256 + j * 64) / kG] = sum;
+            }
         }
     }
     consumers_sync();
@@ -465,16 +496,18 @@ bool plan_for(int kM, int64_t N, int64_t K, int grp, int device, A4Params &p)
     return true;
 }
 
-// codes as uint64 [N][K/16]: 16 x 16 boxes (128 bytes x 16 rows), 128-byte swizzle
+// codes as uint64 {16 words of a 256-code block, N rows, K/256 blocks}
+// (strides K/2 bytes for a row, 128 bytes for a block): a box of 16 x 16 x 8
+// is one stage, 16 KB, block-major in shared memory with 128-byte rows
 cudaError_t encode_codes(const uint8_t *qs, int64_t N, int64_t K, A4Params &p)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    const cuuint32_t box[2] = {16, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&p.tq, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(qs), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {16, (cuuint64_t)N, (cuuint64_t)(K / 256)};
+    const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), 128};
+    const cuuint32_t box[3] = {16, 16, 8};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&p.tq, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(qs), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

@@ -179,8 +179,8 @@ def test_affine4_rejects_bad_arguments(L):
     assert a4(L, y=NUL) == NULL
     assert a4(L, x=A2) == ALIGN
     assert a4(L, qs=A2) == ALIGN
-    assert a4(L, s=P(0x10001)) == ALIGN
-    assert a4(L, z=P(0x10001)) == ALIGN
+    assert a4(L, s=A2) == ALIGN
+    assert a4(L, z=A2) == ALIGN
     assert a4(L, y=A2, yd=0) == ALIGN
     assert a4(L, st=P(0x10002)) == ALIGN
     assert a4(L, M=0, x=NUL, y=NUL) == OK
