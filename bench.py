@@ -321,6 +321,47 @@ def prefill_gemm(torch, tq2, st, stream, M_list=(512, 2048)):
     return out
 
 
+def affine4_bytes(M, N, K, G):
+    """Algorithmic bytes of one affine-int4 call: 4-bit codes, fp16 s and z
+    per group, fp16 x, fp32 y."""
+    return N * K // 2 + 4 * N * (K // G) + 2 * M * K + 4 * M * N
+
+
+def affine4_shapes(torch, tq2, stream, groups=(64, 128, 256)):
+    """tq2_affine4_matvec at M = 1 on the layer shapes: back-to-back calls
+    over distinct weight copies (>= 4x L2 in total, so weights stream from
+    HBM), us per call, GB/s and the fraction of the measured HBM peak."""
+    import tq2_synth as syn
+    peak, _ = _peak()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = {}
+    for gname, (N, K) in (("qo_4096x4096", (4096, 4096)), ("gateup_16384x4096", (16384, 4096)),
+                          ("down_4096x16384", (4096, 16384))):
+        for G in groups:
+            qs, sc, z = syn.affine4_weights(SEED + 13, N, K, G)
+            one = [torch.from_numpy(a).to(dev) for a in (qs, sc, z)]
+            copies = max(2, int(4 * 129e6 // affine4_bytes(1, N, K, G)) + 1)
+            ws = [one] + [[t.clone() for t in one] for _ in range(copies - 1)]
+            x = torch.from_numpy(syn.activations(SEED + 13, 1, K)).to(dev)
+            ys = [torch.empty((1, N), dtype=torch.float32, device=dev) for _ in ws]
+            with torch.cuda.stream(stream):
+                for (q, a, b), y in zip(ws, ys):
+                    tq2.affine4_matvec(x, q, a, b, G, y=y)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for (q, a, b), y in zip(ws, ys):
+                        tq2.affine4_matvec(x, q, a, b, G, y=y)
+            once = time_graph(torch, g, stream, 2, 1)
+            ms = time_graph(torch, g, stream, max(3, int(0.3 / max(once * 1e-3, 1e-6))), 3)
+            us = 1e3 * ms / len(ws)
+            gbs = affine4_bytes(1, N, K, G) / (us * 1e-6) / 1e9
+            out[f"{gname}_G{G}"] = dict(us_per_call=us, gbs=gbs, frac_of_hbm_peak=gbs / peak,
+                                        distinct_tensors=len(ws))
+            del g, ws, ys, one
+    return out
+
+
 def cpu_baseline_oracle(budget_s=10.0):
     """The CPU oracle (fp64, one thread, as it stands) on layer 0 of the stack."""
     import numpy as np
@@ -458,6 +499,7 @@ def run_gpu(args):
                              groups=("gateup_16384x4096", "down_4096x16384"))
         extras["m_sweep"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep.items()}
         extras["prefill_gemm"] = prefill_gemm(torch, tq2, st, stream)
+        extras["affine4_m1"] = affine4_shapes(torch, tq2, stream)
 
     peak, peak_src = _peak()
     value = job_gbs(world, STACK_BYTES, ms)
@@ -537,6 +579,23 @@ def run_case(args):
     N, K = CASES[args.case]
     dev = torch.device("cuda", 0)
     tq2.load()
+    if args.affine4_group:  # the affine-int4 sibling: distinct copies of one weight set
+        G = args.affine4_group
+        one = [torch.from_numpy(a).to(dev) for a in syn.affine4_weights(SEED, N, K, G)]
+        ws4 = [one] + [[t.clone() for t in one] for _ in range(args.copies - 1)]
+        x = torch.from_numpy(syn.activations(SEED, args.M, K)).to(dev)
+        y = torch.empty((args.M, N), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.launches):
+            q, sc, z = ws4[i % len(ws4)]
+            tq2.affine4_matvec(x, q, sc, z, G, y=y)
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / args.launches
+        print(json.dumps({"case": args.case, "affine4_group": G, "N": N, "K": K, "M": args.M,
+                          "copies": args.copies, "launches": args.launches,
+                          "wall_us_per_call_eager": round(dt * 1e6, 2)}))
+        return
     ws = []
     for c in range(args.copies):
         bits = torch.from_numpy(syn.code_bits(SEED, syn.tensor_id(c, syn.SLOT_CODE_BITS),
@@ -617,6 +676,8 @@ def main():
     ap.add_argument("--copies", type=int, default=8)
     ap.add_argument("--launches", type=int, default=8)
     ap.add_argument("--case-impl", type=int, default=0)
+    ap.add_argument("--affine4-group", type=int, default=0,
+                    help="with --case: run tq2_affine4_matvec with this group size instead")
     args = ap.parse_args()
     if args.case:
         return run_case(args)

@@ -288,7 +288,12 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
 
     // Lane (g, t): A rows g and g + 8; B column / accumulator columns 2t and
     // 2t + 1, i.e. activation row t >> 1 and classes 2 (t & 1), 2 (t & 1) + 1.
+    // A row g is stage row rw = 2 (g & 3) + (g >> 2) (and rw + 8): a
+    // half-warp then reads rows 0, 2, 4, 6 (or 1, 3, 5, 7), whose swizzled
+    // 16-byte chunks are 8 distinct ones, so the code loads are free of bank
+    // conflicts.
     const int g = lane >> 2, t = lane & 3;
+    const int rw = 2 * (g & 3) + (g >> 2);
     const int pcls = t & 1;
     const int mrow = t >> 1;
     const bool mine = mrow < kM;
@@ -312,9 +317,9 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
             uint2 wl[4], wh[4], bx[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t off = (uint32_t)((((2 * j + (t >> 1)) ^ (g & 7)) << 4) + (t & 1) * 8);
-                wl[j] = lds64(cb + (uint32_t)g * 128u + off);
-                wh[j] = lds64(cb + (uint32_t)(g + 8) * 128u + off);
+                const uint32_t off = (uint32_t)((((2 * j + (t >> 1)) ^ rw) << 4) + (t & 1) * 8);
+                wl[j] = lds64(cb + (uint32_t)rw * 128u + off);
+                wh[j] = lds64(cb + (uint32_t)(rw + 8) * 128u + off);
                 bx[j] = (lane < 16 * kM) ? lds64(xf + ((uint32_t)((kb * 4 + j) * 16 * kM) + (uint32_t)lane) * 8u)
                                          : make_uint2(0u, 0u);
             }
@@ -343,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                 const float dlo = pcls ? (c[2][0] + c[3][1] * 0.0625f) : (c[0][0] + c[1][1] * 0.0625f);
                 const float dhi = pcls ? (c[2][2] + c[3][3] * 0.0625f) : (c[0][2] + c[1][3] * 0.0625f);
                 const int grp = kb * kGpb + gi;
-                const uint32_t plo = lds32(szs + (uint32_t)((rg * 16 + g) * szstr + grp) * 4u);
-                const uint32_t phi = lds32(szs + (uint32_t)((rg * 16 + g + 8) * szstr + grp) * 4u);
+                const uint32_t plo = lds32(szs + (uint32_t)((rg * 16 + rw) * szstr + grp) * 4u);
+                const uint32_t phi = lds32(szs + (uint32_t)((rg * 16 + rw + 8) * szstr + grp) * 4u);
                 const float slo = h2f((uint16_t)(plo & 0xffffu)), zlo = h2f((uint16_t)(plo >> 16));
                 const float shi = h2f((uint16_t)(phi & 0xffffu)), zhi = h2f((uint16_t)(phi >> 16));
                 // the zero-point term once per row and activation row (class pair 0)
@@ -367,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
             const float vlo = acc_lo + __shfl_xor_sync(0xffffffffu, acc_lo, 1);
             const float vhi = acc_hi + __shfl_xor_sync(0xffffffffu, acc_hi, 1);
             if (pcls == 0 && mine) {
-                red[((rg * kWarps + warp) * kM + mrow) * 16 + g] = vlo;
-                red[((rg * kWarps + warp) * kM + mrow) * 16 + g + 8] = vhi;
+                red[((rg * kWarps + warp) * kM + mrow) * 16 + rw] = vlo;
+                red[((rg * kWarps + warp) * kM + mrow) * 16 + rw + 8] = vhi;
             }
             acc_lo = acc_hi = 0.0f;
             kc = 0;
