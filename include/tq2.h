@@ -267,7 +267,8 @@ TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, con
  * the fp32 accumulation error scales with).  Deterministic run to run.
  * Errors: as tq2_matvec (TQ2_ERR_SHAPE, _NULL, _ALIGN, _DTYPE, _CUDA);
  * TQ2_ERR_ARG for G, or a K too long for the x staging to fit in shared
- * memory.  M = 0 or N = 0: nothing is done; K = 0: y = 0.
+ * memory (x of two activation rows is staged whole: K up to ~90,000 for one
+ * row, ~45,000 for two).  M = 0 or N = 0: nothing is done; K = 0: y = 0.
  */
 TQ2_API tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,
                                       const uint16_t *z, int64_t N, int64_t K, int64_t G, void *y,

@@ -370,7 +370,7 @@ tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, c
 
     int dev = 0;
     if ((st = current_device(&dev)) != TQ2_OK) return st;
-    if (!tq2::affine4_supported(N, K, G, dev)) return TQ2_ERR_ARG;
+    if (!tq2::affine4_supported(M, N, K, G, dev)) return TQ2_ERR_ARG;
     tq2::Affine4Args a;
     a.x = x;
     a.qs = qs;

@@ -77,7 +77,7 @@ struct Affine4Args {
     int y_f16;
     cudaStream_t stream;
 };
-bool affine4_supported(int64_t N, int64_t K, int64_t G, int device);
+bool affine4_supported(int64_t M, int64_t N, int64_t K, int64_t G, int device);
 cudaError_t launch_affine4(const Affine4Args &a, int device);
 
 // CUDA-core path (fp32 FMA per code), any M in 1..16.

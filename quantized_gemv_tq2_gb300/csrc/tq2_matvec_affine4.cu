@@ -520,11 +520,13 @@ cudaError_t encode_codes(const uint8_t *qs, int64_t N, int64_t K, A4Params &p)
 
 }  // namespace
 
-bool affine4_supported(int64_t N, int64_t K, int64_t grp, int device)
+bool affine4_supported(int64_t M, int64_t N, int64_t K, int64_t grp, int device)
 {
-    if (N < 1 || K < 256 || K % 256 != 0 || (grp != 64 && grp != 128 && grp != 256)) return false;
+    if (M < 1 || N < 1 || K < 256 || K % 256 != 0 || (grp != 64 && grp != 128 && grp != 256)) return false;
     A4Params p{};
-    return plan_for(2, N, K, (int)grp, device, p) && plan_for(1, N, K, (int)grp, device, p);
+    // the launches take activation rows two at a time, the last one alone when M is odd
+    if (M >= 2 && !plan_for(2, N, K, (int)grp, device, p)) return false;
+    return (M % 2 == 0) || plan_for(1, N, K, (int)grp, device, p);
 }
 
 cudaError_t launch_affine4(const Affine4Args &a, int device)

@@ -114,3 +114,25 @@ def test_affine4_layer_shapes_sampled(T, N, K, G):
     y_ref, tol = oracle.affine4_rows(x, qs, s, z, K, G, rows)
     y = _run(T, x, qs, s, z, G)
     assert_within_tolerance(y[:, rows].astype(np.float64), y_ref, tol, f"N={N} K={K} G={G}")
+
+
+def test_affine4_long_k(T):
+    """K = 32768 (128 blocks of x staged per CTA; two activation rows need
+    the one-CTA-per-SM plan): full compare against the oracle."""
+    x, qs, s, z = _case(21, 2, 40, 32768, 256, heavy=True)
+    y_ref, tol = oracle.affine4(x, qs, s, z, 32768, 256)
+    y = _run(T, x, qs, s, z, 256)
+    assert_within_tolerance(y.astype(np.float64), y_ref, tol, "K=32768")
+
+
+def test_affine4_k_too_long_is_an_argument_error(T):
+    """x of two rows at K = 131072 cannot be staged in shared memory: the
+    call returns TQ2_ERR_ARG before launching anything."""
+    import quantized_gemv_tq2_gb300 as tq2
+    K, N = 131072, 16
+    x = T.zeros((2, K), dtype=T.float16, device="cuda")
+    qs = T.zeros((N, K // 2), dtype=T.uint8, device="cuda")
+    s = T.zeros((N, K // 64), dtype=T.float16, device="cuda")
+    with pytest.raises(tq2.TQ2Error) as e:
+        tq2.affine4_matvec(x, qs, s, s, 64)
+    assert e.value.status == 5
