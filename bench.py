@@ -388,18 +388,21 @@ def cpu_baseline_oracle(budget_s=10.0):
 
 def read_profile_traffic():
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel source (sha256 match); else None."""
+    on the current kernel sources (sha256 of both kernels of the step match);
+    else None."""
     import hashlib
-    src = os.path.join(ROOT, "quantized_gemv_tq2_gb300", "csrc", "tq2_matvec_mma.cu")
+    csrc = os.path.join(ROOT, "quantized_gemv_tq2_gb300", "csrc")
     prof = os.path.join(ROOT, "profiles", "tq2_matvec_mma_stack_m1.md")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = {key: hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest()
+               for key, f in (("kernel_source_sha256", "tq2_matvec_mma.cu"),
+                              ("smalln_source_sha256", "tq2_matvec_smalln.cu"))}
         vals = {}
         for line in open(prof):
             if ":" in line and line.strip().startswith("- `"):
                 k, v = line.strip()[3:].split("`:", 1)
                 vals[k.strip()] = v.strip().strip("`")
-        if vals.get("kernel_source_sha256") != sha:
+        if any(vals.get(k) != v for k, v in sha.items()):
             return None
         return float(vals["traffic_bytes_per_launch_avg"])
     except Exception:
@@ -533,7 +536,8 @@ def run_gpu(args):
         "pct_of_peak": round(100 * per_gpu / peak, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "tq2::matvec_mma_kernel<1> (all 224 launches of a step)",
+            "kernel": "tq2::matvec_mma_kernel<1> (q, o, gate, up, down: 160 launches) and "
+                      "tq2::matvec_smalln_kernel<1,1> (k, v: 64 launches): all 224 launches of a step",
             "achieved": round(per_gpu, 2),
             "peak": peak,
             "unit": "GB/s",

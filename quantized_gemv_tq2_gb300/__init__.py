@@ -24,11 +24,12 @@ __all__ = [
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_TC05", "IMPL_PS", "IMPL_DP4", "IMPL_GEMM",
+    "IMPL_SMALLN",
 ]
 
 F32, F16 = 0, 1
 FLAG_BAD_CODE, FLAG_NONFINITE, FLAG_INEXACT, FLAG_TIMEOUT = 1, 2, 4, 8
-IMPL_AUTO, IMPL_MMA, IMPL_SIMT, IMPL_TC05, IMPL_PS, IMPL_DP4, IMPL_GEMM = 0, 1, 2, 3, 4, 5, 6
+IMPL_AUTO, IMPL_MMA, IMPL_SIMT, IMPL_TC05, IMPL_PS, IMPL_DP4, IMPL_GEMM, IMPL_SMALLN = 0, 1, 2, 3, 4, 5, 6, 7
 HEADER = os.path.join(os.path.dirname(_build.PKG), "include", "tq2.h")
 
 _lock = threading.Lock()

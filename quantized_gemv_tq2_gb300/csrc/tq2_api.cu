@@ -85,8 +85,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
     if (!(out_scale >= 0.0f) || !std::isfinite(out_scale)) return TQ2_ERR_ARG;
-    if (impl < 0 || impl > 6) return TQ2_ERR_ARG;
-    if ((impl == 1 || impl == 3) && M > 2) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 7) return TQ2_ERR_ARG;
+    if ((impl == 1 || impl == 3 || impl == 7) && M > 2) return TQ2_ERR_ARG;
     if (impl == 5 && M > 1) return TQ2_ERR_ARG;
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
@@ -118,7 +118,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     a.inv_out = out_scale != 0.0f ? 1.0f / out_scale : 0.0f;
     a.stream = s;
 
-    // impl 0: for M <= 2 the class-column mma.sync kernel; for more rows the
+    // impl 0: for M <= 2 and a few output rows per CTA (k/v-sized N) the
+    // small-N kernel, else for M <= 2 the class-column mma.sync kernel; for more rows the
     // pre-scaled mma.sync kernel, whose time grows with M, until the tcgen05
     // GEMM (whose time is flat up to 16 rows: an MMA of 128 weight rows x up
     // to 64 activation rows costs the same) is faster -- measured on GB300:
@@ -128,7 +129,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     int which = impl;
     if (impl == 0) {
         const bool gemm_wins = a.M >= 10 || (a.M >= 6 && K >= 8192) || (a.M >= 8 && N <= 512);
-        if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
+        if (a.M <= 2 && tq2::smalln_matvec_preferred(a.M, N, K, dev)) which = 7;
+        else if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
         else if (gemm_wins && tq2::gemm_tc05_supported(a.M, N, K, dev)) which = 6;
         else if (tq2::ps_matvec_supported(a.M, N, K, dev)) which = 4;
         else which = 2;
@@ -142,12 +144,15 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
         return TQ2_ERR_ARG;
     } else if (impl == 6 && !tq2::gemm_tc05_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
+    } else if (impl == 7 && !tq2::smalln_matvec_supported(a.M, N, K, dev)) {
+        return TQ2_ERR_ARG;
     }
     cudaError_t e = (which == 3)   ? tq2::launch_matvec_tc05(a, dev)
                     : (which == 1) ? tq2::launch_matvec_mma(a, dev)
                     : (which == 4) ? tq2::launch_matvec_ps(a, dev)
                     : (which == 5) ? tq2::launch_matvec_dp4(a, dev)
                     : (which == 6) ? tq2::launch_gemm_tc05(a, dev)
+                    : (which == 7) ? tq2::launch_matvec_smalln(a, dev)
                                    : tq2::launch_matvec_simt(a, dev);
     if (e == cudaSuccess) e = cudaGetLastError();
     return from_cuda(e);

@@ -80,6 +80,14 @@ struct Affine4Args {
 bool affine4_supported(int64_t M, int64_t N, int64_t K, int64_t G, int device);
 cudaError_t launch_affine4(const Affine4Args &a, int device);
 
+// Few-rows-per-CTA path for small N (k/v-sized): M <= 2, K <= 16384, at most
+// 4 output rows per CTA with one CTA per SM; codes and scales in registers
+// before the PDL wait, CUDA-core sums, one reduction.  Returns false when
+// the shape does not fit.
+bool smalln_matvec_supported(int M, int64_t N, int64_t K, int device);
+bool smalln_matvec_preferred(int M, int64_t N, int64_t K, int device);  // faster than impl 1 here
+cudaError_t launch_matvec_smalln(const MatvecArgs &a, int device);
+
 // CUDA-core path (fp32 FMA per code), any M in 1..16.
 cudaError_t launch_matvec_simt(const MatvecArgs &a, int device);
 

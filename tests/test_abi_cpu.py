@@ -57,7 +57,8 @@ def test_matvec_rejects_bad_dtype_and_args(L):
     assert mv(L, s=-0.5) == ARG
     assert mv(L, s=float("nan")) == ARG
     assert mv(L, s=float("inf")) == ARG
-    assert mv(L, impl=7) == ARG
+    assert mv(L, impl=8) == ARG
+    assert mv(L, impl=7, M=3) == ARG  # the small-N kernel takes M <= 2
     assert mv(L, impl=5, M=2) == ARG  # the dp4a kernel takes M = 1
     assert mv(L, impl=-1) == ARG
     assert mv(L, impl=1, M=3) == ARG  # the class-column tensor-core kernels take M <= 2
@@ -77,7 +78,7 @@ def test_requant_rejects_bad_arguments(L):
     assert rq(L, K=300) == SHAPE
     assert rq(L, M=17) == SHAPE
     assert rq(L, yd=3) == DTYPE
-    assert rq(L, impl=7) == ARG
+    assert rq(L, impl=8) == ARG
     assert rq(L, impl=1, M=3) == ARG
     assert rq(L, x=NUL) == NULL
     assert rq(L, y=A2) == ALIGN

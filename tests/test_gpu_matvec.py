@@ -11,7 +11,7 @@ from gpu_util import Case, assert_within_tolerance, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = {"auto": 0, "mma": 1, "simt": 2, "tc05": 3, "ps": 4, "dp4": 5, "gemm": 6}
+IMPLS = {"auto": 0, "mma": 1, "simt": 2, "tc05": 3, "ps": 4, "dp4": 5, "gemm": 6, "smalln": 7}
 
 
 @pytest.fixture(scope="module")
@@ -31,7 +31,7 @@ def _run(T, case, impl, y_dtype=0, rows=None):
     try:
         y = tq2.matvec(x, qs, d, y_dtype=y_dtype, act_scale=case.s, status=st, impl=impl)
     except tq2.TQ2Error as e:
-        if e.status == 5 and impl in (1, 3, 4, 5, 6):
+        if e.status == 5 and impl in (1, 3, 4, 5, 6, 7):
             return None
         raise
     T.cuda.synchronize()
@@ -42,8 +42,8 @@ def _run(T, case, impl, y_dtype=0, rows=None):
 
 def _impls_for(M):
     if M == 1:
-        return ["auto", "tc05", "mma", "ps", "dp4", "gemm", "simt"]
-    return ["auto", "tc05", "mma", "ps", "gemm", "simt"] if M <= 2 else ["auto", "ps", "gemm", "simt"]
+        return ["auto", "tc05", "mma", "ps", "dp4", "gemm", "smalln", "simt"]
+    return ["auto", "tc05", "mma", "ps", "gemm", "smalln", "simt"] if M <= 2 else ["auto", "ps", "gemm", "simt"]
 
 
 # ---------------------------------------------------------------- small shapes, full compare
@@ -63,6 +63,21 @@ def test_matvec_small_shapes(T, M, N, K, prologue):
             if y is None:
                 continue
             assert_within_tolerance(y, y_ref, tol, f"{name} yd={yd} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 4096), (2, 256, 4096), (1, 600, 4096), (2, 608, 16384),
+                                   (1, 152, 12288), (1, 7, 256)])
+@pytest.mark.parametrize("prologue", [False, True])
+def test_matvec_small_n_kernel(T, M, N, K, prologue):
+    """impl 7 (one to four output rows per CTA, CUDA-core sums) on the k/v
+    shape and at its limits: 4 rows per CTA, K = 16384 with two activation
+    rows, K not a multiple of 4096, fewer rows than SMs; both y dtypes."""
+    case = Case(seed=N + K + M, M=M, N=N, K=K, heavy=prologue, prologue=prologue)
+    y_ref, tol = case.reference()
+    for yd in (0, 1):
+        y = _run(T, case, IMPLS["smalln"], y_dtype=yd)
+        assert y is not None, "the small-N kernel refused a shape it should take"
+        assert_within_tolerance(y, y_ref, tol, f"smalln yd={yd} M={M} N={N} K={K}")
 
 
 def test_matvec_pr1_seed0(T):
@@ -121,7 +136,7 @@ def test_matvec_one_hot_large_k(T):
         x = np.zeros((1, K), dtype=np.float16)
         x[0, k] = 1.0
         want = case.d[:, k // 256].astype(np.float64) * (case.codes[:, k].astype(np.float64) - 1)
-        for impl in ("mma", "tc05", "ps", "dp4", "simt"):
+        for impl in ("mma", "tc05", "ps", "dp4", "smalln", "simt"):
             got = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl]))[0].astype(np.float64)
             assert np.array_equal(got, want), (impl, k)
 
