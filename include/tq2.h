@@ -130,7 +130,9 @@ TQ2_API tq2_status tq2_from_dense(const void *W, tq2_dtype w_dtype, int64_t N, i
  * Weights and scales are prefetched before the kernel waits on the previous
  * kernel in the stream (programmatic dependent launch): qs and d must not be
  * written by the kernel that immediately precedes this call on the stream
- * when that kernel is itself a tq2_matvec.
+ * when that kernel is itself one of this library's products (tq2_matvec,
+ * tq2_matvec_impl, tq2_matvec_requant, tq2_matvec_grouped, tq2_gemm,
+ * tq2_affine4_matvec), which let the next kernel start early.
  */
 TQ2_API tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                       int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
@@ -269,6 +271,9 @@ TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, con
  * Accuracy: |y - exact| <= 1e-3 * sum_g |s_g| sum_{k in g} |x_k| (q_k +
  * |z_g|) + 1e-6 per element (the magnitude of the two factored sums, which
  * the fp32 accumulation error scales with).  Deterministic run to run.
+ * As tq2_matvec, qs, s and z are read before the wait on the previous kernel
+ * in the stream: the immediately preceding kernel, if one of this library's,
+ * must not write them.
  * Errors: as tq2_matvec (TQ2_ERR_SHAPE, _NULL, _ALIGN, _DTYPE, _CUDA);
  * TQ2_ERR_ARG for G, or a K too long for the x staging to fit in shared
  * memory (x of two activation rows is staged whole: K up to ~90,000 for one
