@@ -251,10 +251,11 @@ SHAPE_GROUPS = {"qo_4096x4096": ("q", "o"), "kv_256x4096": ("k", "v"),
                 "gateup_16384x4096": ("gate", "up"), "down_4096x16384": ("down",)}
 
 
-def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None):
+def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None, heavy=False, prologue=False):
     """Back-to-back calls of one shape over the stack's distinct tensors
     (q/o: 64 tensors, 278 MB; k/v: 64, 18 MB -- L2-resident; gate/up: 64,
-    1.1 GB; down: 32, 555 MB)."""
+    1.1 GB; down: 32, 555 MB); optionally heavy-tailed x (1 % of entries
+    x50) and the int8 prologue with each linear's act_scale."""
     out = {}
     dev = st["X"].device
     for gname, names in SHAPE_GROUPS.items():
@@ -264,9 +265,10 @@ def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None):
         N, K = st["lin"][idx[0]][2], st["lin"][idx[0]][3]
         for M in M_list:
             import tq2_synth as syn
-            x = torch.from_numpy(syn.activations(SEED + 7, M, K, linear=0)).to(dev)
+            x = torch.from_numpy(syn.activations(SEED + 7, M, K, linear=0, heavy=heavy)).to(dev)
             ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in idx]
-            calls = [(x, st["qs"][i], st["d"][i], y, 0.0, impl, 0.0) for i, y in zip(idx, ys)]
+            calls = [(x, st["qs"][i], st["d"][i], y, st["scales"][i] if prologue else 0.0, impl, 0.0)
+                     for i, y in zip(idx, ys)]
             g = capture(torch, tq2, st, calls, stream)
             one = time_graph(torch, g, stream, 2, 1)
             reps = max(3, int(0.3 / max(one * 1e-3, 1e-6)))  # ~0.3 s of replays
@@ -536,6 +538,9 @@ def run_gpu(args):
         sweep = shape_graphs(torch, tq2, st, stream, M_list=(2, 4, 8, 16),
                              groups=("gateup_16384x4096", "down_4096x16384"))
         extras["m_sweep"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep.items()}
+        sweep_h = shape_graphs(torch, tq2, st, stream, M_list=(1, 2, 4, 8, 16),
+                               groups=("gateup_16384x4096", "down_4096x16384"), heavy=True, prologue=True)
+        extras["m_sweep_heavy_prologue"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep_h.items()}
         extras["prefill_gemm"] = prefill_gemm(torch, tq2, st, stream)
         extras["affine4_m1"] = affine4_shapes(torch, tq2, stream)
 
