@@ -33,7 +33,8 @@
 //     (1024 + q) - 1025 = q - 1 (exact) times d_b, written with tcgen05.st
 //     into a ring of 64-column TMEM slots (one per stage); with the int8
 //     prologue they also fake-quantise each x stage in shared memory first
-//     (element-wise, 1/8 of the stage per warp) and release it to the MMA
+//     (element-wise, by the half of the warps that expands the stage, a
+//     quarter each, so the halves stay independent) and release it to the MMA
 //     issuer (a generic-to-async proxy fence, then an mbarrier); at the end
 //     they read D (one
 //     column per activation row) and store y, with the optional int8
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(bfull0 + 8u * i, 1);
-            mbar_init(bconv0 + 8u * i, kUnpackWarps);
+            mbar_init(bconv0 + 8u * i, kUnpackWarps / 2);  // the half that expands the stage converts it
             mbar_init(afull0 + 8u * i, 4);
             mbar_init(sempty0 + 8u * i, 1);
         }
@@ -297,10 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     {
         bool alive = true;
         int cur_w = -1;
-        for (int g = prologue ? 0 : half; g < ngroups; g += prologue ? 1 : 2) {
+        for (int g = half; g < ngroups; g += 2) {
             if (prologue) {
                 // x' = clamp(rint(x * (1/s)), -128, 127) (times s at the store),
-                // this warp's 1/8 of stage g, in place
+                // in place, by the half of the warps that expands stage g (a
+                // quarter each): the two halves stay independent, as without
+                // the prologue
                 const int r = g % SB;
                 if (alive &&
                     !__all_sync(0xffffffffu, mbar_wait(bfull0 + 8u * (uint32_t)r, (uint32_t)((g / SB) & 1)))) {
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 }
                 if (alive) {
                     const uint32_t xb = bring + (uint32_t)r * (2u * BN * 128u);
-                    for (int c = uw * 32 + lane; c < 2 * BN * 8; c += kUnpackWarps * 32) {
+                    for (int c = (uw & 3) * 32 + lane; c < 2 * BN * 8; c += (kUnpackWarps / 2) * 32) {
                         const uint4 v = lds128(xb + (uint32_t)c * 16u);
                         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -326,7 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bconv0 + 8u * (uint32_t)r);
-                if ((g & 1) != half) continue;  // the other half expands this group's A
             }
             const int ws = g >> 1;           // code stage (2 groups)
             const int u0 = (g & 1) * 2;      // first 16-byte unit of the group in the row
