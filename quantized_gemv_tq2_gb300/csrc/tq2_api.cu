@@ -122,13 +122,23 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     // small-N kernel, else for M <= 2 the class-column mma.sync kernel; for more rows the
     // pre-scaled mma.sync kernel, whose time grows with M, until the tcgen05
     // GEMM (whose time is flat up to 16 rows: an MMA of 128 weight rows x up
-    // to 64 activation rows costs the same) is faster -- measured on GB300:
-    // from M = 10, from M = 6 when K >= 8192, from M = 8 when N <= 512;
-    // CUDA cores as the last resort.  The tcgen05 matvec (impl 3) is correct
-    // but slower, so it runs only on request.
+    // to 64 activation rows costs the same) is faster; CUDA cores as the last
+    // resort.  The crossovers, measured on GB300 (us per call, back to back
+    // over distinct weights, pre-scaled against GEMM):
+    //   q/o 4096x4096:      M = 8: 6.9 / 9.5, M = 10: 9.8 / 9.5; with the
+    //                       int8 prologue M = 10: 11.2 / 11.2, M = 12: 12.5 / 11.2
+    //   gate/up 16384x4096: M = 12: 19.5 / 22.9, M = 16: 23.3 / 22.9; with
+    //                       the prologue M = 16: 25.6 / 29.7
+    //   down 4096x16384:    M = 7: 23.9 / 25.5, M = 8: 25.5 / 25.5; with the
+    //                       prologue M = 8: 30.9 / 32.9, M = 10: 41.6 / 33.0
+    // (the GEMM applies the prologue per x stage, the pre-scaled kernel once
+    // per call, so the prologue moves the crossover up).  The tcgen05 matvec
+    // (impl 3) is correct but slower, so it runs only on request.
     int which = impl;
     if (impl == 0) {
-        const bool gemm_wins = a.M >= 10 || (a.M >= 6 && K >= 8192) || (a.M >= 8 && N <= 512);
+        const bool gemm_wins = (act_scale != 0.0f)
+                                   ? (a.M >= 9 && K >= 8192) || (a.M >= 8 && N <= 512) || (a.M >= 11 && N < 8192)
+                                   : (a.M >= 8 && (K >= 8192 || N <= 512)) || (a.M >= 10 && N < 8192) || a.M >= 16;
         if (a.M <= 2 && tq2::smalln_matvec_preferred(a.M, N, K, dev)) which = 7;
         else if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
         else if (gemm_wins && tq2::gemm_tc05_supported(a.M, N, K, dev)) which = 6;

@@ -89,13 +89,29 @@ __device__ __forceinline__ void report_timeout(const PsParams &p, volatile int *
 //   frag:  block bx (within the x chunk) holds 512*M bytes; n-tile nt starts
 //          at 4096*nt and has Mt = min(8, M - 8nt) columns; word slot jw
 //          (0..3) is a 128*Mt region; in it, (half h, quad t, column g) is a
-//          16-byte entry at (h*4*Mt + t*Mt + g)*16.  Half 0 holds classes 0, 1,
-//          half 1 classes 2, 3, each class as the (b0, b1) register pair.
+//          16-byte entry at (h*4*Mt + t*Mt + col)*16, col = g for a partial
+//          n-tile and g ^ sw(t, jw) for a full one (Mt = 8).  Half 0 holds
+//          classes 0, 1, half 1 classes 2, 3, each class as the (b0, b1)
+//          register pair.
 //   xinfo: float2 (C init, rescale) per (block, column), 8*NT columns a block.
+// The swizzle of a full n-tile: shared memory serves a 16-byte access of 8
+// lanes at a time, one 16-byte slot of each 128-byte row per lane.  The MMA
+// reads (lanes g in {2q, 2q+1} x t in 0..3, fixed jw) and the staging writes
+// (lanes t in {2p, 2p+1} x jw in 0..3, fixed g) each need 8 distinct slots
+// mod 8; with col = g, Mt = 8 gives 4 and 1 (measured at M = 8: 560 K load
+// and 557 K store bank conflicts per q/o call, 55 K and 188 K at M = 6).
+// sw = (jw & 1) | (t & 1) << 1 | ((t >> 1) ^ (jw >> 1)) << 2 puts g's bits,
+// t's and jw's each on their own bit of the slot, so both read 8.
+__device__ __forceinline__ int col_slot(int t, int g, int jw, int Mt)
+{
+    const int sw = (jw & 1) | ((t & 1) << 1) | (((t >> 1) ^ (jw >> 1)) << 2);
+    return t * Mt + (Mt == 8 ? (g ^ sw) : g);
+}
+
 __device__ __forceinline__ uint32_t frag_off(int bx, int nt, int jw, int h, int t, int g, int M)
 {
     const int Mt = min(8, M - 8 * nt);
-    return (uint32_t)(bx * 512 * M + nt * 4096 + jw * 128 * Mt + (h * 4 * Mt + t * Mt + g) * 16);
+    return (uint32_t)(bx * 512 * M + nt * 4096 + jw * 128 * Mt + (h * 4 * Mt + col_slot(t, g, jw, Mt)) * 16);
 }
 
 // Turn x (rows m, blocks [kb0, kb0 + nbx)) into B fragments and xinfo.
@@ -206,17 +222,19 @@ __device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uin
 }
 
 // 16 HMMA of one (16-row group, 256-block) unit for n-tile nt: words jw of
-// rows g and g + 8 are (wa, wb); two accumulator chains, merged on return.
+// rows g and g + 8 are (wa, wb); the block's B fragments start at fb, this
+// lane's entry of word jw, half 0, at fb + xo[jw], of half 1 at + h1; two
+// accumulator chains, merged on return.
 __device__ __forceinline__ void unit_mma(float (&c)[4], const uint32_t (&wa)[4], const uint32_t (&wb)[4],
-                                         uint32_t fb, uint32_t jw_stride, float2 init)
+                                         uint32_t fb, const uint32_t (&xo)[4], uint32_t h1, float2 init)
 {
     float ca[4] = {init.x, init.y, init.x, init.y};
     float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int jw = 0; jw < 4; ++jw) {
         const uint32_t w0 = wa[jw], w1 = wb[jw], s0 = w0 >> 8, s1 = w1 >> 8;
-        const uint4 f0 = lds128(fb + (uint32_t)jw * jw_stride);
-        const uint4 f1 = lds128(fb + (uint32_t)jw * jw_stride + 64u * (jw_stride >> 7));
+        const uint4 f0 = lds128(fb + xo[jw]);
+        const uint4 f1 = lds128(fb + xo[jw] + h1);
         float (&cc)[4] = (jw < 2) ? ca : cb;
         mma_16816(cc, w0 & 0x00030003u, w1 & 0x00030003u, s0 & 0x00030003u, s1 & 0x00030003u, f0.x, f0.y);
         mma_16816(cc, w0 & 0x000C000Cu, w1 & 0x000C000Cu, s0 & 0x000C000Cu, s1 & 0x000C000Cu, f0.z, f0.w);
@@ -368,9 +386,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     consumers_sync();
 
     const int g = lane >> 2, t = lane & 3;
-    int gsel[NT];
+    uint32_t xo[NT][4];  // this lane's B entry of word jw within a block, per n-tile
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) gsel[nt] = (8 * nt + g < M) ? g : 0;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int gsel = (8 * nt + g < M) ? g : 0;
+#pragma unroll
+        for (int jw = 0; jw < 4; ++jw) xo[nt][jw] = frag_off(0, nt, jw, 0, t, gsel, M);
+    }
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
@@ -441,10 +463,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int Mt = min(8, M - 8 * nt);
-                    const uint32_t fb = frag + frag_off(bx, nt, 0, 0, t, gsel[nt], M);
+                    const uint32_t fb = frag + (uint32_t)(bx * 512 * M);
                     const float4 xi = *reinterpret_cast<const float4 *>(&xinfo[bx * 8 * NT + 8 * nt + 2 * t]);
                     float c[4];
-                    unit_mma(c, wa, wb, fb, (uint32_t)(128 * Mt), make_float2(xi.x, xi.z));
+                    unit_mma(c, wa, wb, fb, xo[nt], (uint32_t)(64 * Mt), make_float2(xi.x, xi.z));
                     acc[nt][0] = fmaf(c[0], xi.y * d0, acc[nt][0]);
                     acc[nt][1] = fmaf(c[1], xi.w * d0, acc[nt][1]);
                     acc[nt][2] = fmaf(c[2], xi.y * d8, acc[nt][2]);
@@ -582,9 +604,14 @@ int max_dynamic_smem(int device)
     return v;
 }
 
-// Prefer a plan that lets two CTAs share an SM (the next call's weights then
-// stream while this one computes), resident x before K-chunked x, and one CTA
-// per SM before more.
+// Prefer resident x (staged once) over K-chunked x, then a plan that lets two
+// CTAs share an SM (the next call's weights then stream while this one
+// computes) over one CTA per SM, and one CTA per SM before more.  Resident x
+// on one CTA per SM beats K-chunked x on two where both fit (measured on
+// GB300, back-to-back calls: down 4096x16384 at M = 3 / 4 / 5: 15.7 / 17.7 /
+// 18.9 against 16.4 / 18.3 / 19.7 us; gate/up 16384x4096 at M = 7 / 8: 14.2
+// / 18.7 against 14.7 / 19.0 us): K-chunked x is re-staged per K range
+// behind two barriers that drain the stage ring.
 bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
 {
     const int max_dyn = (M <= 8) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
@@ -595,6 +622,9 @@ bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
         for (int cap : {kTwoPerSm, max_dyn}) {
             if (cap > max_dyn) continue;
             if (make_plan(M, N, K, G, cap, true, 0, p)) return true;
+        }
+        for (int cap : {kTwoPerSm, max_dyn}) {
+            if (cap > max_dyn) continue;
             for (int kcb : {16, 8, 4, 2, 1})
                 if (make_plan(M, N, K, G, cap, false, kcb, p)) return true;
         }
