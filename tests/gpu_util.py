@@ -60,3 +60,30 @@ def sample_rows(N, count, seed=0):
     r = set(int(v) for v in base if 0 <= v < N)
     r.update(int(v) for v in rng.choice(N, size=min(count, N), replace=False))
     return np.array(sorted(r), dtype=np.int64)
+
+
+class GuardedOutput:
+    """An output tensor [M, N] inside a larger buffer whose PAD elements on
+    each side hold a canary bit pattern, to catch writes outside [M, N]."""
+
+    PAD = 256
+
+    def __init__(self, M, N, dtype_code=0):
+        import torch
+        self.M, self.N = M, N
+        if dtype_code == 0:
+            self.buf = torch.empty(M * N + 2 * self.PAD, dtype=torch.int32, device="cuda")
+            self.buf.fill_(0x7F8DEAD5)  # a NaN pattern no kernel writes
+            self.y = self.buf[self.PAD:self.PAD + M * N].view(torch.float32).view(M, N)
+        else:
+            self.buf = torch.empty(M * N + 2 * self.PAD, dtype=torch.int16, device="cuda")
+            self.buf.fill_(0x7E5B)
+            self.y = self.buf[self.PAD:self.PAD + M * N].view(torch.float16).view(M, N)
+        self.canary = self.buf[0].item()
+
+    def check(self, what=""):
+        import torch
+        lo = self.buf[:self.PAD]
+        hi = self.buf[self.PAD + self.M * self.N:]
+        assert bool(torch.all(lo == self.canary)), f"{what}: write below y"
+        assert bool(torch.all(hi == self.canary)), f"{what}: write above y"

@@ -39,7 +39,7 @@ __all__ = [
     "SLOT_ACT_SCALE", "SLOT_DENSE", "SLOT_OUT_SCALE",
     "tensor_id", "words", "uniform", "normal",
     "code_bits", "codes_from_bits", "codes_from_bits_torch", "codes", "scales", "activations",
-    "act_scale", "dense_normal",
+    "act_scale", "dense_normal", "small_int_activations", "pow2_scales",
 ]
 
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -56,6 +56,8 @@ SLOT_ACT_SCALE = 5
 SLOT_DENSE = 6
 SLOT_OUT_SCALE = 7
 SLOT_ZERO_POINT = 8
+SLOT_EXACT_X = 9
+SLOT_EXACT_D = 10
 
 
 def tensor_id(linear: int, slot: int) -> int:
@@ -166,6 +168,25 @@ def dense_normal(seed: int, n: int, k: int, linear: int = 0,
     """A generic (not ternary) dense weight [n, k] fp32 ~ N(0, sigma^2)."""
     z = normal(seed, tensor_id(linear, SLOT_DENSE), n * k)
     return (sigma * z).astype(np.float32).reshape(n, k)
+
+
+# ---------------------------------------------------------------- exact-sum inputs
+def small_int_activations(seed: int, m: int, k: int, linear: int = 0,
+                          amax: int = 2, exp: int = -2) -> np.ndarray:
+    """x [m, k] fp16 with every entry an integer in [-amax, amax] times 2^exp
+    (uniform on the integers).  With power-of-two scales every partial sum of
+    the matvec is then an exact fp32 value at the sizes used here."""
+    u = uniform(seed, tensor_id(linear, SLOT_EXACT_X), m * k)
+    a = np.floor(u * (2 * amax + 1)) - amax
+    return (a * 2.0 ** exp).astype(np.float16).reshape(m, k)
+
+
+def pow2_scales(seed: int, n: int, nblocks: int, linear: int = 0,
+                emin: int = -4, emax: int = 0) -> np.ndarray:
+    """Block scales [n, nblocks] fp16, each 2^e with e uniform on [emin, emax]."""
+    u = uniform(seed, tensor_id(linear, SLOT_EXACT_D), n * nblocks)
+    e = emin + np.floor(u * (emax - emin + 1))
+    return np.exp2(e).astype(np.float16).reshape(n, nblocks)
 
 
 # ---------------------------------------------------------------- affine int4
