@@ -251,34 +251,62 @@ SHAPE_GROUPS = {"qo_4096x4096": ("q", "o"), "kv_256x4096": ("k", "v"),
                 "gateup_16384x4096": ("gate", "up"), "down_4096x16384": ("down",)}
 
 
-def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None, heavy=False, prologue=False):
-    """Back-to-back calls of one shape over the stack's distinct tensors
-    (q/o: 64 tensors, 278 MB; k/v: 64, 18 MB -- L2-resident; gate/up: 64,
-    1.1 GB; down: 32, 555 MB); optionally heavy-tailed x (1 % of entries
-    x50) and the int8 prologue with each linear's act_scale."""
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
+
+
+def shape_pool(torch, st, names, min_bytes=4 * L2_BYTES):
+    """Distinct (qs, d) pairs of one shape totalling at least min_bytes: the
+    stack's own tensors first, then copies of them (new allocations), so
+    that back-to-back calls read their weights from HBM, not L2."""
+    idx = [i for i, (L, n, N, K) in enumerate(st["lin"]) if n in names]
+    N, K = st["lin"][idx[0]][2], st["lin"][idx[0]][3]
+    per = N * K // 4 + 2 * N * (K // 256)
+    need = max(len(idx), -(-min_bytes // per))
+    pool = [(st["qs"][i], st["d"][i]) for i in idx]
+    j = 0
+    while len(pool) < need:
+        q, d = pool[j % len(idx)]
+        pool.append((q.clone(), d.clone()))
+        j += 1
+    return pool, N, K
+
+
+def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None, heavy=False, prologue=False,
+                 repeats=21):
+    """Back-to-back calls of one shape over distinct weight sets totalling at
+    least 4x L2 (q/o 120 sets, 520 MB; k/v 1,844 sets, 516 MB; gate/up and
+    down 30 sets, 521 MB), one CUDA graph per shape and M replayed `repeats`
+    times: us per call as the median and the 95th percentile over the
+    replays; optionally heavy-tailed x (1 % of entries x50) and the int8
+    prologue with each linear's act_scale."""
     out = {}
     dev = st["X"].device
+    import tq2_synth as syn
     for gname, names in SHAPE_GROUPS.items():
         if groups is not None and gname not in groups:
             continue
-        idx = [i for i, (L, n, N, K) in enumerate(st["lin"]) if n in names]
-        N, K = st["lin"][idx[0]][2], st["lin"][idx[0]][3]
+        pool, N, K = shape_pool(torch, st, names)
+        sc = [st["scales"][i] for i, (L, n, N_, K_) in enumerate(st["lin"]) if n in names]
         for M in M_list:
-            import tq2_synth as syn
             x = torch.from_numpy(syn.activations(SEED + 7, M, K, linear=0, heavy=heavy)).to(dev)
-            ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in idx]
-            calls = [(x, st["qs"][i], st["d"][i], y, st["scales"][i] if prologue else 0.0, impl, 0.0)
-                     for i, y in zip(idx, ys)]
+            ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in pool]
+            calls = [(x, q, d, y, sc[j % len(sc)] if prologue else 0.0, impl, 0.0)
+                     for j, ((q, d), y) in enumerate(zip(pool, ys))]
             g = capture(torch, tq2, st, calls, stream)
-            one = time_graph(torch, g, stream, 2, 1)
-            reps = max(3, int(0.3 / max(one * 1e-3, 1e-6)))  # ~0.3 s of replays
-            ms = time_graph(torch, g, stream, reps, 3)
-            nbytes = len(idx) * linear_bytes(M, N, K)
-            out[(gname, M)] = dict(us_per_call=1e3 * ms / len(idx),
-                                   gbs=nbytes / (ms * 1e-3) / 1e9,
-                                   distinct_tensors=len(idx),
-                                   distinct_bytes=nbytes)
+            time_graph(torch, g, stream, 2, 1)
+            per_rep = [1e3 * time_graph(torch, g, stream, 1, 1 if r == 0 else 0) / len(pool)
+                       for r in range(repeats)]
+            per_rep.sort()
+            med = statistics.median(per_rep)
+            p95 = per_rep[min(len(per_rep) - 1, int(round(0.95 * (len(per_rep) - 1))))]
+            nbytes = linear_bytes(M, N, K)
+            out[(gname, M)] = dict(us_per_call=med, us_p95=p95,
+                                   gbs=nbytes / (med * 1e-6) / 1e9,
+                                   distinct_weight_sets=len(pool),
+                                   distinct_bytes=len(pool) * (N * K // 4 + 2 * N * (K // 256)),
+                                   repeats=repeats)
             del g, ys
+        del pool
     return out
 
 
@@ -364,28 +392,80 @@ def affine4_shapes(torch, tq2, stream, groups=(64, 128, 256)):
     return out
 
 
-def cpu_baseline_oracle(budget_s=10.0):
-    """The CPU oracle (fp64, one thread, as it stands) on layer 0 of the stack."""
+def cpu_info():
+    """(cores in this process's affinity mask, CPU model string)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu part")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            model = "unknown"
+    return cores, model
+
+
+def cpu_baseline_oracle(budget_s=10.0, stack_host=None):
+    """The CPU oracle (plain C, fp64, as it stands) timed on the host: one
+    thread on layer 0 of the stack, and every core of the process's affinity
+    mask (rows split in contiguous ranges, one oracle call per range) on the
+    PR1 linear, one q/o linear, layer 0 and -- when the stack's weights are
+    given (copied from the device) -- the whole 224-linear stack once.  The
+    headline value is the whole stack on all cores."""
     import numpy as np
     import oracle
     import tq2_synth as syn
-    done_bytes, t_total, n_lin = 0, 0.0, 0
+    cores, model = cpu_info()
+    layer = []
     for L, name, N, K in stack_linears()[:7]:
         codes = syn.codes(SEED, N, K, linear=L)
         qs, _ = oracle.pack(codes)
-        d = syn.scales(SEED, N, K // 256, linear=L)
-        x = syn.activations(SEED, 1, K, linear=L)
+        layer.append((syn.activations(SEED, 1, K, linear=L), qs, syn.scales(SEED, N, K // 256, linear=L), N, K))
+
+    def run(items, threads):
         t0 = time.perf_counter()
-        oracle.matvec(x, qs, d, K)
-        t_total += time.perf_counter() - t0
-        done_bytes += linear_bytes(1, N, K)
-        n_lin += 1
-        if t_total > budget_s:
-            break
-    return dict(value=done_bytes / t_total / 1e9, unit="GB/s", cores=1, kind="oracle",
-                sample=f"layer 0 of the stack: {n_lin} linears, {done_bytes} algorithmic bytes, "
-                       f"plain C fp64 oracle, 1 thread, {t_total:.2f} s",
-                tok_s=1.0 / (t_total * STACK_BYTES / done_bytes))
+        nbytes = 0
+        for x, qs, d, N, K in items:
+            oracle.matvec_threads(x, qs, d, K, threads=threads)
+            nbytes += linear_bytes(1, N, K)
+        return nbytes, time.perf_counter() - t0
+
+    b1, t1 = run(layer, 1)
+    out = dict(kind="oracle", unit="GB/s", cores=cores, cpu_model=model,
+               one_thread_layer0=dict(gbs=b1 / t1 / 1e9, seconds=t1))
+    # PR1: one 32 x 512 linear, many calls (latency-bound at this size, one thread)
+    c = syn.codes(0, 32, 512)
+    q1, _ = oracle.pack(c)
+    pr1 = [(syn.activations(0, 1, 512), q1, syn.scales(0, 32, 2), 32, 512)] * 2000
+    bp, tp = run(pr1, 1)
+    out["pr1_one_thread"] = dict(us_per_call=1e6 * tp / len(pr1), gbs=bp / tp / 1e9)
+    bq, tq = run(layer[:1], cores)
+    out["qo_all_cores"] = dict(gbs=bq / tq / 1e9, seconds=tq)
+    bl, tl = run(layer, cores)
+    out["layer0_all_cores"] = dict(gbs=bl / tl / 1e9, seconds=tl)
+    if stack_host is not None:
+        bs, ts = run(stack_host, cores)
+        out["stack_all_cores"] = dict(gbs=bs / ts / 1e9, seconds=ts, tok_s=1.0 / ts)
+        out["value"] = bs / ts / 1e9
+        out["sample"] = (f"the whole 224-linear stack once (the device's packed weights copied to the host, "
+                         f"{bs} algorithmic bytes), plain C fp64 oracle, {cores} threads over row ranges "
+                         f"({model}), {ts:.2f} s; also one thread on layer 0, all cores on PR1 / q/o / layer 0")
+    else:
+        out["value"] = bl / tl / 1e9
+        out["sample"] = (f"layer 0 of the stack (7 linears, {bl} algorithmic bytes), plain C fp64 oracle, "
+                         f"{cores} threads over row ranges ({model}), {tl:.2f} s")
+    out["tok_s"] = out["value"] * 1e9 / STACK_BYTES
+    return out
 
 
 def read_profile_traffic():
@@ -506,6 +586,17 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e2e_ms, dev)
     del graphs, st2, bufs
 
+    # per-shape back-to-back calls (>= 4x L2 of distinct weights per shape):
+    # the roofline of each call shape, in the headline line
+    per_shape = {}
+    if rank == 0:
+        peak0, _ = _peak()
+        for (gname, M), v in shape_graphs(torch, tq2, st, stream, M_list=(1,)).items():
+            per_shape[gname] = dict(us_per_call=round(v["us_per_call"], 4), us_p95=round(v["us_p95"], 4),
+                                    gbs=round(v["gbs"], 1), frac=round(v["gbs"] / peak0, 4),
+                                    distinct_weight_sets=v["distinct_weight_sets"],
+                                    distinct_bytes=v["distinct_bytes"], repeats=v["repeats"])
+
     extras = {}
     if not args.quick and rank == 0:
         gp = capture(torch, tq2, st, stack_calls(st, prologue=True), stream)
@@ -529,8 +620,6 @@ def run_gpu(args):
             how="per layer q,k,v as one tq2_matvec_grouped launch on a shared x, o, gate,up as one "
                 "grouped launch on a shared x, down: 4 launches per layer, the same 224 weight sets")
         del gg
-        shapes = shape_graphs(torch, tq2, st, stream, M_list=(1,))
-        extras["shapes_m1"] = {k[0]: v for k, v in shapes.items()}
         simt = shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=2)
         extras["shapes_m1_cuda_core_impl"] = {k[0]: v for k, v in simt.items()}
         pre = shape_graphs(torch, tq2, st, stream, M_list=(1, 2), impl=4)
@@ -586,6 +675,10 @@ def run_gpu(args):
             "peak_source": peak_src,
             "per_launch": f"avg algorithmic bytes {STACK_BYTES / launches_per_step:.0f} / "
                           f"avg launch time {1e3 * ms / launches_per_step:.3f} us",
+            "per_shape": per_shape,
+            "per_shape_how": "M = 1, back-to-back tq2_matvec calls in a CUDA graph over distinct weight "
+                             "sets totalling >= 4x L2; median and 95th percentile of 21 replays; "
+                             "frac = GB/s / peak",
         },
         "e2e": {
             "value": round(job_gbs(world, STACK_BYTES, e2e_ms), 2),
@@ -603,7 +696,13 @@ def run_gpu(args):
     if extras:
         line["extras"] = extras
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_oracle(args.cpu_seconds)
+        stack_host = None
+        if not args.quick:  # the device's stack, copied to the host once
+            xh = st["x_host"].numpy()
+            stack_host = [(xh[st["x_off"][i]:st["x_off"][i] + K].reshape(1, K), st["qs"][i].cpu().numpy(),
+                           st["d"][i].cpu().numpy(), N, K) for i, (L, n, N, K) in enumerate(st["lin"])]
+        line["cpu_baseline"] = cpu_baseline_oracle(args.cpu_seconds, stack_host)
+        del stack_host
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -681,11 +780,12 @@ def run_reference(args):
     qs, _ = oracle.pack(codes)
     d = syn.scales(SEED, N, K // 256, linear=L)
     x = syn.activations(SEED, 1, K, linear=L)
+    cores, model = cpu_info()
     for _ in range(args.warmup):
-        oracle.matvec(x, qs, d, K)
+        oracle.matvec_threads(x, qs, d, K, threads=cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.matvec(x, qs, d, K)
+        oracle.matvec_threads(x, qs, d, K, threads=cores)
     dt = (time.perf_counter() - t0) / args.steps
     nbytes = linear_bytes(1, N, K)
     v = nbytes / dt / 1e9
@@ -697,9 +797,10 @@ def run_reference(args):
         "data": "synthetic (seeded; MiniCPM4-8B shapes)",
         "config": {"workload": WORKLOAD, "step_sample": "the k linear of layer 0 (4096->256)"},
         "tok_s": round(v * 1e9 / STACK_BYTES, 4),
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "one 4096->256 linear of the stack per step, plain C fp64 oracle, "
-                                   "1 thread"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "cpu_model": model,
+                         "sample": f"one 4096->256 linear of the stack per step, plain C fp64 oracle, "
+                                   f"{cores} threads over row ranges"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

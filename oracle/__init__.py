@@ -234,6 +234,57 @@ def matvec(x: np.ndarray, qs: np.ndarray, d: np.ndarray, K: int, act_scale: floa
     return y, t
 
 
+_executor = None
+
+
+def _pool(n):
+    """A persistent pool of at least n host threads (ctypes calls drop the GIL)."""
+    global _executor
+    from concurrent.futures import ThreadPoolExecutor
+    with _lock:
+        if _executor is None or _executor._max_workers < n:
+            if _executor is not None:
+                _executor.shutdown(wait=True)
+            _executor = ThreadPoolExecutor(max_workers=n)
+        return _executor
+
+
+def matvec_threads(x: np.ndarray, qs: np.ndarray, d: np.ndarray, K: int, act_scale: float = 0.0,
+                   threads: int = 1):
+    """The same fp64 matvec (``matvec``) on ``threads`` host threads: the
+    output rows are split into contiguous ranges and each range is one call
+    of the C oracle (ctypes releases the GIL during the call).  The arithmetic
+    per element is unchanged; only the rows run concurrently."""
+    xb = _bits16(x)
+    if xb.ndim == 1:
+        xb = xb.reshape(1, -1)
+    M = xb.shape[0]
+    q = _c(qs, np.uint8)
+    db = _bits16(d)
+    N = q.shape[0]
+    _check_shape(N, K)
+    threads = max(1, min(int(threads), N if N > 0 else 1))
+    lib = _load()
+    bounds = [N * i // threads for i in range(threads + 1)]
+    parts = [None] * threads
+
+    def run(i):
+        r0, r1 = bounds[i], bounds[i + 1]
+        y = np.zeros((M, r1 - r0), dtype=np.float64)
+        t = np.zeros((M, r1 - r0), dtype=np.float64)
+        if r1 > r0:
+            lib.tq2o_matvec_f64(_ptr(xb), M, _ptr(q[r0:r1]), _ptr(db[r0:r1]), r1 - r0, K,
+                                float(np.float32(act_scale)), _ptr(y), _ptr(t))
+        parts[i] = (y, t)
+
+    if threads == 1:
+        run(0)
+    else:
+        list(_pool(threads).map(run, range(threads)))
+    return (np.concatenate([p_[0] for p_ in parts], axis=1),
+            np.concatenate([p_[1] for p_ in parts], axis=1))
+
+
 def matvec_rows(x, qs, d, K, rows, act_scale: float = 0.0):
     """fp64 matvec for the output rows ``rows`` only: (y, tol) [M, len(rows)]."""
     xb = _bits16(x)
