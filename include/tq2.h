@@ -283,6 +283,28 @@ TQ2_API tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_
                                       const uint16_t *z, int64_t N, int64_t K, int64_t G, void *y,
                                       tq2_dtype y_dtype, uint32_t *d_status, tq2_stream_t stream);
 
+/*
+ * tq2_test_matvec_stall -- a test hook, not part of the product (the pages
+ * have no counterpart): tq2_matvec_impl with impl 1 and fp32 y, except that
+ * in every CTA the weight producer skips the copy of pipeline stage
+ * stall_stage, and every bounded device wait gives up after wait_limit_us
+ * microseconds instead of the normal 200 ms.  The consumers' wait for the
+ * skipped stage therefore runs out: the kernel sets TQ2_FLAG_TIMEOUT in
+ * *d_status, waits (bounded) for the copies it did issue, and returns
+ * without storing y.  A test uses it to check that the timeout path reports
+ * the failure and leaves the context usable (the next call is correct).
+ *   stall_stage  >= 0, else TQ2_ERR_ARG; a stage index past a CTA's last
+ *                stage skips nothing in that CTA.
+ *   wait_limit_us  1 .. 200000, else TQ2_ERR_ARG.
+ *   d_status   required (TQ2_ERR_NULL if NULL), 4-byte aligned.
+ *   Other arguments and errors as tq2_matvec_impl with impl 1 (M <= 2,
+ *   TQ2_ERR_ARG for a shape impl 1 cannot plan).  The call takes about two
+ *   wait limits on the device.
+ */
+TQ2_API tq2_status tq2_test_matvec_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                                         int64_t N, int64_t K, float *y, uint32_t *d_status,
+                                         tq2_stream_t stream, int stall_stage, int wait_limit_us);
+
 /* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
  * host thread ("no error" if none): name and description, static storage. */
 TQ2_API const char *tq2_last_cuda_error(void);

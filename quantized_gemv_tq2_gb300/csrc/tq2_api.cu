@@ -77,7 +77,8 @@ tq2_status current_device(int *dev)
 
 tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                          int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
-                         float out_scale, uint32_t *d_status, tq2_stream_t stream, int impl)
+                         float out_scale, uint32_t *d_status, tq2_stream_t stream, int impl,
+                         int stall_stage = -1, unsigned long long wait_limit_ns = 0)
 {
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
@@ -117,6 +118,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     a.out_scale = out_scale;
     a.inv_out = out_scale != 0.0f ? 1.0f / out_scale : 0.0f;
     a.stream = s;
+    a.stall_stage = stall_stage;
+    a.wait_limit_ns = wait_limit_ns;
 
     // impl 0: for M <= 2 and a few output rows per CTA (k/v-sized N) the
     // small-N kernel, else for M <= 2 the class-column mma.sync kernel; for more rows the
@@ -235,6 +238,17 @@ tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_t *qs, c
     (void)workspace;
     (void)workspace_bytes;
     return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, d_status, stream, impl);
+}
+
+tq2_status tq2_test_matvec_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
+                                 int64_t K, float *y, uint32_t *d_status, tq2_stream_t stream, int stall_stage,
+                                 int wait_limit_us)
+{
+    if (stall_stage < 0) return TQ2_ERR_ARG;
+    if (wait_limit_us < 1 || wait_limit_us > 200000) return TQ2_ERR_ARG;
+    if (d_status == nullptr) return TQ2_ERR_NULL;
+    return matvec_common(x, M, qs, d, N, K, y, TQ2_F32, 0.0f, 0.0f, d_status, stream, 1, stall_stage,
+                         (unsigned long long)wait_limit_us * 1000ull);
 }
 
 tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,

@@ -70,16 +70,22 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity; give up after kTimeoutNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Wait for the phase with the given parity; give up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned long long limit_ns)
 {
     if (mbar_test_wait(bar, parity)) return true;  // non-blocking fast path
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+
+// Wait for the phase with the given parity; give up after kTimeoutNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait_for(bar, parity, kTimeoutNs);
 }
 
 // The same wait with cluster-scope acquire: for barriers that CTAs of a

@@ -26,6 +26,12 @@ struct MatvecArgs {
     float out_scale;     // 0: y stored as computed; else requantised to int8 at store
     float inv_out;       // fp32(1/out_scale), correctly rounded on the host
     cudaStream_t stream;
+    // Limit of every bounded device wait of the class-column kernel (0: the
+    // default, 200 ms), and a test hook of that kernel: the weight producer
+    // skips the copy of this stage (-1: none), so that the consumers' wait
+    // for it runs out and the timeout path runs.
+    unsigned long long wait_limit_ns = 0;
+    int stall_stage = -1;
 };
 
 // Tensor-core path (mma.sync on masked code words, TMA bulk staging).

@@ -263,7 +263,7 @@ __device__ __forceinline__ void consume(const Dp4Params &p, uint8_t *smem, uint6
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
+        if (ok && lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));  // none after a wait ran out
         if (++slot == S) {
             slot = 0;
             phase ^= 1;
@@ -360,7 +360,7 @@ __device__ __noinline__ void consume3(const Dp4Params &p, uint8_t *smem, uint64_
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
+        if (ok && lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));  // none after a wait ran out
         if (++slot == S) {
             slot = 0;
             phase ^= 1;

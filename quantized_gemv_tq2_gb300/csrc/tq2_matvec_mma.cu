@@ -149,6 +149,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // full[S], empty[S]
     uint8_t *ring = smem + p.off_ring;
+    const unsigned long long lim = p.a.wait_limit_ns ? p.a.wait_limit_ns : kTimeoutNs;
 
     // Let the next kernel in the stream start its own weight prefetch.
     asm volatile("griddepcontrol.launch_dependents;");
@@ -173,11 +174,15 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
             const int round = s / S;
             // every lane waits (acquire); the decision is made warp-uniform
             if (round > 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[S + slot]), (round - 1) & 1))) {
+                !__all_sync(0xffffffffu, mbar_wait_for(smem_addr(&bars[S + slot]), (round - 1) & 1, lim))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            if (s == p.a.stall_stage) {  // test hook: no copy for this stage
+                issued = s + 1;
+                continue;
+            }
             const int rgb = s / p.n_kc, kc = s % p.n_kc;
             const int rg0 = rgb * p.rg_s;
             const int rows = min(p.rg_s * 16, nrows - rg0 * 16);
@@ -216,9 +221,14 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
             issued = s + 1;
         }
         // No copy may still be writing shared memory when the CTA exits.
+        // (Slots are refilled only after every consumer has waited for and
+        // read the previous stage, so the last copy of a slot is the only one
+        // that can be in flight; a skipped stage had none: its slot's last
+        // copy is the one before it.)
         for (int slot = 0; slot < S && slot < issued; ++slot) {
-            const int last = slot + ((issued - 1 - slot) / S) * S;
-            if (!mbar_wait(smem_addr(&bars[slot]), (last / S) & 1) && lane == 0)
+            int last = slot + ((issued - 1 - slot) / S) * S;
+            if (last == p.a.stall_stage) last -= S;
+            if (last >= 0 && !mbar_wait_for(smem_addr(&bars[slot]), (last / S) & 1, lim) && lane == 0)
                 report_timeout(p, abort_flag);
         }
         return;
@@ -492,7 +502,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         };
         int sl = 0, ph = 0;
         bool ok = n_stages > 0;
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[0]), 0u))) {
+        if (ok && !__all_sync(0xffffffffu, mbar_wait_for(smem_addr(&bars[0]), 0u, lim))) {
             if (lane == 0) report_timeout(p, abort_flag);
             ok = false;
         }
@@ -526,7 +536,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                     }
                 }
                 if (u + 1 == kUpw && s + 1 < n_stages) {
-                    if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[nsl]), (uint32_t)nph))) {
+                    if (__all_sync(0xffffffffu, mbar_wait_for(smem_addr(&bars[nsl]), (uint32_t)nph, lim))) {
                         load_codes(nsl);
                     } else {
                         if (lane == 0) report_timeout(p, abort_flag);
@@ -558,7 +568,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         // every lane waits (acquire); the decision is made warp-uniform
         bool ok = alive;
         if (ok && !__all_sync(0xffffffffu, ready_lane) &&
-            !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[slot]), (uint32_t)phase))) {
+            !__all_sync(0xffffffffu, mbar_wait_for(smem_addr(&bars[slot]), (uint32_t)phase, lim))) {
             if (lane == 0) report_timeout(p, abort_flag);
             ok = alive = false;
         }
@@ -705,8 +715,11 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
             }
             }
         }
+        // a warp that gave up releases no more slots: the producer's next
+        // wait for them runs out too, and no copy is issued into a slot whose
+        // stage was not waited for
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
+        if (ok && lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
         if (++slot == S) {
             slot = 0;
             phase ^= 1;

@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));
+        if (ok && lane == 0) mbar_arrive(smem_addr(&bars[S + slot]));  // none after a wait ran out
         if (++slot == S) {
             slot = 0;
             phase ^= 1;
