@@ -178,19 +178,18 @@ TQ2_API size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K);
  * measurement: impl 0 = automatic (what tq2_matvec runs), 1 = warp-level
  * tensor cores with one accumulator per code class (mma.sync on masked code
  * words, TMA-staged weights), 2 = CUDA cores (fp32 FMA per code),
- * 3 = 5th-generation tensor cores (tcgen05 MMA with the unpacked codes in
- * tensor memory), 4 = warp-level tensor cores with x pre-scaled per code
- * class (one accumulator whose 8 columns are 8 activation rows), 5 = CUDA-core
- * 8-bit dot products (dp4a) on x split per 256-block into one to three 8-bit
- * pieces, 6 = the tcgen05 GEMM of tq2_gemm (5th-generation tensor cores, an
- * MMA of 128 weight rows x 16 activation rows), 7 = CUDA cores for a few
- * output rows per CTA (k/v-sized N: codes and scales in registers before the
- * wait on the previous kernel, one reduction).  Impls 1, 3 and 7 take M <= 2
- * (impl 3 also needs K % 512 == 0 and K <= 16384; impl 7 K <= 16384 and at
- * most 4 rows per CTA, one CTA per SM), impl 4 takes M <= 16, impl 5 takes
- * M = 1 and K <= 16384;
- * outside their range they return TQ2_ERR_ARG.  Same contract as tq2_matvec
- * otherwise.
+ * 4 = warp-level
+ * tensor cores with x pre-scaled per code class (one accumulator whose 8
+ * columns are 8 activation rows), 6 = the tcgen05 GEMM of tq2_gemm
+ * (5th-generation tensor cores, an MMA of 128 weight rows x 16 activation
+ * rows), 7 = CUDA cores for a few output rows per CTA (k/v-sized N: codes and
+ * scales in registers before the wait on the previous kernel, one
+ * reduction).  Impls 1 and 7 take M <= 2 (impl 7 also K <= 16384 and at most
+ * 4 rows per CTA, one CTA per SM), impl 4 takes M <= 16;
+ * outside their range they return TQ2_ERR_ARG.  Numbers 3 (a tcgen05
+ * matvec) and 5 (a dp4a matvec) are retired: both were slower than impl 1 on
+ * every shape, and they now return TQ2_ERR_ARG (the numbers are not reused).
+ * Same contract as tq2_matvec otherwise.
  */
 TQ2_API tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                            int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,

@@ -86,9 +86,8 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
     if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
     if (!(out_scale >= 0.0f) || !std::isfinite(out_scale)) return TQ2_ERR_ARG;
-    if (impl < 0 || impl > 7) return TQ2_ERR_ARG;
-    if ((impl == 1 || impl == 3 || impl == 7) && M > 2) return TQ2_ERR_ARG;
-    if (impl == 5 && M > 1) return TQ2_ERR_ARG;
+    if (impl < 0 || impl > 7 || impl == 3 || impl == 5) return TQ2_ERR_ARG;  // 3, 5: retired
+    if ((impl == 1 || impl == 7) && M > 2) return TQ2_ERR_ARG;
     if (M == 0 || N == 0) return TQ2_OK;
     if (y == nullptr) return TQ2_ERR_NULL;
     if (K > 0 && (x == nullptr || qs == nullptr || d == nullptr)) return TQ2_ERR_NULL;
@@ -135,8 +134,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     //   down 4096x16384:    M = 7: 23.9 / 25.5, M = 8: 25.5 / 25.5; with the
     //                       prologue M = 8: 30.9 / 32.9, M = 10: 41.6 / 33.0
     // (the GEMM applies the prologue per x stage, the pre-scaled kernel once
-    // per call, so the prologue moves the crossover up).  The tcgen05 matvec
-    // (impl 3) is correct but slower, so it runs only on request.
+    // per call, so the prologue moves the crossover up).
     int which = impl;
     if (impl == 0) {
         const bool gemm_wins = (act_scale != 0.0f)
@@ -149,21 +147,15 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
         else which = 2;
     } else if (impl == 1 && !tq2::mma_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
-    } else if (impl == 3 && !tq2::tc05_matvec_supported(a.M, N, K, dev)) {
-        return TQ2_ERR_ARG;
     } else if (impl == 4 && !tq2::ps_matvec_supported(a.M, N, K, dev)) {
-        return TQ2_ERR_ARG;
-    } else if (impl == 5 && !tq2::dp4_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
     } else if (impl == 6 && !tq2::gemm_tc05_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
     } else if (impl == 7 && !tq2::smalln_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
     }
-    cudaError_t e = (which == 3)   ? tq2::launch_matvec_tc05(a, dev)
-                    : (which == 1) ? tq2::launch_matvec_mma(a, dev)
+    cudaError_t e = (which == 1)   ? tq2::launch_matvec_mma(a, dev)
                     : (which == 4) ? tq2::launch_matvec_ps(a, dev)
-                    : (which == 5) ? tq2::launch_matvec_dp4(a, dev)
                     : (which == 6) ? tq2::launch_gemm_tc05(a, dev)
                     : (which == 7) ? tq2::launch_matvec_smalln(a, dev)
                                    : tq2::launch_matvec_simt(a, dev);

@@ -47,11 +47,6 @@ bool mma_group_supported(int M, int n, const int64_t *N, int64_t K, int device);
 cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
                                     void *const *y, const int64_t *N, int device);
 
-// 5th-generation tensor-core path (tcgen05 MMA, A in tensor memory), M <= 2,
-// K a multiple of 512 with K / S <= 4096.  Returns false when unsupported.
-bool tc05_matvec_supported(int M, int64_t N, int64_t K, int device);
-cudaError_t launch_matvec_tc05(const MatvecArgs &a, int device);
-
 // Ternary GEMM for many activation rows (any M): tcgen05 MMAs over weights
 // expanded to (q - 1) * d in tensor memory, x tiles by TMA (fake-quantised in
 // shared memory when act_scale != 0).
@@ -63,11 +58,6 @@ cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device);
 // when the shape does not fit.
 bool ps_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_ps(const MatvecArgs &a, int device);
-
-// Integer-dot path (dp4a on x split into 8-bit pieces per 256-block), M = 1,
-// K <= 16384.  Returns false when the shape does not fit.
-bool dp4_matvec_supported(int M, int64_t N, int64_t K, int device);
-cudaError_t launch_matvec_dp4(const MatvecArgs &a, int device);
 
 // Affine-int4 matvec (zero point factored out per group of G codes): codes
 // [N][K/2] (two per byte, low nibble first), s and z fp16 [N][K/G], G in

@@ -60,10 +60,10 @@ def test_matvec_rejects_bad_dtype_and_args(L):
     assert mv(L, s=float("inf")) == ARG
     assert mv(L, impl=8) == ARG
     assert mv(L, impl=7, M=3) == ARG  # the small-N kernel takes M <= 2
-    assert mv(L, impl=5, M=2) == ARG  # the dp4a kernel takes M = 1
+    assert mv(L, impl=5) == ARG  # retired numbers
+    assert mv(L, impl=3) == ARG
     assert mv(L, impl=-1) == ARG
     assert mv(L, impl=1, M=3) == ARG  # the class-column tensor-core kernels take M <= 2
-    assert mv(L, impl=3, M=3) == ARG
     assert mv(L, impl=4, M=17) == SHAPE  # the pre-scaled kernel takes M <= 16, as the API
 
 

@@ -11,7 +11,7 @@ from gpu_util import Case, assert_within_tolerance, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = {"auto": 0, "mma": 1, "simt": 2, "tc05": 3, "ps": 4, "dp4": 5, "gemm": 6}
+IMPLS = {"auto": 0, "mma": 1, "simt": 2, "ps": 4, "gemm": 6, "smalln": 7}
 
 
 @pytest.fixture(scope="module")

@@ -11,7 +11,7 @@ from gpu_util import Case, assert_within_tolerance, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = {"auto": 0, "mma": 1, "simt": 2, "tc05": 3, "ps": 4, "dp4": 5, "gemm": 6, "smalln": 7}
+IMPLS = {"auto": 0, "mma": 1, "simt": 2, "ps": 4, "gemm": 6, "smalln": 7}
 
 
 @pytest.fixture(scope="module")
@@ -31,7 +31,7 @@ def _run(T, case, impl, y_dtype=0, rows=None):
     try:
         y = tq2.matvec(x, qs, d, y_dtype=y_dtype, act_scale=case.s, status=st, impl=impl)
     except tq2.TQ2Error as e:
-        if e.status == 5 and impl in (1, 3, 4, 5, 6, 7):
+        if e.status == 5 and impl in (1, 4, 6, 7):
             return None
         raise
     T.cuda.synchronize()
@@ -41,9 +41,7 @@ def _run(T, case, impl, y_dtype=0, rows=None):
 
 
 def _impls_for(M):
-    if M == 1:
-        return ["auto", "tc05", "mma", "ps", "dp4", "gemm", "smalln", "simt"]
-    return ["auto", "tc05", "mma", "ps", "gemm", "smalln", "simt"] if M <= 2 else ["auto", "ps", "gemm", "simt"]
+    return ["auto", "mma", "ps", "gemm", "smalln", "simt"] if M <= 2 else ["auto", "ps", "gemm", "simt"]
 
 
 # ---------------------------------------------------------------- small shapes, full compare
@@ -106,7 +104,7 @@ def test_matvec_pr1_exhaustive(T):
         codes = oracle.unpack(qs, K).astype(np.float64)
         want = (np.repeat(d.astype(np.float64), 256, axis=1) * (codes - 1)).T  # [K, N]
         qd, dd = dev(qs), dev(d)
-        for impl, mstep in (("mma", 2), ("tc05", 2), ("ps", 16), ("ps", 4), ("dp4", 1), ("simt", 16), ("auto", 1)):
+        for impl, mstep in (("mma", 2), ("ps", 16), ("ps", 4), ("smalln", 1), ("simt", 16), ("auto", 1)):
             for k0 in range(0, K, mstep):
                 x = np.zeros((mstep, K), dtype=np.float16)
                 for i in range(mstep):
@@ -119,12 +117,9 @@ def test_matvec_pr1_exhaustive(T):
         for seed in range(4):
             x = syn.activations(seed, 2, K)
             y_ref, tol = oracle.matvec(x, qs, d, K)
-            for impl in ("mma", "tc05", "ps", "simt"):
+            for impl in ("mma", "ps", "smalln", "simt"):
                 y = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl])).astype(np.float64)
                 assert_within_tolerance(y, y_ref, tol, f"exhaustive t={t} seed={seed} {impl}")
-            for i in range(2):
-                y = host(tq2.matvec(dev(x[i:i + 1]), qd, dd, impl=IMPLS["dp4"])).astype(np.float64)
-                assert_within_tolerance(y, y_ref[i:i + 1], tol[i:i + 1], f"exhaustive t={t} seed={seed} dp4 row {i}")
 
 
 def test_matvec_one_hot_large_k(T):
@@ -136,7 +131,7 @@ def test_matvec_one_hot_large_k(T):
         x = np.zeros((1, K), dtype=np.float16)
         x[0, k] = 1.0
         want = case.d[:, k // 256].astype(np.float64) * (case.codes[:, k].astype(np.float64) - 1)
-        for impl in ("mma", "tc05", "ps", "dp4", "smalln", "simt"):
+        for impl in ("mma", "ps", "smalln", "simt"):
             got = host(tq2.matvec(dev(x), qd, dd, impl=IMPLS[impl]))[0].astype(np.float64)
             assert np.array_equal(got, want), (impl, k)
 
@@ -152,40 +147,9 @@ def test_matvec_extreme_values(T):
     case.d[1, :] = np.float16(60000.0)
     case.d[2, 1] = 0
     y_ref, tol = case.reference()
-    for name in ("mma", "tc05", "ps", "simt"):
+    for name in ("mma", "ps", "smalln", "simt"):
         y = _run(T, case, IMPLS[name])
         assert_within_tolerance(y, y_ref, tol, name)
-
-
-@pytest.mark.parametrize("kind", ["normal", "outlier", "prologue", "zeros", "tiny", "huge", "mixed_blocks"])
-@pytest.mark.parametrize("N,K", [(40, 1024), (33, 4352), (24, 16384)])
-def test_matvec_dp4_piece_paths(T, kind, N, K):
-    """The dp4a kernel's x decompositions: one int8 piece (prologue), two
-    pieces (blocks whose rounding bound fits), three pieces (an outlier
-    anywhere), all-zero, subnormal and near-overflow fp16 x; plus run-to-run
-    determinism."""
-    import quantized_gemv_tq2_gb300 as tq2
-    case = Case(seed=K + N, M=1, N=N, K=K, heavy=(kind == "prologue"), prologue=(kind == "prologue"))
-    if kind == "outlier":
-        case.x[0, 7] = np.float16(3000.0)
-    elif kind == "zeros":
-        case.x[:] = 0
-    elif kind == "tiny":
-        case.x[:] = (case.x.astype(np.float32) * np.float32(2.0 ** -20)).astype(np.float16)
-    elif kind == "huge":
-        case.x[:] = (case.x.astype(np.float32) * np.float32(20000.0)).clip(-65504, 65504).astype(np.float16)
-    elif kind == "mixed_blocks":
-        case.x[0, :256] = (case.x[0, :256].astype(np.float32) * np.float32(2.0 ** -18)).astype(np.float16)
-        case.x[0, 256:512] = 0
-    y_ref, tol = case.reference()
-    first = None
-    for yd in ((0,) if kind == "huge" else (0, 1)):  # huge: |y| beyond the fp16 range
-        y = _run(T, case, IMPLS["dp4"], y_dtype=yd)
-        assert_within_tolerance(y, y_ref, tol, f"dp4 {kind} yd={yd}")
-        if yd == 0:
-            first = y
-    for _ in range(5):
-        assert np.array_equal(_run(T, case, IMPLS["dp4"]), first)
 
 
 def test_matvec_empty_shapes(T):
@@ -207,7 +171,7 @@ def test_matvec_is_deterministic(T):
     import quantized_gemv_tq2_gb300 as tq2
     case = Case(seed=21, M=2, N=1000, K=4096)
     x, qs, d = case.device()
-    for impl in (1, 2, 3, 4):
+    for impl in (1, 2, 4, 6):
         first = host(tq2.matvec(x, qs, d, impl=impl))
         for _ in range(20):
             assert np.array_equal(host(tq2.matvec(x, qs, d, impl=impl)), first)
@@ -219,8 +183,12 @@ def test_matvec_is_deterministic(T):
 def test_matvec_qo_and_kv_full(T, seed, N):
     case = Case(seed=seed, M=1, N=N, K=4096)
     y_ref, tol = case.reference()
-    for name in ("auto", "tc05", "mma", "ps", "dp4", "simt"):
-        assert_within_tolerance(_run(T, case, IMPLS[name]), y_ref, tol, f"{name} N={N}")
+    for name in ("auto", "mma", "ps", "gemm", "smalln", "simt"):
+        y = _run(T, case, IMPLS[name])
+        if y is None:  # the small-N kernel takes k/v-sized N only
+            assert name == "smalln" and N > 4 * 152
+            continue
+        assert_within_tolerance(y, y_ref, tol, f"{name} N={N}")
 
 
 @pytest.mark.parametrize("N,K", [(16384, 4096), (4096, 16384)])
