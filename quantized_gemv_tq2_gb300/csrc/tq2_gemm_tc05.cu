@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     constexpr uint32_t kBStageBytes = 2u * kBoxBytes;       // kKs = 8 k-steps
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t N = p.a.N, K = p.a.K;
+    const int64_t N = p.a.N;
     const int M = p.a.M;
     const int S = p.S;
     const int rank = (int)(blockIdx.x % (unsigned)S), tile = (int)(blockIdx.x / (unsigned)S);
@@ -268,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 umma_commit(sempty0 + 8u * r);  // A slot and x buffer free once these MMAs completed
             }
             umma_commit(dfull);  // every MMA issued above has completed
+            // tensor memory is freed only once those MMAs are done, even if
+            // the epilogue's own wait for them ran out
+            if (!mbar_wait(dfull, 0u)) report_timeout(p, abort_flag);
         }
         __syncwarp();
         named_barrier(2, kTmemThreads);  // (b) the epilogue has read D
@@ -328,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> MMA reads
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bconv0 + 8u * (uint32_t)r);
+                if (alive && lane == 0) mbar_arrive(bconv0 + 8u * (uint32_t)r);
             }
             const int ws = g >> 1;           // code stage (2 groups)
             const int u0 = (g & 1) * 2;      // first 16-byte unit of the group in the row
             const int slot = ws % SW;
             if (ws != cur_w) {
-                if (cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
+                if (alive && cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
                 cur_w = ws;
                 if (alive && !__all_sync(0xffffffffu, mbar_wait(wfull0 + 8u * slot, (uint32_t)((ws / SW) & 1)))) {
                     if (lane == 0) report_timeout(p, abort_flag);
@@ -367,10 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
             }
+            // a warp whose wait ran out releases nothing it did not wait
+            // for: no slot is refilled while its last copy may be in flight,
+            // and no barrier runs a phase ahead of its waiters
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull0 + 8u * a);
+            if (alive && lane == 0) mbar_arrive(afull0 + 8u * a);
         }
-        if (cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
+        if (alive && cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
     }
 
     // epilogue: D column c is activation row m0 + c; this warp takes half of them
@@ -424,6 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     named_barrier(3, kUnpackWarps * 32);  // every partial of this CTA written
     const uint32_t part_s = smem_addr(part);
     if (uw == 0 && lane < S && lane != rank) {  // tell every peer: my partial is ready
+        // A CTA that gave up (a bounded wait ran out) first sets every peer's
+        // abort flag, so that no peer reads its partial: its shared memory
+        // must not be touched once it may exit (ordered before the arrival
+        // by the release fence).
+        if (*abort_flag != 0) {
+            uint32_t rflag;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rflag) : "r"(smem_addr(&abort_sh)), "r"(lane));
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(rflag), "r"(1u) : "memory");
+        }
         uint32_t remote;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(pready), "r"(lane));
         asm volatile("fence.acq_rel.cluster;\n\tmbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
@@ -431,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     }
     bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(pready, 0u));
     if (!ok && lane == 0) report_timeout(p, abort_flag);
+    // a peer that gave up has set this CTA's flag before its arrival: no remote
+    // reads then (the result is invalid and TQ2_FLAG_TIMEOUT reported anyway)
+    ok = ok && !__any_sync(0xffffffffu, *abort_flag != 0);
     // this CTA's columns [rank BN/S, (rank+1) BN/S), summed over the S partials in rank order
     const int cols = BN / S, c_lo = rank * cols;
     const int tid_u = uw * 32 + lane;
