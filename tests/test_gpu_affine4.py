@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import tq2_synth as syn
-from gpu_util import assert_within_tolerance, dev, host, sample_rows
+from gpu_util import GuardedOutput, assert_within_tolerance, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -32,10 +32,12 @@ def _case(seed, M, N, K, G, heavy=False):
 def _run(T, x, qs, s, z, G, y_dtype=0):
     import quantized_gemv_tq2_gb300 as tq2
     st = T.zeros(1, dtype=T.int32, device="cuda")
-    y = tq2.affine4_matvec(dev(x), dev(qs), dev(s), dev(z), G, y_dtype=y_dtype, status=st)
+    out = GuardedOutput(x.shape[0], qs.shape[0], y_dtype)  # canaries on both sides of y
+    tq2.affine4_matvec(dev(x), dev(qs), dev(s), dev(z), G, y=out.y, status=st)
     T.cuda.synchronize()
     assert int(st.item()) == 0
-    return host(y)
+    out.check(f"affine4 M={x.shape[0]} N={qs.shape[0]} K={x.shape[1]} G={G}")
+    return host(out.y)
 
 
 @pytest.mark.parametrize("M,N,K,G", [

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import tq2_synth as syn
-from gpu_util import Case, assert_within_tolerance, dev, host, sample_rows
+from gpu_util import Case, GuardedOutput, assert_within_tolerance, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +27,12 @@ def _gemm(T, case, impl, y_dtype=0, out_scale=0.0):
     import quantized_gemv_tq2_gb300 as tq2
     x, qs, d = case.device()
     st = T.zeros(1, dtype=T.int32, device="cuda")
-    y = tq2.gemm(x, qs, d, y_dtype=y_dtype, act_scale=case.s, out_scale=out_scale, status=st, impl=impl)
+    out = GuardedOutput(case.M, case.N, y_dtype)  # canaries on both sides of y
+    tq2.gemm(x, qs, d, y=out.y, act_scale=case.s, out_scale=out_scale, status=st, impl=impl)
     T.cuda.synchronize()
     assert int(st.item()) == 0
-    return host(y).astype(np.float64)
+    out.check(f"gemm impl={impl} M={case.M} N={case.N} K={case.K}")
+    return host(out.y).astype(np.float64)
 
 
 @pytest.mark.parametrize("M,N,K", [

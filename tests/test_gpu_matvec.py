@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import tq2_synth as syn
-from gpu_util import Case, assert_within_tolerance, dev, host, sample_rows
+from gpu_util import Case, GuardedOutput, assert_within_tolerance, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -28,16 +28,18 @@ def _run(T, case, impl, y_dtype=0, rows=None):
     import quantized_gemv_tq2_gb300 as tq2
     x, qs, d = case.device()
     st = T.zeros(1, dtype=T.int32, device="cuda")
+    out = GuardedOutput(case.M, case.N, y_dtype)  # canaries on both sides of y
     try:
-        y = tq2.matvec(x, qs, d, y_dtype=y_dtype, act_scale=case.s, status=st, impl=impl)
+        tq2.matvec(x, qs, d, y=out.y, act_scale=case.s, status=st, impl=impl)
     except tq2.TQ2Error as e:
         if e.status == 5 and impl in (1, 4, 6, 7):
             return None
         raise
     T.cuda.synchronize()
     assert int(st.item()) == 0
-    out = host(y).astype(np.float64)
-    return out if rows is None else out[:, rows]
+    out.check(f"impl={impl} M={case.M} N={case.N} K={case.K}")
+    y = host(out.y).astype(np.float64)
+    return y if rows is None else y[:, rows]
 
 
 def _impls_for(M):

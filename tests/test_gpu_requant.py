@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import Case, host, sample_rows
+from gpu_util import Case, GuardedOutput, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -36,16 +36,17 @@ def _run(T, case, impl, out_scale, y_dtype=0):
     import quantized_gemv_tq2_gb300 as tq2
     x, qs, d = case.device()
     st = T.zeros(1, dtype=T.int32, device="cuda")
+    out = GuardedOutput(case.M, case.N, y_dtype)  # canaries on both sides of y
     try:
-        y = tq2.matvec(x, qs, d, y_dtype=y_dtype, act_scale=case.s, status=st, impl=impl,
-                       out_scale=out_scale)
+        tq2.matvec(x, qs, d, y=out.y, act_scale=case.s, status=st, impl=impl, out_scale=out_scale)
     except tq2.TQ2Error as e:
         if e.status == 5 and impl in (1, 4, 6, 7):
             return None  # that kernel does not take this shape
         raise
     T.cuda.synchronize()
     assert int(st.item()) == 0
-    return host(y)
+    out.check(f"requant impl={impl} M={case.M} N={case.N} K={case.K}")
+    return host(out.y)
 
 
 def check_requant(y_gpu, y_ref, tol_sum, s_o, y_dtype, what):
