@@ -158,17 +158,37 @@ TQ2_API tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, c
  *   y_dtype, act_scale, d_status, stream  as tq2_matvec (one act_scale for
  *              the shared x).
  *
- * Results equal n_mats tq2_matvec calls with the same x; when M <= 2 and
- * K <= 4096 they run as ONE kernel launch (the CTAs split between the
- * matrices in proportion to their rows; x staged and the wait on the previous
- * kernel paid once), otherwise as consecutive calls on the stream.  Errors:
- * as tq2_matvec for every matrix (checked before anything is enqueued);
- * TQ2_ERR_ARG for n_mats out of range; TQ2_ERR_NULL for a NULL array.
+ * Results equal n_mats tq2_matvec calls with the same x.  They run as ONE
+ * kernel launch (the CTAs split between the matrices in proportion to their
+ * rows; x staged and the wait on the previous kernel paid once) when M <= 2
+ * (the class-column kernel, any K), or when 3 <= M <= 8 and each matrix alone
+ * would run the pre-scaled kernel (not the GEMM; any K); otherwise as
+ * consecutive calls on the stream.  Errors: as tq2_matvec for every matrix (checked
+ * before anything is enqueued); TQ2_ERR_ARG for n_mats out of range;
+ * TQ2_ERR_NULL for a NULL array.
  */
 TQ2_API tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats,
                                       const uint8_t *const *qs, const uint16_t *const *d,
                                       const int64_t *N, void *const *y, tq2_dtype y_dtype,
                                       float act_scale, uint32_t *d_status, tq2_stream_t stream);
+
+/*
+ * tq2_matvec_grouped_requant -- tq2_matvec_grouped with the static int8
+ * requantisation of each matrix's result at store, with that matrix's own
+ * output scale ("gemma4 wNa8o8 requires int8 activations" page, the recipe:
+ * one input quantisation shared by q/k/v and by gate/up, each linear's
+ * output requantised with its own output_activation_scale).
+ *   out_scale  HOST array of n_mats scales (read during the call, not kept);
+ *              each >= 0 and finite, else TQ2_ERR_ARG; 0 stores that
+ *              matrix's y unchanged.  NULL: TQ2_ERR_NULL.
+ * y_j is what tq2_matvec_requant(..., out_scale[j], ...) stores; everything
+ * else as tq2_matvec_grouped.
+ */
+TQ2_API tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, int n_mats,
+                                              const uint8_t *const *qs, const uint16_t *const *d,
+                                              const int64_t *N, void *const *y, tq2_dtype y_dtype,
+                                              float act_scale, const float *out_scale, uint32_t *d_status,
+                                              tq2_stream_t stream);
 
 /* Bytes of workspace tq2_matvec needs for this shape (0 for every shape today). */
 TQ2_API size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -23,13 +23,13 @@ __all__ = [
     "matvec_workspace_size",
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT",
-    "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_TC05", "IMPL_PS", "IMPL_DP4", "IMPL_GEMM",
-    "IMPL_SMALLN",
+    "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_PS", "IMPL_GEMM", "IMPL_SMALLN",
 ]
 
 F32, F16 = 0, 1
 FLAG_BAD_CODE, FLAG_NONFINITE, FLAG_INEXACT, FLAG_TIMEOUT = 1, 2, 4, 8
-IMPL_AUTO, IMPL_MMA, IMPL_SIMT, IMPL_TC05, IMPL_PS, IMPL_DP4, IMPL_GEMM, IMPL_SMALLN = 0, 1, 2, 3, 4, 5, 6, 7
+# (3 and 5 are retired kernel numbers: TQ2_ERR_ARG)
+IMPL_AUTO, IMPL_MMA, IMPL_SIMT, IMPL_PS, IMPL_GEMM, IMPL_SMALLN = 0, 1, 2, 4, 6, 7
 HEADER = os.path.join(os.path.dirname(_build.PKG), "include", "tq2.h")
 
 _lock = threading.Lock()
@@ -66,6 +66,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_matvec_impl.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P, I32]
         L.tq2_matvec_requant.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
         L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P]
+        L.tq2_matvec_grouped_requant.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P, P]
         L.tq2_gemm.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, P, I32]
         L.tq2_affine4_matvec.argtypes = [P, I64, P, P, P, I64, I64, I64, P, I32, P, P]
         L.tq2_test_matvec_stall.argtypes = [P, I64, P, P, I64, I64, P, P, P, I32, I32]
@@ -77,7 +78,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_last_cuda_error.argtypes = []
         L.tq2_last_cuda_error.restype = ctypes.c_char_p
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
-                   "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_gemm", "tq2_affine4_matvec",
+                   "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_matvec_grouped_requant", "tq2_gemm",
+                   "tq2_affine4_matvec",
                    "tq2_test_matvec_stall", "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
@@ -216,9 +218,11 @@ def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, statu
 
 
 def matvec_grouped(x, qs_list, d_list, y_list=None, y_dtype=None, act_scale: float = 0.0,
-                   status=None, stream=None):
+                   status=None, stream=None, out_scales=None):
     """[y_j] = ternary matvecs of one shared x [M,K] with several packed
-    matrices (tq2_matvec_grouped): one launch when the library can group them."""
+    matrices (tq2_matvec_grouped): one launch when the library can group them.
+    out_scales (one float per matrix) requantises each y_j to int8 at store
+    with its own scale (tq2_matvec_grouped_requant)."""
     torch = _torch()
     if x.dim() == 1:
         x = x.view(1, -1)
@@ -239,11 +243,18 @@ def matvec_grouped(x, qs_list, d_list, y_list=None, y_dtype=None, act_scale: flo
     da = Pn(*[_ptr(d).value for d in d_list])
     ya = Pn(*[_ptr(y).value for y in y_list])
     na = (ctypes.c_int64 * n)(*[q.shape[0] for q in qs_list])
-    st = load().tq2_matvec_grouped(_ptr(x), M, K, n, ctypes.cast(qa, ctypes.c_void_p),
-                                   ctypes.cast(da, ctypes.c_void_p), ctypes.cast(na, ctypes.c_void_p),
-                                   ctypes.cast(ya, ctypes.c_void_p), ycode, float(act_scale),
-                                   _ptr(status), _stream_ptr(stream))
-    _check(st, "tq2_matvec_grouped")
+    common = (_ptr(x), M, K, n, ctypes.cast(qa, ctypes.c_void_p), ctypes.cast(da, ctypes.c_void_p),
+              ctypes.cast(na, ctypes.c_void_p), ctypes.cast(ya, ctypes.c_void_p), ycode, float(act_scale))
+    if out_scales is None:
+        st = load().tq2_matvec_grouped(*common, _ptr(status), _stream_ptr(stream))
+        _check(st, "tq2_matvec_grouped")
+    else:
+        if len(out_scales) != n:
+            raise ValueError("out_scales needs one scale per matrix")
+        sa = (ctypes.c_float * n)(*[float(v) for v in out_scales])
+        st = load().tq2_matvec_grouped_requant(*common, ctypes.cast(sa, ctypes.c_void_p), _ptr(status),
+                                               _stream_ptr(stream))
+        _check(st, "tq2_matvec_grouped_requant")
     return y_list
 
 

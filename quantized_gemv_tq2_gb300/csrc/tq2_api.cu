@@ -75,6 +75,13 @@ tq2_status current_device(int *dev)
     return from_cuda(cudaGetDevice(dev));
 }
 
+// The tcgen05 GEMM beats the pre-scaled kernel (crossovers measured, see
+// the dispatch in matvec_common; the same with and without the prologue).
+bool gemm_preferred(int M, int64_t N, int64_t K)
+{
+    return (M >= 9 && (K >= 8192 || N <= 512)) || (M >= 12 && N < 8192);
+}
+
 tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                          int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
                          float out_scale, uint32_t *d_status, tq2_stream_t stream, int impl,
@@ -126,20 +133,16 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     // GEMM (whose time is flat up to 16 rows: an MMA of 128 weight rows x up
     // to 64 activation rows costs the same) is faster; CUDA cores as the last
     // resort.  The crossovers, measured on GB300 (us per call, back to back
-    // over distinct weights, pre-scaled against GEMM):
-    //   q/o 4096x4096:      M = 8: 6.9 / 9.5, M = 10: 9.8 / 9.5; with the
-    //                       int8 prologue M = 10: 11.2 / 11.2, M = 12: 12.5 / 11.2
-    //   gate/up 16384x4096: M = 12: 19.5 / 22.9, M = 16: 23.3 / 22.9; with
-    //                       the prologue M = 16: 25.6 / 29.7
-    //   down 4096x16384:    M = 7: 23.9 / 25.5, M = 8: 25.5 / 25.5; with the
-    //                       prologue M = 8: 30.9 / 32.9, M = 10: 41.6 / 33.0
-    // (the GEMM applies the prologue per x stage, the pre-scaled kernel once
-    // per call, so the prologue moves the crossover up).
+    // over distinct weights, pre-scaled against GEMM, without / with the int8
+    // prologue):
+    //   q/o 4096x4096:      M = 10: 9.0 / 9.7, 10.5 / 11.4; M = 12: 10.1 / 9.7, 11.8 / 11.4
+    //   k/v 256x4096:       M = 8: 5.2 / 6.5, 6.5 / 7.1; M = 10: 7.5 / 6.5, 9.0 / 7.2
+    //   gate/up 16384x4096: M = 16: 20.7 / 23.4, 23.1 / 30.8 (the pre-scaled kernel throughout)
+    //   down 4096x16384:    M = 8: 26.0 / 26.1, 31.2 / 34.1; M = 10: 35.7 / 26.1, 41.8 / 34.1
+    // (M = 9 starts the pre-scaled kernel's second n-tile of 8 rows).
     int which = impl;
     if (impl == 0) {
-        const bool gemm_wins = (act_scale != 0.0f)
-                                   ? (a.M >= 9 && K >= 8192) || (a.M >= 8 && N <= 512) || (a.M >= 11 && N < 8192)
-                                   : (a.M >= 8 && (K >= 8192 || N <= 512)) || (a.M >= 10 && N < 8192) || a.M >= 16;
+        const bool gemm_wins = gemm_preferred(a.M, N, K);
         if (a.M <= 2 && tq2::smalln_matvec_preferred(a.M, N, K, dev)) which = 7;
         else if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
         else if (gemm_wins && tq2::gemm_tc05_supported(a.M, N, K, dev)) which = 6;
@@ -243,9 +246,15 @@ tq2_status tq2_test_matvec_stall(const uint16_t *x, int64_t M, const uint8_t *qs
                          (unsigned long long)wait_limit_us * 1000ull);
 }
 
-tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
-                              const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
-                              float act_scale, uint32_t *d_status, tq2_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+// tq2_matvec_grouped and tq2_matvec_grouped_requant (out_scale: host array of
+// n_mats scales, or nullptr for none).
+tq2_status matvec_grouped_common(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
+                                 const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
+                                 float act_scale, const float *out_scale, uint32_t *d_status, tq2_stream_t stream)
 {
     if (n_mats < 1 || n_mats > TQ2_MAX_GROUP) return TQ2_ERR_ARG;
     if (qs == nullptr || d == nullptr || N == nullptr || y == nullptr) return TQ2_ERR_NULL;
@@ -257,6 +266,7 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
         if (M < 0 || M > 16) return TQ2_ERR_SHAPE;
         if (y_dtype != TQ2_F32 && y_dtype != TQ2_F16) return TQ2_ERR_DTYPE;
         if (!(act_scale >= 0.0f) || !std::isfinite(act_scale)) return TQ2_ERR_ARG;
+        if (out_scale && (!(out_scale[j] >= 0.0f) || !std::isfinite(out_scale[j]))) return TQ2_ERR_ARG;
         if (M == 0 || N[j] == 0) continue;
         if (y[j] == nullptr) return TQ2_ERR_NULL;
         if (K > 0 && (x == nullptr || qs[j] == nullptr || d[j] == nullptr)) return TQ2_ERR_NULL;
@@ -271,6 +281,7 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
     const uint16_t *gd[TQ2_MAX_GROUP];
     void *gy[TQ2_MAX_GROUP];
     int64_t gn[TQ2_MAX_GROUP];
+    float gs[TQ2_MAX_GROUP], gi[TQ2_MAX_GROUP];
     int n = 0;
     for (int j = 0; j < n_mats; ++j) {
         if (M == 0 || N[j] == 0) continue;
@@ -278,13 +289,24 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
         gd[n] = d[j];
         gy[n] = y[j];
         gn[n] = N[j];
+        gs[n] = out_scale ? out_scale[j] : 0.0f;
+        gi[n] = gs[n] != 0.0f ? 1.0f / gs[n] : 0.0f;  // IEEE-correct division
         ++n;
     }
     int dev = 0;
     tq2_status st = TQ2_OK;
     if (K > 0 && n > 1) {
         if ((st = current_device(&dev)) != TQ2_OK) return st;
-        if (tq2::mma_group_supported((int)M, n, gn, K, dev)) {
+        // the pre-scaled kernel where a single call would run it, up to 8
+        // rows (one n-tile): measured back to back over distinct weights,
+        // q/k/v grouped against separate calls at M = 4 / 8: 5.0 / 6.4 against
+        // 12.9 / 17.1 us, gate/up 16.7 / 19.6 against 20.1 / 25.0 us; at
+        // M = 16 gate/up grouped took 42.4 against 41.6 us
+        bool ps_each = M > 2 && M <= 8;
+        for (int j = 0; j < n; ++j) ps_each = ps_each && !gemm_preferred((int)M, gn[j], K);
+        const bool mma = M <= 2 && tq2::mma_group_supported((int)M, n, gn, K, dev);
+        const bool ps = !mma && ps_each && tq2::ps_group_supported((int)M, n, gn, K, dev);
+        if (mma || ps) {
             tq2::MatvecArgs a;
             a.x = x;
             a.qs = nullptr;
@@ -297,20 +319,41 @@ tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mat
             a.y_f16 = (y_dtype == TQ2_F16);
             a.act_scale = act_scale;
             a.inv_scale = act_scale != 0.0f ? 1.0f / act_scale : 0.0f;
-            a.out_scale = 0.0f;
+            a.out_scale = 0.0f;  // per matrix: gs, gi
             a.inv_out = 0.0f;
             a.stream = reinterpret_cast<cudaStream_t>(stream);
-            cudaError_t e = tq2::launch_matvec_mma_group(a, n, gq, gd, gy, gn, dev);
+            cudaError_t e = mma ? tq2::launch_matvec_mma_group(a, n, gq, gd, gy, gn, gs, gi, dev)
+                                : tq2::launch_matvec_ps_group(a, n, gq, gd, gy, gn, gs, gi, dev);
             if (e == cudaSuccess) e = cudaGetLastError();
             return from_cuda(e);
         }
     }
     // otherwise one call per matrix, same x, same stream
     for (int j = 0; j < n; ++j) {
-        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, 0.0f, d_status, stream, 0);
+        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, gs[j], d_status, stream, 0);
         if (st != TQ2_OK) return st;
     }
     return TQ2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
+                              const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
+                              float act_scale, uint32_t *d_status, tq2_stream_t stream)
+{
+    return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, nullptr, d_status, stream);
+}
+
+tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
+                                      const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
+                                      float act_scale, const float *out_scale, uint32_t *d_status,
+                                      tq2_stream_t stream)
+{
+    if (out_scale == nullptr) return TQ2_ERR_NULL;
+    return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, out_scale, d_status, stream);
 }
 
 tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,

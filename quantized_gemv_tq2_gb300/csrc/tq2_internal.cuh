@@ -40,12 +40,20 @@ struct MatvecArgs {
 bool mma_matvec_supported(int M, int64_t N, int64_t K, int device);
 cudaError_t launch_matvec_mma(const MatvecArgs &a, int device);
 
-// The same kernel over a group of up to 4 weight matrices that share x (and
-// K <= 4096): one launch, CTAs split in proportion to the rows.  qs/d/y/N
-// are host arrays of n device pointers / row counts.
+// The same kernel over a group of up to 4 weight matrices that share x: one
+// launch, CTAs split in proportion to the rows.  qs/d/y/N are host arrays of
+// n device pointers / row counts; out_scale/inv_out host arrays of n output
+// scales and their fp32 reciprocals (nullptr: none).
 bool mma_group_supported(int M, int n, const int64_t *N, int64_t K, int device);
 cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
-                                    void *const *y, const int64_t *N, int device);
+                                    void *const *y, const int64_t *N, const float *out_scale,
+                                    const float *inv_out, int device);
+
+// The pre-scaled kernel over such a group (M in 1..16).
+bool ps_group_supported(int M, int n, const int64_t *N, int64_t K, int device);
+cudaError_t launch_matvec_ps_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                                   void *const *y, const int64_t *N, const float *out_scale,
+                                   const float *inv_out, int device);
 
 // Ternary GEMM for many activation rows (any M): tcgen05 MMAs over weights
 // expanded to (q - 1) * d in tensor memory, x tiles by TMA (fake-quantised in

@@ -69,8 +69,8 @@ constexpr int kChunkBlocks = 16;                    // 256-blocks per stage row 
 constexpr int kTargetSmem = 112 * 1024;             // two CTAs per SM (PDL overlap)
 
 // One weight matrix of a launch.  A single call has one; a grouped call
-// (several matrices sharing x, K <= 4096) gives each matrix a contiguous range
-// of CTAs [g0, g0 + G) in proportion to its rows.
+// (several matrices sharing x) gives each matrix a contiguous range of CTAs
+// [g0, g0 + G) in proportion to its rows, and its own output scale.
 constexpr int kMaxGroup = 4;
 struct GroupMat {
     const uint8_t *qs;   // [N, K/4]
@@ -78,12 +78,14 @@ struct GroupMat {
     void *y;             // [M, N]
     int64_t N;
     int g0, G;
+    float out_scale;     // 0: y as computed; else requantised at store
+    float inv_out;       // fp32(1/out_scale)
 };
 
 struct MmaParams {
-    // K > 4096 only: qs as a 2-D tensor of uint64 [N][K/32], boxes of
-    // 128 x {16, 8, 4, 2, 1} rows
-    CUtensorMap tmap[5];  // 64-byte aligned by its type
+    // K > 4096 only: each matrix's qs as a 2-D tensor of uint64 [N][K/32],
+    // boxes of 128 x {16, 8, 4, 2, 1} rows
+    CUtensorMap tmap[kMaxGroup][5];  // 64-byte aligned by its type
     MatvecArgs a;
     int tma2d;       // 0: 1-D bulk copies of whole rows; 1: 2-D tensor boxes
     int G;           // CTAs; CTA i owns rows [i*N/G, (i+1)*N/G)
@@ -203,14 +205,14 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 const int y0 = (int)(r0 + rg0 * 16);
                 const int x = kc * 128;
                 if (rows == 16) {
-                    if (lane == 0) tensor2d_g2s(dst0, &p.tmap[0], x, y0, full, pol);
+                    if (lane == 0) tensor2d_g2s(dst0, &p.tmap[mi][0], x, y0, full, pol);
                 } else {
                     int roff = 0, box = 0;
 #pragma unroll
                     for (int i = 1; i < 5; ++i) {
                         const int h = 16 >> i;
                         if (rows & h) {
-                            if (lane == box) tensor2d_g2s(dst0 + roff * 1024, &p.tmap[i], x, y0 + roff, full, pol);
+                            if (lane == box) tensor2d_g2s(dst0 + roff * 1024, &p.tmap[mi][i], x, y0 + roff, full, pol);
                             roff += h;
                             ++box;
                         }
@@ -743,7 +745,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) s += red[((rg * kConsumerWarps + w) * kM + m) * 16 + ri];
         if (prologue) s *= p.a.act_scale;
-        s = requant_out(s, p.a.out_scale, p.a.inv_out);
+        s = requant_out(s, p.mats[mi].out_scale, p.mats[mi].inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(y_g)[o] = __float2half_rn(s);
@@ -856,7 +858,7 @@ bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaParams &p
 // for the largest per-CTA row count.
 bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, int max_dyn, MmaParams &p)
 {
-    if (max_dyn <= 0 || n < 1 || n > kMaxGroup || K > 256 * kChunkBlocks) return false;
+    if (max_dyn <= 0 || n < 1 || n > kMaxGroup) return false;
     int64_t total = 0;
     for (int j = 0; j < n; ++j) {
         if (N[j] < 1) return false;
@@ -902,16 +904,16 @@ bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, int max_d
 }
 
 // qs as uint64 [N][K/32]; boxes 128 x {16, 8, 4, 2, 1}
-cudaError_t encode_qs_maps(const MatvecArgs &a, MmaParams &p)
+cudaError_t encode_qs_maps(const uint8_t *qs, int64_t N, int64_t K, CUtensorMap (&tmap)[5])
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
+    const cuuint64_t dims[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
     const cuuint32_t estr[2] = {1, 1};
     for (int i = 0; i < 5; ++i) {
         const cuuint32_t box[2] = {128, (cuuint32_t)(16 >> i)};
-        CUresult r = enc(&p.tmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.qs), dims,
+        CUresult r = enc(&tmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(qs), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -927,9 +929,9 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
     if (!plan_for(kM, a.N, a.K, device, max_dynamic_smem<kM>(device), p))
         return cudaErrorInvalidConfiguration;
     p.n_mats = 1;
-    p.mats[0] = GroupMat{a.qs, a.d, a.y, a.N, 0, p.G};
+    p.mats[0] = GroupMat{a.qs, a.d, a.y, a.N, 0, p.G, a.out_scale, a.inv_out};
     if (p.tma2d) {
-        cudaError_t e = encode_qs_maps(a, p);
+        cudaError_t e = encode_qs_maps(a.qs, a.N, a.K, p.tmap[0]);
         if (e != cudaSuccess) return e;
     }
     auto kern = matvec_mma_kernel<kM>;
@@ -948,7 +950,8 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
 
 template <int kM>
 cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
-                              void *const *y, const int64_t *N, int device)
+                              void *const *y, const int64_t *N, const float *out_scale, const float *inv_out,
+                              int device)
 {
     MmaParams p{};
     p.a = a;
@@ -957,6 +960,12 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
         p.mats[j].qs = qs[j];
         p.mats[j].d = d[j];
         p.mats[j].y = y[j];
+        p.mats[j].out_scale = out_scale ? out_scale[j] : 0.0f;
+        p.mats[j].inv_out = inv_out ? inv_out[j] : 0.0f;
+        if (p.tma2d) {
+            cudaError_t e = encode_qs_maps(qs[j], N[j], a.K, p.tmap[j]);
+            if (e != cudaSuccess) return e;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.G);
@@ -982,10 +991,11 @@ bool mma_group_supported(int M, int n, const int64_t *N, int64_t K, int device)
 }
 
 cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
-                                    void *const *y, const int64_t *N, int device)
+                                    void *const *y, const int64_t *N, const float *out_scale,
+                                    const float *inv_out, int device)
 {
-    if (a.M == 1) return launch_group_impl<1>(a, n, qs, d, y, N, device);
-    if (a.M == 2) return launch_group_impl<2>(a, n, qs, d, y, N, device);
+    if (a.M == 1) return launch_group_impl<1>(a, n, qs, d, y, N, out_scale, inv_out, device);
+    if (a.M == 2) return launch_group_impl<2>(a, n, qs, d, y, N, out_scale, inv_out, device);
     return cudaErrorInvalidValue;
 }
 

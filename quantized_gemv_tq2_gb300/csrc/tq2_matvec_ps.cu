@@ -38,6 +38,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "tq2_device.cuh"
@@ -54,8 +55,23 @@ constexpr int kThreads = kConsumers + 32;      // + one producer warp
 constexpr int kMaxStages = 8;
 constexpr int kTwoPerSm = 112 * 1024;          // shared memory that lets two CTAs share an SM
 
+// One weight matrix of a launch.  A single call has one; a grouped call
+// (several matrices sharing x) gives each matrix a contiguous range of CTAs
+// [g0, g0 + G) in proportion to its rows, and its own output scale.
+constexpr int kMaxGroup = 4;
+struct PsMat {
+    const uint8_t *qs;   // [N, K/4]
+    const uint16_t *d;   // [N, K/256]
+    void *y;             // [M, N]
+    int64_t N;
+    int g0, G;
+    float out_scale;     // 0: y as computed; else requantised at store
+    float inv_out;       // fp32(1/out_scale)
+};
+
 struct PsParams {
-    CUtensorMap tmap[5];  // qs as uint64 [N][K/32], boxes (kcb*8) x {16, 8, 4, 2, 1} rows
+    // each matrix's qs as uint64 [N][K/32], boxes (kcb*8) x {16, 8, 4, 2, 1} rows
+    CUtensorMap tmap[kMaxGroup][5];
     MatvecArgs a;
     int G;        // CTAs
     int B;        // 256-blocks along K
@@ -71,6 +87,8 @@ struct PsParams {
     int dstr;     // floats per row of the d slice (B + 1: odd, conflict-free)
     int xblocks;  // 256-blocks per x chunk (kcb * xkc)
     int off_bar, off_red, off_dsm, off_xinfo, off_frag, off_ring, smem_total;
+    int n_mats;
+    PsMat mats[kMaxGroup];
 };
 
 __device__ __forceinline__ void consumers_sync()
@@ -254,9 +272,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int M = p.a.M;
-    const int64_t N = p.a.N, K = p.a.K;
-    const int64_t r0 = (int64_t)blockIdx.x * N / p.G;
-    const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / p.G;
+    // this CTA's matrix and rows
+    int mi = 0;
+    while (mi + 1 < p.n_mats && (int)blockIdx.x >= p.mats[mi + 1].g0) ++mi;
+    const uint8_t *const qs_g = p.mats[mi].qs;
+    const uint16_t *const d_g = p.mats[mi].d;
+    void *const y_g = p.mats[mi].y;
+    const int64_t N = p.mats[mi].N, K = p.a.K;
+    const int cta = (int)blockIdx.x - p.mats[mi].g0, G_m = p.mats[mi].G;
+    const int64_t r0 = (int64_t)cta * N / G_m;
+    const int64_t r1 = (int64_t)(cta + 1) * N / G_m;
     const int nrows = (int)(r1 - r0);
     const int nrg = (nrows + 15) >> 4;
     const int n_rgs = (nrg + p.R - 1) / p.R;  // stage row steps
@@ -306,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
                 const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full, bytes);
-                    bulk_g2s(dst0, p.a.qs + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
+                    bulk_g2s(dst0, qs_g + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
                 }
             } else {
                 // boxes of 16 rows x (kcb*64) bytes; the last group split into 8/4/2/1
@@ -315,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
                 const int x = kc * p.kcb * 8;
                 int roff = 0, box = 0;
                 while (roff + 16 <= rows) {
-                    if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[0], x, (int)(r0 + rg0 * 16 + roff), full, pol);
+                    if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[mi][0], x, (int)(r0 + rg0 * 16 + roff), full, pol);
                     roff += 16;
                     ++box;
                 }
@@ -323,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
                 for (int i = 1; i < 5; ++i) {
                     const int hh = 16 >> i;
                     if ((rows - roff) & hh) {
-                        if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[i], x, (int)(r0 + rg0 * 16 + roff), full, pol);
+                        if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[mi][i], x, (int)(r0 + rg0 * 16 + roff), full, pol);
                         roff += hh;
                         ++box;
                     }
@@ -360,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     for (int i = tid; i < p.xblocks * 8 * NT; i += kConsumers) xinfo[i] = make_float2(0.0f, 0.0f);
     {
         const int nd = nrows * B;
-        const uint16_t *dsrc = p.a.d + r0 * B;
+        const uint16_t *dsrc = d_g + r0 * B;
         for (int base = 0; base < nd; base += kConsumers * 8) {
             uint16_t v[8];
 #pragma unroll
@@ -417,6 +442,122 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     const uint32_t ring_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
     const uint32_t a_half = (uint32_t)(8 * p.rb);
 
+    // K = 4096 with x resident: every stage is one 16-row group x all 16
+    // blocks, and warp w takes blocks w and w + 8 of every stage, so its B
+    // fragment bases and per-column block terms stay in registers for the
+    // whole call.  A stage's codes go to registers as soon as its copy has
+    // landed and the slot is released at once; the next stage's codes are
+    // read once this stage's last MMAs are issued.  Four accumulator chains
+    // (one per code class) per block.
+    const bool fast = p.n_kc == 1 && p.R == 1 && p.kcb == 16 && p.xkc == 1;
+    if (fast) {
+        constexpr int kU = 16 / kWarps;  // blocks per warp and stage
+        uint32_t fbu[kU], au[kU], du[kU], xiu[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int b = warp + u * kWarps;
+            fbu[u] = frag + (uint32_t)(b * 512 * M);
+            au[u] = ring_thr + (uint32_t)(b * 64);
+            du[u] = smem_addr(dsm) + (uint32_t)(g * p.dstr + b) * 4u;
+            xiu[u] = smem_addr(xinfo) + (uint32_t)(b * 8 * NT + 2 * t) * 8u;  // + 64 per n-tile
+        }
+        uint32_t h1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) h1[nt] = (uint32_t)(64 * min(8, M - 8 * nt));
+        const uint32_t d_half = (uint32_t)(8 * p.dstr) * 4u, d_rg = (uint32_t)(16 * p.dstr) * 4u;
+        uint32_t W[kU][4], V[kU][4];
+        float dg[kU], dg8[kU];
+        // a stage's codes to registers; the slot is released once they are read
+#define TQ2_PS_LOAD_CODES(SL)                                                              \
+        do {                                                                               \
+            _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
+                const uint32_t pa_ = au[u_] + (uint32_t)((SL) * p.stage_bytes);           \
+                const uint4 va_ = lds128(pa_), vb_ = lds128(pa_ + a_half);                 \
+                W[u_][0] = va_.x; W[u_][1] = va_.y; W[u_][2] = va_.z; W[u_][3] = va_.w;    \
+                V[u_][0] = vb_.x; V[u_][1] = vb_.y; V[u_][2] = vb_.z; V[u_][3] = vb_.w;    \
+            }                                                                              \
+            __syncwarp();                                                                  \
+            if (lane == 0) mbar_arrive(smem_addr(&bars[S + (SL)]));                        \
+        } while (0)
+#define TQ2_PS_LOAD_SCALES(RG)                                                             \
+        do {                                                                               \
+            _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
+                dg[u_] = lds_f32(du[u_] + (uint32_t)(RG) * d_rg);                          \
+                dg8[u_] = lds_f32(du[u_] + (uint32_t)(RG) * d_rg + d_half);                \
+            }                                                                              \
+        } while (0)
+        int sl = 0, ph = 0;
+        bool ok = n_stages > 0;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[0]), 0u))) {
+            if (lane == 0) report_timeout(p, abort_flag);
+            ok = false;
+        }
+        if (ok) {
+            TQ2_PS_LOAD_CODES(0);
+            TQ2_PS_LOAD_SCALES(0);
+        }
+        for (int s = 0; ok && s < n_stages; ++s) {
+            const int nsl = (sl + 1 == S) ? 0 : sl + 1;
+            const int nph = (sl + 1 == S) ? (ph ^ 1) : ph;
+            float acc[NT][4];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float4 xi;
+                    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                                 : "=f"(xi.x), "=f"(xi.y), "=f"(xi.z), "=f"(xi.w)
+                                 : "r"(xiu[u] + (uint32_t)(64 * nt)));
+                    float c0[4] = {xi.x, xi.z, xi.x, xi.z};
+                    float c1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c2[4] = {0.0f, 0.0f, 0.0f, 0.0f},
+                          c3[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int jw = 0; jw < 4; ++jw) {
+                        const uint32_t w0 = W[u][jw], w1 = V[u][jw], s0 = w0 >> 8, s1 = w1 >> 8;
+                        const uint4 f0 = lds128(fbu[u] + xo[nt][jw]);
+                        const uint4 f1 = lds128(fbu[u] + xo[nt][jw] + h1[nt]);
+                        mma_16816(c0, w0 & 0x00030003u, w1 & 0x00030003u, s0 & 0x00030003u, s1 & 0x00030003u, f0.x, f0.y);
+                        mma_16816(c1, w0 & 0x000C000Cu, w1 & 0x000C000Cu, s0 & 0x000C000Cu, s1 & 0x000C000Cu, f0.z, f0.w);
+                        mma_16816(c2, w0 & 0x00300030u, w1 & 0x00300030u, s0 & 0x00300030u, s1 & 0x00300030u, f1.x, f1.y);
+                        mma_16816(c3, w0 & 0x00C000C0u, w1 & 0x00C000C0u, s0 & 0x00C000C0u, s1 & 0x00C000C0u, f1.z, f1.w);
+                    }
+                    const float e0 = xi.y * dg[u], e1 = xi.w * dg[u], e2 = xi.y * dg8[u], e3 = xi.w * dg8[u];
+                    acc[nt][0] = fmaf((c0[0] + c1[0]) + (c2[0] + c3[0]), e0, u ? acc[nt][0] : 0.0f);
+                    acc[nt][1] = fmaf((c0[1] + c1[1]) + (c2[1] + c3[1]), e1, u ? acc[nt][1] : 0.0f);
+                    acc[nt][2] = fmaf((c0[2] + c1[2]) + (c2[2] + c3[2]), e2, u ? acc[nt][2] : 0.0f);
+                    acc[nt][3] = fmaf((c0[3] + c1[3]) + (c2[3] + c3[3]), e3, u ? acc[nt][3] : 0.0f);
+                }
+                if (u + 1 == kU && s + 1 < n_stages) {
+                    // this stage's codes are all in MMA operands: read the next stage's
+                    if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[nsl]), (uint32_t)nph))) {
+                        TQ2_PS_LOAD_CODES(nsl);
+                    } else {
+                        if (lane == 0) report_timeout(p, abort_flag);
+                        ok = false;
+                    }
+                }
+            }
+            if (ok && s + 1 < n_stages) TQ2_PS_LOAD_SCALES(s + 1);
+            // row group s: this warp's partials (each row group once per warp)
+            float *rp = red + ((s * kWarps + warp) * 16) * M;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int col = 8 * nt + 2 * t;
+                if (col < M) {
+                    rp[g * M + col] = acc[nt][0];
+                    rp[(g + 8) * M + col] = acc[nt][2];
+                }
+                if (col + 1 < M) {
+                    rp[g * M + col + 1] = acc[nt][1];
+                    rp[(g + 8) * M + col + 1] = acc[nt][3];
+                }
+            }
+            sl = nsl;
+            ph = nph;
+        }
+#undef TQ2_PS_LOAD_CODES
+#undef TQ2_PS_LOAD_SCALES
+    } else {
     int slot = 0, phase = 0;
     int xc = 0, rgi = 0, kci = 0;
     bool alive = true;
@@ -497,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     }
     (void)n_xc;
     if (cur_rg >= 0) flush(cur_rg);
+    }
     consumers_sync();
     if (*abort_flag) return;  // y is invalid; TQ2_FLAG_TIMEOUT was reported
 
@@ -508,27 +650,26 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) s += red[((rg * kWarps + w) * 16 + ri) * M + m];
         if (prologue) s *= p.a.act_scale;
-        s = requant_out(s, p.a.out_scale, p.a.inv_out);
+        s = requant_out(s, p.mats[mi].out_scale, p.mats[mi].inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
         if (p.a.y_f16)
-            reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(s);
+            reinterpret_cast<__half *>(y_g)[o] = __float2half_rn(s);
         else
-            reinterpret_cast<float *>(p.a.y)[o] = s;
+            reinterpret_cast<float *>(y_g)[o] = s;
     }
 }
 
 // ------------------------------------------------------------------ host side
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Shared-memory plan for G CTAs within `cap` bytes; false if it cannot fit.
-bool make_plan(int M, int64_t N, int64_t K, int G, int cap, bool resident, int kcb_try, PsParams &p)
+// Shared-memory plan for CTAs of at most max_rows rows within `cap` bytes;
+// false if it cannot fit.
+bool make_plan(int M, int64_t max_rows, int64_t K, int cap, bool resident, int kcb_try, PsParams &p)
 {
     const int64_t B = K / 256;
     if (B < 1 || B > (1 << 20)) return false;
-    p.G = G;
     p.B = (int)B;
     p.NT = (M + 7) / 8;
-    const int64_t max_rows = (N + G - 1) / G;
     p.max_rg = (int)((max_rows + 15) / 16);
     if (resident) {
         if (B <= 16) {
@@ -612,38 +753,108 @@ int max_dynamic_smem(int device)
 // 18.9 against 16.4 / 18.3 / 19.7 us; gate/up 16384x4096 at M = 7 / 8: 14.2
 // / 18.7 against 14.7 / 19.0 us): K-chunked x is re-staged per K range
 // behind two barriers that drain the stage ring.
+bool plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, PsParams &p)
+{
+    for (int cap : {kTwoPerSm, max_dyn}) {
+        if (cap > max_dyn) continue;
+        if (make_plan(M, max_rows, K, cap, true, 0, p)) return true;
+    }
+    for (int cap : {kTwoPerSm, max_dyn}) {
+        if (cap > max_dyn) continue;
+        for (int kcb : {16, 8, 4, 2, 1})
+            if (make_plan(M, max_rows, K, cap, false, kcb, p)) return true;
+    }
+    return false;
+}
+
+int max_dyn_for(int M, int device)
+{
+    return (M <= 8) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
+}
+
 bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
 {
-    const int max_dyn = (M <= 8) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
+    const int max_dyn = max_dyn_for(M, device);
     if (max_dyn <= 0 || M < 1 || M > 16) return false;
     const int nsm = sm_count(device);
     int G = (int)((N < (int64_t)nsm) ? N : nsm);
     for (;;) {
-        for (int cap : {kTwoPerSm, max_dyn}) {
-            if (cap > max_dyn) continue;
-            if (make_plan(M, N, K, G, cap, true, 0, p)) return true;
-        }
-        for (int cap : {kTwoPerSm, max_dyn}) {
-            if (cap > max_dyn) continue;
-            for (int kcb : {16, 8, 4, 2, 1})
-                if (make_plan(M, N, K, G, cap, false, kcb, p)) return true;
+        if (plan_rows(M, (N + G - 1) / G, K, max_dyn, p)) {
+            p.G = G;
+            p.n_mats = 1;
+            p.mats[0].N = N;
+            p.mats[0].g0 = 0;
+            p.mats[0].G = G;
+            return true;
         }
         if (G >= N) return false;
         G = (int)((2 * (int64_t)G < N) ? 2 * G : N);
     }
 }
 
+// CTAs of a group in proportion to the matrices' rows (at least one each,
+// one per SM in total first, then twice as many while no plan fits), then
+// the plan for the largest per-CTA row count.
+bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, PsParams &p)
+{
+    const int max_dyn = max_dyn_for(M, device);
+    if (max_dyn <= 0 || M < 1 || M > 16 || n < 1 || n > kMaxGroup) return false;
+    int64_t total = 0;
+    for (int j = 0; j < n; ++j) {
+        if (N[j] < 1) return false;
+        total += N[j];
+    }
+    const int nsm = sm_count(device);
+    for (int cap = nsm; cap <= 64 * nsm; cap *= 2) {
+        int G[kMaxGroup], sum = 0;
+        for (int j = 0; j < n; ++j) {
+            int64_t g = (int64_t)cap * N[j] / total;
+            if (g < 1) g = 1;
+            if (g > N[j]) g = (int)N[j];
+            G[j] = (int)g;
+            sum += G[j];
+        }
+        while (sum < cap) {  // leftover CTAs to the matrix with the most rows per CTA
+            int best = -1;
+            double worst = 0.0;
+            for (int j = 0; j < n; ++j)
+                if (G[j] < N[j] && (double)N[j] / G[j] > worst) {
+                    worst = (double)N[j] / G[j];
+                    best = j;
+                }
+            if (best < 0) break;
+            ++G[best];
+            ++sum;
+        }
+        int64_t max_rows = 0;
+        int g0 = 0;
+        for (int j = 0; j < n; ++j) {
+            max_rows = std::max<int64_t>(max_rows, (N[j] + G[j] - 1) / G[j]);
+            p.mats[j].N = N[j];
+            p.mats[j].g0 = g0;
+            p.mats[j].G = G[j];
+            g0 += G[j];
+        }
+        if (plan_rows(M, max_rows, K, max_dyn, p)) {
+            p.n_mats = n;
+            p.G = g0;
+            return true;
+        }
+    }
+    return false;
+}
+
 // qs as uint64 [N][K/32]; boxes (kcb*8) x {16, 8, 4, 2, 1}
-cudaError_t encode_maps(const MatvecArgs &a, PsParams &p)
+cudaError_t encode_maps(const uint8_t *qs, int64_t N, int64_t K, int kcb, CUtensorMap (&tmap)[5])
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
+    const cuuint64_t dims[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
     const cuuint32_t estr[2] = {1, 1};
     for (int i = 0; i < 5; ++i) {
-        const cuuint32_t box[2] = {(cuuint32_t)(p.kcb * 8), (cuuint32_t)(16 >> i)};
-        CUresult r = enc(&p.tmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.qs), dims, strides,
+        const cuuint32_t box[2] = {(cuuint32_t)(kcb * 8), (cuuint32_t)(16 >> i)};
+        CUresult r = enc(&tmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(qs), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -652,26 +863,59 @@ cudaError_t encode_maps(const MatvecArgs &a, PsParams &p)
 }
 
 template <int NT>
-cudaError_t launch_impl(const MatvecArgs &a, int device)
+cudaError_t launch_params(const PsParams &p, cudaStream_t stream)
 {
-    PsParams p{};
-    p.a = a;
-    if (!plan_for(a.M, a.N, a.K, device, p)) return cudaErrorInvalidConfiguration;
-    if (p.tma2d) {
-        cudaError_t e = encode_maps(a, p);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.G);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)p.smem_total;
-    cfg.stream = a.stream;
+    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, matvec_ps_kernel<NT>, p);
+}
+
+template <int NT>
+cudaError_t launch_impl(const MatvecArgs &a, int device)
+{
+    PsParams p{};
+    p.a = a;
+    if (!plan_for(a.M, a.N, a.K, device, p)) return cudaErrorInvalidConfiguration;
+    p.mats[0].qs = a.qs;
+    p.mats[0].d = a.d;
+    p.mats[0].y = a.y;
+    p.mats[0].out_scale = a.out_scale;
+    p.mats[0].inv_out = a.inv_out;
+    if (p.tma2d) {
+        cudaError_t e = encode_maps(a.qs, a.N, a.K, p.kcb, p.tmap[0]);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_params<NT>(p, a.stream);
+}
+
+template <int NT>
+cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                              void *const *y, const int64_t *N, const float *out_scale, const float *inv_out,
+                              int device)
+{
+    PsParams p{};
+    p.a = a;
+    if (!group_plan(a.M, n, N, a.K, device, p)) return cudaErrorInvalidConfiguration;
+    for (int j = 0; j < n; ++j) {
+        p.mats[j].qs = qs[j];
+        p.mats[j].d = d[j];
+        p.mats[j].y = y[j];
+        p.mats[j].out_scale = out_scale ? out_scale[j] : 0.0f;
+        p.mats[j].inv_out = inv_out ? inv_out[j] : 0.0f;
+        if (p.tma2d) {
+            cudaError_t e = encode_maps(qs[j], N[j], a.K, p.kcb, p.tmap[j]);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return launch_params<NT>(p, a.stream);
 }
 
 }  // namespace
@@ -681,6 +925,22 @@ bool ps_matvec_supported(int M, int64_t N, int64_t K, int device)
     if (M < 1 || M > 16 || N < 1 || K < 256) return false;
     PsParams p{};
     return plan_for(M, N, K, device, p);
+}
+
+bool ps_group_supported(int M, int n, const int64_t *N, int64_t K, int device)
+{
+    if (M < 1 || M > 16 || K < 256) return false;
+    PsParams p{};
+    return group_plan(M, n, N, K, device, p);
+}
+
+cudaError_t launch_matvec_ps_group(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                                   void *const *y, const int64_t *N, const float *out_scale,
+                                   const float *inv_out, int device)
+{
+    if (a.M >= 1 && a.M <= 8) return launch_group_impl<1>(a, n, qs, d, y, N, out_scale, inv_out, device);
+    if (a.M >= 9 && a.M <= 16) return launch_group_impl<2>(a, n, qs, d, y, N, out_scale, inv_out, device);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_matvec_ps(const MatvecArgs &a, int device)

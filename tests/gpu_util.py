@@ -87,3 +87,28 @@ class GuardedOutput:
         hi = self.buf[self.PAD + self.M * self.N:]
         assert bool(torch.all(lo == self.canary)), f"{what}: write below y"
         assert bool(torch.all(hi == self.canary)), f"{what}: write above y"
+
+
+def check_requant(y_gpu, y_ref, tol_sum, s_o, y_dtype, what):
+    """Codes within the tolerance band, stored values exactly code * s_o."""
+    s32 = np.float32(s_o)
+    yg = np.asarray(y_gpu)
+    code = np.rint(yg.astype(np.float64) / np.float64(s32))
+    assert np.all(np.abs(code) <= 128), what
+    assert np.all((code >= -128) & (code <= 127)), what
+    stored = code.astype(np.float32) * s32  # one fp32 rounding, as the kernel
+    if y_dtype == 1:
+        stored = stored.astype(np.float16)
+    assert np.array_equal(yg, stored.astype(yg.dtype)), what + ": stored value is not code * s"
+    bound = oracle.tolerance(tol_sum)
+    lo, _ = oracle.requant(y_ref - bound, s_o)
+    hi, _ = oracle.requant(y_ref + bound, s_o)
+    ref, _ = oracle.requant(y_ref, s_o)
+    bad = (code < lo) | (code > hi)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} codes outside the band; first at {i}: "
+                             f"gpu={code[i]} band=[{lo[i]}, {hi[i]}] y_ref={y_ref[i]!r}")
+    # the kernel's sums are far more accurate than the bound: it almost
+    # always lands on the oracle's own code
+    assert np.mean(code == ref) > 0.9, what

@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
                           "tq2_matvec_impl", "tq2_matvec_requant", "tq2_gemm",
                           "tq2_affine4_matvec", "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version",
-                          "tq2_test_matvec_stall"}
+                          "tq2_test_matvec_stall", "tq2_matvec_grouped_requant"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
 
@@ -173,6 +173,16 @@ def test_grouped_rejects_bad_arguments(L):
     assert G(y=Pn(0x40000, 0, 0x60000)) == NULL
     assert G(x=A2) == ALIGN
     assert G(M=0) == OK                           # nothing to do
+    # the requantising variant: one finite, non-negative scale per matrix
+    F3 = ctypes.c_float * n
+    R = lambda sc, **k: L.tq2_matvec_grouped_requant(k.get("x", A16), k.get("M", 1), 512, n, cast(good), cast(good),
+                                                     cast(Ns), cast(ys), 0, 0.0, sc, NUL, S)
+    assert R(NUL) == NULL
+    assert R(cast(F3(0.5, -0.1, 0.2))) == ARG
+    assert R(cast(F3(0.5, float("inf"), 0.2))) == ARG
+    assert R(cast(F3(0.5, float("nan"), 0.2))) == ARG
+    assert R(cast(F3(0.5, 0.0, 0.2)), M=0) == OK
+    assert R(cast(F3(0.5, 0.1, 0.2)), x=A2) == ALIGN
     assert G(N=(ctypes.c_int64 * n)(0, 0, 0)) == OK
 
 

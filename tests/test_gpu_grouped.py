@@ -1,13 +1,16 @@
-"""GPU parity of tq2_matvec_grouped (several matrices sharing x) against the
-CPU oracle, per matrix: the one-launch path (M <= 2, K <= 4096) with decoder
-layer shapes, odd sizes and the prologue; the fallback path (M > 2 or
-K > 4096); and the back-to-back graph configuration the benchmark times."""
+"""GPU parity of tq2_matvec_grouped and tq2_matvec_grouped_requant (several
+matrices sharing x) against the CPU oracle, per matrix: one launch of the
+class-column kernel (M <= 2, any K) and of the pre-scaled kernel (M up to 16,
+K = 4096 and longer), decoder layer shapes, odd sizes and the prologue; the
+fallback to consecutive calls where a matrix would take the GEMM; each
+matrix's own output requantisation; guard bands around every y; and the
+back-to-back graph configuration the benchmark times."""
 import numpy as np
 import pytest
 
 import oracle
 import tq2_synth as syn
-from gpu_util import assert_within_tolerance, dev, host, sample_rows
+from gpu_util import GuardedOutput, assert_within_tolerance, check_requant, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -32,14 +35,20 @@ def _mats(seed, Ns, K):
 
 
 @pytest.mark.parametrize("M,K,Ns", [
-    (1, 4096, (4096, 256, 256)),      # q, k, v
+    (1, 4096, (4096, 256, 256)),      # q, k, v: class-column kernel, one launch
     (1, 4096, (16384, 16384)),        # gate, up
     (2, 4096, (4096, 256, 256)),
     (1, 1024, (33, 1, 300)),
     (2, 256, (17, 17)),
     (1, 512, (5, 7, 11, 13)),         # four matrices
-    (3, 1024, (40, 24)),              # M > 2: consecutive calls
-    (1, 8448, (50, 70)),              # K > 4096: consecutive calls
+    (1, 8448, (50, 70)),              # K > 4096: 2-D boxes, one tensor map per matrix
+    (2, 16384, (300, 41)),
+    (3, 1024, (40, 24)),              # M > 2: pre-scaled kernel, one launch
+    (4, 4096, (4096, 256, 256)),      # q, k, v at M = 4 (one 16-row group x 16 blocks per stage)
+    (8, 4096, (16384, 16384)),        # gate, up at M = 8
+    (16, 4096, (1000, 3000)),         # M > 8: consecutive calls
+    (5, 8448, (100, 60)),             # M > 2, K > 4096
+    (12, 4096, (4096, 256, 256)),     # k/v would take the GEMM: consecutive calls
 ])
 @pytest.mark.parametrize("prologue", [False, True])
 @pytest.mark.parametrize("yd", [0, 1])
@@ -50,15 +59,79 @@ def test_grouped_matches_oracle(T, M, K, Ns, prologue, yd):
     s = float(syn.act_scale(seed)) if prologue else 0.0
     mats = _mats(seed, Ns, K)
     st = T.zeros(1, dtype=T.int32, device="cuda")
-    ys = tq2.matvec_grouped(dev(x), [dev(q) for q, _ in mats], [dev(d) for _, d in mats], y_dtype=yd,
-                            act_scale=s, status=st)
+    outs = [GuardedOutput(M, N, yd) for N in Ns]
+    tq2.matvec_grouped(dev(x), [dev(q) for q, _ in mats], [dev(d) for _, d in mats], y_list=[o.y for o in outs],
+                       act_scale=s, status=st)
     T.cuda.synchronize()
     assert int(st.item()) == 0
-    for j, ((qs, d), y) in enumerate(zip(mats, ys)):
+    for j, ((qs, d), out) in enumerate(zip(mats, outs)):
         N = Ns[j]
+        out.check(f"matrix {j} N={N}")
         rows = sample_rows(N, 128, seed=j) if N > 2048 else np.arange(N)
         y_ref, tol = oracle.matvec_rows(x, qs, d, K, rows, act_scale=s)
-        assert_within_tolerance(host(y)[:, rows].astype(np.float64), y_ref, tol, f"matrix {j} N={N}")
+        assert_within_tolerance(host(out.y)[:, rows].astype(np.float64), y_ref, tol, f"matrix {j} N={N}")
+
+
+@pytest.mark.parametrize("M,K,Ns", [
+    (1, 4096, (4096, 256, 256)),
+    (2, 8448, (70, 50)),
+    (4, 4096, (4096, 256, 256)),
+    (8, 4096, (16384, 16384)),
+    (12, 4096, (4096, 256, 256)),     # consecutive calls, each with its own scale
+])
+@pytest.mark.parametrize("yd", [0, 1])
+def test_grouped_requant_per_matrix(T, M, K, Ns, yd):
+    """Each matrix's y is requantised with its own out_scale (0 for one of
+    them: stored as computed), with and without the int8 prologue."""
+    import quantized_gemv_tq2_gb300 as tq2
+    for prologue in (False, True):
+        seed = 70 + M + len(Ns) + int(prologue)
+        x = syn.activations(seed, M, K, heavy=prologue)
+        s = float(syn.act_scale(seed)) if prologue else 0.0
+        mats = _mats(seed, Ns, K)
+        scales = [0.37 * (j + 1) for j in range(len(Ns))]
+        scales[-1] = 0.0
+        st = T.zeros(1, dtype=T.int32, device="cuda")
+        outs = [GuardedOutput(M, N, yd) for N in Ns]
+        tq2.matvec_grouped(dev(x), [dev(q) for q, _ in mats], [dev(d) for _, d in mats],
+                           y_list=[o.y for o in outs], act_scale=s, status=st, out_scales=scales)
+        T.cuda.synchronize()
+        assert int(st.item()) == 0
+        for j, ((qs, d), out) in enumerate(zip(mats, outs)):
+            N = Ns[j]
+            out.check(f"requant matrix {j}")
+            rows = sample_rows(N, 128, seed=j) if N > 2048 else np.arange(N)
+            y_ref, tol = oracle.matvec_rows(x, qs, d, K, rows, act_scale=s)
+            yg = host(out.y)[:, rows]
+            what = f"M={M} matrix {j} N={N} s_o={scales[j]} prologue={prologue}"
+            if scales[j] == 0.0:
+                assert_within_tolerance(yg.astype(np.float64), y_ref, tol, what)
+            else:
+                check_requant(yg, y_ref, tol, scales[j], yd, what)
+
+
+def test_grouped_prescaled_equals_single_calls(T):
+    """One pre-scaled launch over q/k/v agrees with the single-matrix
+    pre-scaled launches to fp32 rounding.  (The group's rows per CTA differ
+    from a single call's, so the shared-memory plan, and with it whether x
+    stays resident or is staged per K range, can differ; that changes the
+    order of the fp32 block sums, not the result beyond rounding.)"""
+    import quantized_gemv_tq2_gb300 as tq2
+    K, Ns = 4096, (4096, 256, 256)
+    for M in (3, 4, 8):
+        xh = syn.activations(M, M, K)
+        x = dev(xh)
+        mh = _mats(M, Ns, K)
+        mats = [(dev(q), dev(d)) for q, d in mh]
+        ys = tq2.matvec_grouped(x, [q for q, _ in mats], [d for _, d in mats])
+        for (qh, dh), (q, d), y in zip(mh, mats, ys):
+            single = tq2.matvec(x, q, d, impl=tq2.IMPL_PS)
+            T.cuda.synchronize()
+            rows = sample_rows(qh.shape[0], 256, seed=M)
+            _, tol_sum = oracle.matvec_rows(xh, qh, dh, K, rows)
+            diff = np.abs(host(y)[:, rows].astype(np.float64) - host(single)[:, rows].astype(np.float64))
+            # reordered fp32 sums: a few units of 2^-24 of sum |d_b x_k|, far below the parity bound
+            assert np.all(diff <= 1e-6 * tol_sum + 1e-7), (M, float((diff / (tol_sum + 1e-30)).max()))
 
 
 def test_grouped_equals_single_calls(T):
