@@ -324,6 +324,27 @@ TQ2_API tq2_status tq2_test_matvec_stall(const uint16_t *x, int64_t M, const uin
                                          int64_t N, int64_t K, float *y, uint32_t *d_status,
                                          tq2_stream_t stream, int stall_stage, int wait_limit_us);
 
+/*
+ * tq2_test_gemm_stall -- a test hook, not part of the product (the pages
+ * have no counterpart): tq2_gemm with impl 1 (the tcgen05 GEMM) and fp32 y,
+ * except that in every CTA the x producer skips the copy of its stage
+ * stall_stage (stages of 8 k-steps, counted within the CTA's share of K),
+ * and every wait of the stage rings gives up after wait_limit_us
+ * microseconds instead of 200 ms (the waits for the MMAs' completion, which
+ * guard the release of tensor memory, and the split-K hand-off waits keep
+ * 200 ms).  The MMA issuer's wait for that stage runs out: the kernel sets
+ * TQ2_FLAG_TIMEOUT in *d_status, drains its copies and MMAs, frees its tensor
+ * memory and returns without storing y.
+ *   stall_stage, wait_limit_us, d_status  as tq2_test_matvec_stall.
+ *   act_scale  as tq2_gemm (> 0 also runs the in-place x conversion, whose
+ *              wait runs out too).
+ *   Other arguments and errors as tq2_gemm with impl 1 (TQ2_ERR_ARG for a
+ *   shape the GEMM cannot plan).  The call takes a few wait limits.
+ */
+TQ2_API tq2_status tq2_test_gemm_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
+                                       int64_t N, int64_t K, float *y, float act_scale, uint32_t *d_status,
+                                       tq2_stream_t stream, int stall_stage, int wait_limit_us);
+
 /* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
  * host thread ("no error" if none): name and description, static storage. */
 TQ2_API const char *tq2_last_cuda_error(void);

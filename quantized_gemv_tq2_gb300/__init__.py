@@ -70,6 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_gemm.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, P, I32]
         L.tq2_affine4_matvec.argtypes = [P, I64, P, P, P, I64, I64, I64, P, I32, P, P]
         L.tq2_test_matvec_stall.argtypes = [P, I64, P, P, I64, I64, P, P, P, I32, I32]
+        L.tq2_test_gemm_stall.argtypes = [P, I64, P, P, I64, I64, P, F, P, P, I32, I32]
         L.tq2_matvec_workspace_size.argtypes = [I64, I64, I64]
         L.tq2_matvec_workspace_size.restype = SZ
         L.tq2_status_string.argtypes = [I32]
@@ -80,7 +81,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
                    "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_matvec_grouped_requant", "tq2_gemm",
                    "tq2_affine4_matvec",
-                   "tq2_test_matvec_stall", "tq2_version"):
+                   "tq2_test_matvec_stall", "tq2_test_gemm_stall", "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
         return L
@@ -317,6 +318,27 @@ def test_matvec_stall(x, qs, d, status, stall_stage: int, wait_limit_us: int, y=
     _check(load().tq2_test_matvec_stall(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), _ptr(status),
                                         _stream_ptr(stream), int(stall_stage), int(wait_limit_us)),
            "tq2_test_matvec_stall")
+    return y
+
+
+def test_gemm_stall(x, qs, d, status, stall_stage: int, wait_limit_us: int, act_scale: float = 0.0, y=None,
+                    stream=None):
+    """Test hook (tq2_test_gemm_stall): the tcgen05 GEMM with one x stage's
+    copy skipped in every CTA and the stage-ring waits limited to
+    wait_limit_us, so that its timeout path runs.  Not part of the product."""
+    torch = _torch()
+    M, K = x.shape
+    N = qs.shape[0]
+    if x.dtype != torch.float16 or d.dtype != torch.float16 or qs.dtype != torch.uint8:
+        raise TypeError("x and d must be float16, qs uint8")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=qs.device)
+    if y.dtype != torch.float32:
+        raise TypeError("y must be float32")
+    _need_cuda(x, qs, d, y, status)
+    _check(load().tq2_test_gemm_stall(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), float(act_scale), _ptr(status),
+                                      _stream_ptr(stream), int(stall_stage), int(wait_limit_us)),
+           "tq2_test_gemm_stall")
     return y
 
 

@@ -356,9 +356,13 @@ tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, i
     return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, out_scale, d_status, stream);
 }
 
-tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
-                    void *y, tq2_dtype y_dtype, float act_scale, float out_scale, uint32_t *d_status,
-                    tq2_stream_t stream, int impl)
+}  // extern "C"
+
+namespace {
+
+tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
+                       void *y, tq2_dtype y_dtype, float act_scale, float out_scale, uint32_t *d_status,
+                       tq2_stream_t stream, int impl, int stall_stage = -1, unsigned long long wait_limit_ns = 0)
 {
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
@@ -401,6 +405,8 @@ tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint1
         a.out_scale = out_scale;
         a.inv_out = out_scale != 0.0f ? 1.0f / out_scale : 0.0f;
         a.stream = s;
+        a.stall_stage = stall_stage;
+        a.wait_limit_ns = wait_limit_ns;
         cudaError_t e = tq2::launch_gemm_tc05(a, dev);
         if (e == cudaSuccess) e = cudaGetLastError();
         return from_cuda(e);
@@ -412,6 +418,28 @@ tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint1
         if (st != TQ2_OK) return st;
     }
     return TQ2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
+                    void *y, tq2_dtype y_dtype, float act_scale, float out_scale, uint32_t *d_status,
+                    tq2_stream_t stream, int impl)
+{
+    return gemm_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, d_status, stream, impl);
+}
+
+tq2_status tq2_test_gemm_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
+                               int64_t K, float *y, float act_scale, uint32_t *d_status, tq2_stream_t stream,
+                               int stall_stage, int wait_limit_us)
+{
+    if (stall_stage < 0) return TQ2_ERR_ARG;
+    if (wait_limit_us < 1 || wait_limit_us > 200000) return TQ2_ERR_ARG;
+    if (d_status == nullptr) return TQ2_ERR_NULL;
+    return gemm_common(x, M, qs, d, N, K, y, TQ2_F32, act_scale, 0.0f, d_status, stream, 1, stall_stage,
+                       (unsigned long long)wait_limit_us * 1000ull);
 }
 
 tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *s,

@@ -104,13 +104,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait_cluster_for(uint32_t bar, uint32_t parity, unsigned long long limit_ns)
 {
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait_cluster_for(bar, parity, kTimeoutNs);
 }
 
 // For short producer/consumer hand-offs: spin on the non-blocking test

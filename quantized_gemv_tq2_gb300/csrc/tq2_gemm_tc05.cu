@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     // reserves the slack; both rings move together)
     const uint32_t wring = (smem_addr(smem + p.off_w) + 1023u) & ~1023u;
     const uint32_t bring = (smem_addr(smem + p.off_b) + 1023u) & ~1023u;
+    // limit of the stage-ring waits (the completion, tensor-memory and
+    // cluster hand-off waits keep kTimeoutNs, so that a short test limit
+    // never lets a CTA leave while its peers or its MMAs still need it)
+    const unsigned long long lim = p.a.wait_limit_ns ? p.a.wait_limit_ns : kTimeoutNs;
 
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         int issued = 0;
         for (int s = 0; s < nwst; ++s) {
             const int slot = s % SW, round = s / SW;
-            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(wempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait_for(wempty0 + 8u * slot, (uint32_t)((round - 1) & 1), lim))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 break;
             }
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         }
         for (int slot = 0; slot < SW && slot < issued; ++slot) {  // no copy in flight at exit
             const int last = slot + ((issued - 1 - slot) / SW) * SW;
-            if (!mbar_wait(wfull0 + 8u * slot, (uint32_t)((last / SW) & 1)) && lane == 0) report_timeout(p, abort_flag);
+            if (!mbar_wait_for(wfull0 + 8u * slot, (uint32_t)((last / SW) & 1), lim) && lane == 0) report_timeout(p, abort_flag);
         }
         return;
     }
@@ -211,11 +215,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         int issued = 0;
         for (int s = 0; s < nbst; ++s) {
             const int slot = s % SB, round = s / SB;
-            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(sempty0 + 8u * slot, (uint32_t)((round - 1) & 1)))) {
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait_for(sempty0 + 8u * slot, (uint32_t)((round - 1) & 1), lim))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            if (s == p.a.stall_stage) {  // test hook: no copy for this stage
+                issued = s + 1;
+                continue;
+            }
             const uint32_t full = bfull0 + 8u * slot;
             if (lane == 0) mbar_arrive_expect_tx(full, kBStageBytes);
             __syncwarp();
@@ -225,9 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             __syncwarp();
             issued = s + 1;
         }
+        // (a slot is refilled only after the MMAs that read its previous
+        // stage completed, so only its last copy can be in flight; a skipped
+        // stage had none: its slot's last copy is the one before it)
         for (int slot = 0; slot < SB && slot < issued; ++slot) {
-            const int last = slot + ((issued - 1 - slot) / SB) * SB;
-            if (!mbar_wait(bfull0 + 8u * slot, (uint32_t)((last / SB) & 1)) && lane == 0) report_timeout(p, abort_flag);
+            int last = slot + ((issued - 1 - slot) / SB) * SB;
+            if (last == p.a.stall_stage) last -= SB;
+            if (last >= 0 && !mbar_wait_for(bfull0 + 8u * slot, (uint32_t)((last / SB) & 1), lim) && lane == 0)
+                report_timeout(p, abort_flag);
         }
         return;
     }
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             for (int g = 0; g < ngroups; ++g) {
                 const int r = g % SB;
                 const uint32_t par = (uint32_t)((g / SB) & 1);
-                if (!mbar_wait(afull0 + 8u * r, par) || !mbar_wait((prologue ? bconv0 : bfull0) + 8u * r, par)) {
+                if (!mbar_wait_for(afull0 + 8u * r, par, lim) || !mbar_wait_for((prologue ? bconv0 : bfull0) + 8u * r, par, lim)) {
                     report_timeout(p, abort_flag);
                     break;
                 }
@@ -309,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 // the prologue
                 const int r = g % SB;
                 if (alive &&
-                    !__all_sync(0xffffffffu, mbar_wait(bfull0 + 8u * (uint32_t)r, (uint32_t)((g / SB) & 1)))) {
+                    !__all_sync(0xffffffffu, mbar_wait_for(bfull0 + 8u * (uint32_t)r, (uint32_t)((g / SB) & 1), lim))) {
                     if (lane == 0) report_timeout(p, abort_flag);
                     alive = false;
                 }
@@ -339,14 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             if (ws != cur_w) {
                 if (alive && cur_w >= 0 && lane == 0) mbar_arrive(wempty0 + 8u * (cur_w % SW));
                 cur_w = ws;
-                if (alive && !__all_sync(0xffffffffu, mbar_wait(wfull0 + 8u * slot, (uint32_t)((ws / SW) & 1)))) {
+                if (alive && !__all_sync(0xffffffffu, mbar_wait_for(wfull0 + 8u * slot, (uint32_t)((ws / SW) & 1), lim))) {
                     if (lane == 0) report_timeout(p, abort_flag);
                     alive = false;
                 }
             }
             const int a = g % SB;  // stage slot: TMEM A slot a
             if (alive && g >= SB &&
-                !__all_sync(0xffffffffu, mbar_wait(sempty0 + 8u * a, (uint32_t)(((g / SB) - 1) & 1)))) {
+                !__all_sync(0xffffffffu, mbar_wait_for(sempty0 + 8u * a, (uint32_t)(((g / SB) - 1) & 1), lim))) {
                 if (lane == 0) report_timeout(p, abort_flag);
                 alive = false;
             }

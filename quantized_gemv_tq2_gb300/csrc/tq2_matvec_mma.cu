@@ -82,10 +82,8 @@ struct GroupMat {
     float inv_out;       // fp32(1/out_scale)
 };
 
-struct MmaParams {
-    // K > 4096 only: each matrix's qs as a 2-D tensor of uint64 [N][K/32],
-    // boxes of 128 x {16, 8, 4, 2, 1} rows
-    CUtensorMap tmap[kMaxGroup][5];  // 64-byte aligned by its type
+// The launch plan: arguments, grid and shared-memory layout.
+struct MmaPlan {
     MatvecArgs a;
     int tma2d;       // 0: 1-D bulk copies of whole rows; 1: 2-D tensor boxes
     int G;           // CTAs; CTA i owns rows [i*N/G, (i+1)*N/G)
@@ -100,7 +98,17 @@ struct MmaParams {
     int dstr;        // fp32 stride of the d slice rows (B + 1, odd)
     int off_bar, off_red, off_dsm, off_xsum, off_xs, off_ring, smem_total;
     int n_mats;
-    GroupMat mats[kMaxGroup];
+};
+
+// Kernel parameters for up to kG matrices with kT sets of tensor maps (1, or
+// kG for a group at K > 4096): every launch copies its parameters, so a
+// single call carries one matrix and a group without 2-D boxes one map set.
+template <int kG, int kT>
+struct MmaParams : MmaPlan {
+    // K > 4096 only: each matrix's qs as a 2-D tensor of uint64 [N][K/32],
+    // boxes of 128 x {16, 8, 4, 2, 1} rows
+    CUtensorMap tmap[kT][5];  // 64-byte aligned by its type
+    GroupMat mats[kG];
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -118,16 +126,19 @@ __device__ __forceinline__ void consumer_barrier()
             mma_16816(C, w0 & (MASK), w1 & (MASK), s0 & (MASK), s1 & (MASK), b0, b1);          \
     } while (0)
 
-__device__ __forceinline__ void report_timeout(const MmaParams &p, volatile int *abort_flag)
+__device__ __forceinline__ void report_timeout(const MmaPlan &p, volatile int *abort_flag)
 {
     *abort_flag = 1;
     if (p.a.status) atomicOr(p.a.status, TQ2_FLAG_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ kernel
-template <int kM>
+// kHook: the test instantiation (a per-call wait limit and a stage whose copy
+// the producer skips, MatvecArgs::wait_limit_ns / stall_stage); product
+// launches use kHook = false, with the constant limit and no stall check.
+template <int kM, int kG, int kT, bool kHook>
 __global__ void __launch_bounds__(kMmaThreads, 2)
-matvec_mma_kernel(const __grid_constant__ MmaParams p)
+matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int abort_shared;
@@ -136,7 +147,8 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // this CTA's matrix and rows
     int mi = 0;
-    while (mi + 1 < p.n_mats && (int)blockIdx.x >= p.mats[mi + 1].g0) ++mi;
+    if constexpr (kG > 1)
+        while (mi + 1 < p.n_mats && (int)blockIdx.x >= p.mats[mi + 1].g0) ++mi;
     const uint8_t *const qs_g = p.mats[mi].qs;
     const uint16_t *const d_g = p.mats[mi].d;
     void *const y_g = p.mats[mi].y;
@@ -151,7 +163,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // full[S], empty[S]
     uint8_t *ring = smem + p.off_ring;
-    const unsigned long long lim = p.a.wait_limit_ns ? p.a.wait_limit_ns : kTimeoutNs;
+    const unsigned long long lim = (kHook && p.a.wait_limit_ns) ? p.a.wait_limit_ns : kTimeoutNs;
 
     // Let the next kernel in the stream start its own weight prefetch.
     asm volatile("griddepcontrol.launch_dependents;");
@@ -181,7 +193,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            if (s == p.a.stall_stage) {  // test hook: no copy for this stage
+            if (kHook && s == p.a.stall_stage) {  // test hook: no copy for this stage
                 issued = s + 1;
                 continue;
             }
@@ -205,14 +217,15 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
                 const int y0 = (int)(r0 + rg0 * 16);
                 const int x = kc * 128;
                 if (rows == 16) {
-                    if (lane == 0) tensor2d_g2s(dst0, &p.tmap[mi][0], x, y0, full, pol);
+                    if (lane == 0) tensor2d_g2s(dst0, &p.tmap[kT > 1 ? mi : 0][0], x, y0, full, pol);
                 } else {
                     int roff = 0, box = 0;
 #pragma unroll
                     for (int i = 1; i < 5; ++i) {
                         const int h = 16 >> i;
                         if (rows & h) {
-                            if (lane == box) tensor2d_g2s(dst0 + roff * 1024, &p.tmap[mi][i], x, y0 + roff, full, pol);
+                            if (lane == box)
+                                tensor2d_g2s(dst0 + roff * 1024, &p.tmap[kT > 1 ? mi : 0][i], x, y0 + roff, full, pol);
                             roff += h;
                             ++box;
                         }
@@ -229,7 +242,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams p)
         // copy is the one before it.)
         for (int slot = 0; slot < S && slot < issued; ++slot) {
             int last = slot + ((issued - 1 - slot) / S) * S;
-            if (last == p.a.stall_stage) last -= S;
+            if (kHook && last == p.a.stall_stage) last -= S;
             if (last >= 0 && !mbar_wait_for(smem_addr(&bars[slot]), (last / S) & 1, lim) && lane == 0)
                 report_timeout(p, abort_flag);
         }
@@ -759,7 +772,7 @@ static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Shared-memory plan for G CTAs within max_dyn bytes of dynamic shared
 // memory; returns false if it cannot fit.
-bool make_plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, MmaParams &p)
+bool make_plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, MmaPlan &p)
 {
     const int kMaxSmem = max_dyn;
     const int64_t B = K / 256;
@@ -807,7 +820,7 @@ bool make_plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, MmaParams &
     return p.smem_total <= kMaxSmem;
 }
 
-bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaParams &p)
+bool make_plan(int M, int64_t N, int64_t K, int G, int max_dyn, MmaPlan &p)
 {
     p.G = G;
     return make_plan_rows(M, (N + G - 1) / G, K, max_dyn, p);
@@ -827,13 +840,16 @@ int max_dynamic_smem(int device)
     int optin = 0;
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, matvec_mma_kernel<kM>) != cudaSuccess) {
+        cudaFuncGetAttributes(&fa, matvec_mma_kernel<kM, 1, 1, false>) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
-    v = optin - (int)fa.sharedSizeBytes;
-    if (cudaFuncSetAttribute(matvec_mma_kernel<kM>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) !=
-        cudaSuccess) {
+    v = optin - (int)fa.sharedSizeBytes;  // the same static shared memory for both instantiations
+    const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(matvec_mma_kernel<kM, 1, 1, false>, attr, v) != cudaSuccess ||
+        cudaFuncSetAttribute(matvec_mma_kernel<kM, 1, 1, true>, attr, v) != cudaSuccess ||
+        cudaFuncSetAttribute(matvec_mma_kernel<kM, kMaxGroup, 1, false>, attr, v) != cudaSuccess ||
+        cudaFuncSetAttribute(matvec_mma_kernel<kM, kMaxGroup, kMaxGroup, false>, attr, v) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -842,7 +858,7 @@ int max_dynamic_smem(int device)
 }
 
 // Grid and plan: one CTA per SM while the per-CTA share fits, more CTAs otherwise.
-bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaParams &p)
+bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaPlan &p)
 {
     if (max_dyn <= 0) return false;
     int G = (int)((N < (int64_t)sm_count(device)) ? N : sm_count(device));
@@ -856,7 +872,8 @@ bool plan_for(int M, int64_t N, int64_t K, int device, int max_dyn, MmaParams &p
 // CTAs of a group in proportion to the matrices' rows (at least one each,
 // at most one per SM in total while that fits), then the shared-memory plan
 // for the largest per-CTA row count.
-bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, int max_dyn, MmaParams &p)
+template <int kT>
+bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, int max_dyn, MmaParams<kMaxGroup, kT> &p)
 {
     if (max_dyn <= 0 || n < 1 || n > kMaxGroup) return false;
     int64_t total = 0;
@@ -924,7 +941,7 @@ cudaError_t encode_qs_maps(const uint8_t *qs, int64_t N, int64_t K, CUtensorMap 
 template <int kM>
 cudaError_t launch_impl(const MatvecArgs &a, int device)
 {
-    MmaParams p{};
+    MmaParams<1, 1> p{};
     p.a = a;
     if (!plan_for(kM, a.N, a.K, device, max_dynamic_smem<kM>(device), p))
         return cudaErrorInvalidConfiguration;
@@ -934,7 +951,8 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
         cudaError_t e = encode_qs_maps(a.qs, a.N, a.K, p.tmap[0]);
         if (e != cudaSuccess) return e;
     }
-    auto kern = matvec_mma_kernel<kM>;
+    const bool hook = a.stall_stage >= 0 || a.wait_limit_ns != 0;
+    auto kern = hook ? matvec_mma_kernel<kM, 1, 1, true> : matvec_mma_kernel<kM, 1, 1, false>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.G);
     cfg.blockDim = dim3(kMmaThreads);
@@ -948,14 +966,14 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int kM>
-cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
-                              void *const *y, const int64_t *N, const float *out_scale, const float *inv_out,
-                              int device)
+template <int kM, int kT>
+cudaError_t launch_group_kt(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                            void *const *y, const int64_t *N, const float *out_scale, const float *inv_out,
+                            int device, int max_dyn)
 {
-    MmaParams p{};
+    MmaParams<kMaxGroup, kT> p{};
     p.a = a;
-    if (!group_plan(kM, n, N, a.K, device, max_dynamic_smem<kM>(device), p)) return cudaErrorInvalidConfiguration;
+    if (!group_plan(kM, n, N, a.K, device, max_dyn, p)) return cudaErrorInvalidConfiguration;
     for (int j = 0; j < n; ++j) {
         p.mats[j].qs = qs[j];
         p.mats[j].d = d[j];
@@ -963,7 +981,8 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
         p.mats[j].out_scale = out_scale ? out_scale[j] : 0.0f;
         p.mats[j].inv_out = inv_out ? inv_out[j] : 0.0f;
         if (p.tma2d) {
-            cudaError_t e = encode_qs_maps(qs[j], N[j], a.K, p.tmap[j]);
+            if (kT < kMaxGroup) return cudaErrorInvalidConfiguration;  // not reached: see the caller
+            cudaError_t e = encode_qs_maps(qs[j], N[j], a.K, p.tmap[kT > 1 ? j : 0]);
             if (e != cudaSuccess) return e;
         }
     }
@@ -977,7 +996,19 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<kM>, p);
+    return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<kM, kMaxGroup, kT, false>, p);
+}
+
+// One map set unless the plan uses 2-D boxes (K > 4096).
+template <int kM>
+cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *qs, const uint16_t *const *d,
+                              void *const *y, const int64_t *N, const float *out_scale, const float *inv_out,
+                              int device)
+{
+    const int max_dyn = max_dynamic_smem<kM>(device);
+    if (a.K > 256 * kChunkBlocks)
+        return launch_group_kt<kM, kMaxGroup>(a, n, qs, d, y, N, out_scale, inv_out, device, max_dyn);
+    return launch_group_kt<kM, 1>(a, n, qs, d, y, N, out_scale, inv_out, device, max_dyn);
 }
 
 }  // namespace
@@ -985,7 +1016,7 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
 bool mma_group_supported(int M, int n, const int64_t *N, int64_t K, int device)
 {
     if (M < 1 || M > 2 || K < 256) return false;
-    MmaParams p{};
+    MmaParams<kMaxGroup, 1> p{};
     const int max_dyn = (M == 1) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
     return group_plan(M, n, N, K, device, max_dyn, p);
 }
@@ -1002,7 +1033,7 @@ cudaError_t launch_matvec_mma_group(const MatvecArgs &a, int n, const uint8_t *c
 bool mma_matvec_supported(int M, int64_t N, int64_t K, int device)
 {
     if (M < 1 || M > 2 || N < 1 || K < 256) return false;
-    MmaParams p{};
+    MmaPlan p{};
     const int max_dyn = (M == 1) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
     return plan_for(M, N, K, device, max_dyn, p);
 }

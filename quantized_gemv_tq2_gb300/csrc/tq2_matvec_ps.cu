@@ -69,9 +69,8 @@ struct PsMat {
     float inv_out;       // fp32(1/out_scale)
 };
 
-struct PsParams {
-    // each matrix's qs as uint64 [N][K/32], boxes (kcb*8) x {16, 8, 4, 2, 1} rows
-    CUtensorMap tmap[kMaxGroup][5];
+// The launch plan: arguments, grid and shared-memory layout.
+struct PsPlan {
     MatvecArgs a;
     int G;        // CTAs
     int B;        // 256-blocks along K
@@ -88,7 +87,15 @@ struct PsParams {
     int xblocks;  // 256-blocks per x chunk (kcb * xkc)
     int off_bar, off_red, off_dsm, off_xinfo, off_frag, off_ring, smem_total;
     int n_mats;
-    PsMat mats[kMaxGroup];
+};
+
+// Kernel parameters for up to kG matrices (1 for a single call, so that its
+// parameters stay small: every launch copies them).
+template <int kG>
+struct PsParams : PsPlan {
+    // each matrix's qs as uint64 [N][K/32], boxes (kcb*8) x {16, 8, 4, 2, 1} rows
+    CUtensorMap tmap[kG][5];
+    PsMat mats[kG];
 };
 
 __device__ __forceinline__ void consumers_sync()
@@ -96,7 +103,7 @@ __device__ __forceinline__ void consumers_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
-__device__ __forceinline__ void report_timeout(const PsParams &p, volatile int *abort_flag)
+__device__ __forceinline__ void report_timeout(const PsPlan &p, volatile int *abort_flag)
 {
     *abort_flag = 1;
     if (p.a.status) atomicOr(p.a.status, TQ2_FLAG_TIMEOUT);
@@ -138,7 +145,7 @@ __device__ __forceinline__ uint32_t frag_off(int bx, int nt, int jw, int h, int 
 // B entry (both halves, all four classes), so no value crosses lanes; the
 // block sum and the "big" test are half-warp reductions.
 template <int NT>
-__device__ __forceinline__ void stage_x(const PsParams &p, int kb0, int nbx, uint32_t frag, float2 *xinfo,
+__device__ __forceinline__ void stage_x(const PsPlan &p, int kb0, int nbx, uint32_t frag, float2 *xinfo,
                                         int warp, int lane)
 {
     const int M = p.a.M;
@@ -263,8 +270,8 @@ __device__ __forceinline__ void unit_mma(float (&c)[4], const uint32_t (&wa)[4],
     for (int i = 0; i < 4; ++i) c[i] = ca[i] + cb[i];
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(const __grid_constant__ PsParams p)
+template <int NT, int kG>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(const __grid_constant__ PsParams<kG> p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int abort_shared;
@@ -274,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     const int M = p.a.M;
     // this CTA's matrix and rows
     int mi = 0;
-    while (mi + 1 < p.n_mats && (int)blockIdx.x >= p.mats[mi + 1].g0) ++mi;
+    if constexpr (kG > 1)
+        while (mi + 1 < p.n_mats && (int)blockIdx.x >= p.mats[mi + 1].g0) ++mi;
     const uint8_t *const qs_g = p.mats[mi].qs;
     const uint16_t *const d_g = p.mats[mi].d;
     void *const y_g = p.mats[mi].y;
@@ -452,15 +460,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     const bool fast = p.n_kc == 1 && p.R == 1 && p.kcb == 16 && p.xkc == 1;
     if (fast) {
         constexpr int kU = 16 / kWarps;  // blocks per warp and stage
-        uint32_t fbu[kU], au[kU], du[kU], xiu[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int b = warp + u * kWarps;
-            fbu[u] = frag + (uint32_t)(b * 512 * M);
-            au[u] = ring_thr + (uint32_t)(b * 64);
-            du[u] = smem_addr(dsm) + (uint32_t)(g * p.dstr + b) * 4u;
-            xiu[u] = smem_addr(xinfo) + (uint32_t)(b * 8 * NT + 2 * t) * 8u;  // + 64 per n-tile
-        }
+        // shared-memory bases of block warp + u * kWarps, recomputed from the
+        // u = 0 ones at each use (holding all of them spills registers)
+        const uint32_t fb0 = frag + (uint32_t)(warp * 512 * M), fb_step = (uint32_t)(kWarps * 512 * M);
+        const uint32_t au0 = ring_thr + (uint32_t)(warp * 64);
+        const uint32_t du0 = smem_addr(dsm) + (uint32_t)(g * p.dstr + warp) * 4u;
+        const uint32_t xi0 = smem_addr(xinfo) + (uint32_t)(warp * 8 * NT + 2 * t) * 8u;  // + 64 per n-tile
+#define fbu(u) (fb0 + (uint32_t)(u) * fb_step)
+#define au(u) (au0 + (uint32_t)((u) * kWarps * 64))
+#define du(u) (du0 + (uint32_t)((u) * kWarps * 4))
+#define xiu(u) (xi0 + (uint32_t)((u) * kWarps * 8 * NT * 8))
         uint32_t h1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) h1[nt] = (uint32_t)(64 * min(8, M - 8 * nt));
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #define TQ2_PS_LOAD_CODES(SL)                                                              \
         do {                                                                               \
             _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
-                const uint32_t pa_ = au[u_] + (uint32_t)((SL) * p.stage_bytes);           \
+                const uint32_t pa_ = au(u_) + (uint32_t)((SL) * p.stage_bytes);           \
                 const uint4 va_ = lds128(pa_), vb_ = lds128(pa_ + a_half);                 \
                 W[u_][0] = va_.x; W[u_][1] = va_.y; W[u_][2] = va_.z; W[u_][3] = va_.w;    \
                 V[u_][0] = vb_.x; V[u_][1] = vb_.y; V[u_][2] = vb_.z; V[u_][3] = vb_.w;    \
@@ -482,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #define TQ2_PS_LOAD_SCALES(RG)                                                             \
         do {                                                                               \
             _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
-                dg[u_] = lds_f32(du[u_] + (uint32_t)(RG) * d_rg);                          \
-                dg8[u_] = lds_f32(du[u_] + (uint32_t)(RG) * d_rg + d_half);                \
+                dg[u_] = lds_f32(du(u_) + (uint32_t)(RG) * d_rg);                          \
+                dg8[u_] = lds_f32(du(u_) + (uint32_t)(RG) * d_rg + d_half);                \
             }                                                                              \
         } while (0)
         int sl = 0, ph = 0;
@@ -507,15 +516,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
                     float4 xi;
                     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
                                  : "=f"(xi.x), "=f"(xi.y), "=f"(xi.z), "=f"(xi.w)
-                                 : "r"(xiu[u] + (uint32_t)(64 * nt)));
+                                 : "r"(xiu(u) + (uint32_t)(64 * nt)));
                     float c0[4] = {xi.x, xi.z, xi.x, xi.z};
                     float c1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c2[4] = {0.0f, 0.0f, 0.0f, 0.0f},
                           c3[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int jw = 0; jw < 4; ++jw) {
                         const uint32_t w0 = W[u][jw], w1 = V[u][jw], s0 = w0 >> 8, s1 = w1 >> 8;
-                        const uint4 f0 = lds128(fbu[u] + xo[nt][jw]);
-                        const uint4 f1 = lds128(fbu[u] + xo[nt][jw] + h1[nt]);
+                        const uint4 f0 = lds128(fbu(u) + xo[nt][jw]);
+                        const uint4 f1 = lds128(fbu(u) + xo[nt][jw] + h1[nt]);
                         mma_16816(c0, w0 & 0x00030003u, w1 & 0x00030003u, s0 & 0x00030003u, s1 & 0x00030003u, f0.x, f0.y);
                         mma_16816(c1, w0 & 0x000C000Cu, w1 & 0x000C000Cu, s0 & 0x000C000Cu, s1 & 0x000C000Cu, f0.z, f0.w);
                         mma_16816(c2, w0 & 0x00300030u, w1 & 0x00300030u, s0 & 0x00300030u, s1 & 0x00300030u, f1.x, f1.y);
@@ -557,6 +566,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
         }
 #undef TQ2_PS_LOAD_CODES
 #undef TQ2_PS_LOAD_SCALES
+#undef fbu
+#undef au
+#undef du
+#undef xiu
     } else {
     int slot = 0, phase = 0;
     int xc = 0, rgi = 0, kci = 0;
@@ -664,7 +677,7 @@ int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Shared-memory plan for CTAs of at most max_rows rows within `cap` bytes;
 // false if it cannot fit.
-bool make_plan(int M, int64_t max_rows, int64_t K, int cap, bool resident, int kcb_try, PsParams &p)
+bool make_plan(int M, int64_t max_rows, int64_t K, int cap, bool resident, int kcb_try, PsPlan &p)
 {
     const int64_t B = K / 256;
     if (B < 1 || B > (1 << 20)) return false;
@@ -731,12 +744,14 @@ int max_dynamic_smem(int device)
     int optin = 0;
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, matvec_ps_kernel<NT>) != cudaSuccess) {
+        cudaFuncGetAttributes(&fa, matvec_ps_kernel<NT, 1>) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     v = optin - (int)fa.sharedSizeBytes;
-    if (cudaFuncSetAttribute(matvec_ps_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) !=
+    if (cudaFuncSetAttribute(matvec_ps_kernel<NT, kMaxGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(matvec_ps_kernel<NT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -753,7 +768,7 @@ int max_dynamic_smem(int device)
 // 18.9 against 16.4 / 18.3 / 19.7 us; gate/up 16384x4096 at M = 7 / 8: 14.2
 // / 18.7 against 14.7 / 19.0 us): K-chunked x is re-staged per K range
 // behind two barriers that drain the stage ring.
-bool plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, PsParams &p)
+bool plan_rows(int M, int64_t max_rows, int64_t K, int max_dyn, PsPlan &p)
 {
     for (int cap : {kTwoPerSm, max_dyn}) {
         if (cap > max_dyn) continue;
@@ -772,7 +787,7 @@ int max_dyn_for(int M, int device)
     return (M <= 8) ? max_dynamic_smem<1>(device) : max_dynamic_smem<2>(device);
 }
 
-bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
+bool plan_for(int M, int64_t N, int64_t K, int device, PsPlan &p)
 {
     const int max_dyn = max_dyn_for(M, device);
     if (max_dyn <= 0 || M < 1 || M > 16) return false;
@@ -782,9 +797,6 @@ bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
         if (plan_rows(M, (N + G - 1) / G, K, max_dyn, p)) {
             p.G = G;
             p.n_mats = 1;
-            p.mats[0].N = N;
-            p.mats[0].g0 = 0;
-            p.mats[0].G = G;
             return true;
         }
         if (G >= N) return false;
@@ -795,7 +807,7 @@ bool plan_for(int M, int64_t N, int64_t K, int device, PsParams &p)
 // CTAs of a group in proportion to the matrices' rows (at least one each,
 // one per SM in total first, then twice as many while no plan fits), then
 // the plan for the largest per-CTA row count.
-bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, PsParams &p)
+bool group_plan(int M, int n, const int64_t *N, int64_t K, int device, PsParams<kMaxGroup> &p)
 {
     const int max_dyn = max_dyn_for(M, device);
     if (max_dyn <= 0 || M < 1 || M > 16 || n < 1 || n > kMaxGroup) return false;
@@ -862,8 +874,8 @@ cudaError_t encode_maps(const uint8_t *qs, int64_t N, int64_t K, int kcb, CUtens
     return cudaSuccess;
 }
 
-template <int NT>
-cudaError_t launch_params(const PsParams &p, cudaStream_t stream)
+template <int NT, int kG>
+cudaError_t launch_params(const PsParams<kG> &p, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.G);
@@ -875,15 +887,18 @@ cudaError_t launch_params(const PsParams &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, matvec_ps_kernel<NT>, p);
+    return cudaLaunchKernelEx(&cfg, matvec_ps_kernel<NT, kG>, p);
 }
 
 template <int NT>
 cudaError_t launch_impl(const MatvecArgs &a, int device)
 {
-    PsParams p{};
+    PsParams<1> p{};
     p.a = a;
     if (!plan_for(a.M, a.N, a.K, device, p)) return cudaErrorInvalidConfiguration;
+    p.mats[0].N = a.N;
+    p.mats[0].g0 = 0;
+    p.mats[0].G = p.G;
     p.mats[0].qs = a.qs;
     p.mats[0].d = a.d;
     p.mats[0].y = a.y;
@@ -893,7 +908,7 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
         cudaError_t e = encode_maps(a.qs, a.N, a.K, p.kcb, p.tmap[0]);
         if (e != cudaSuccess) return e;
     }
-    return launch_params<NT>(p, a.stream);
+    return launch_params<NT, 1>(p, a.stream);
 }
 
 template <int NT>
@@ -901,7 +916,7 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
                               void *const *y, const int64_t *N, const float *out_scale, const float *inv_out,
                               int device)
 {
-    PsParams p{};
+    PsParams<kMaxGroup> p{};
     p.a = a;
     if (!group_plan(a.M, n, N, a.K, device, p)) return cudaErrorInvalidConfiguration;
     for (int j = 0; j < n; ++j) {
@@ -915,7 +930,7 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
             if (e != cudaSuccess) return e;
         }
     }
-    return launch_params<NT>(p, a.stream);
+    return launch_params<NT, kMaxGroup>(p, a.stream);
 }
 
 }  // namespace
@@ -923,14 +938,14 @@ cudaError_t launch_group_impl(const MatvecArgs &a, int n, const uint8_t *const *
 bool ps_matvec_supported(int M, int64_t N, int64_t K, int device)
 {
     if (M < 1 || M > 16 || N < 1 || K < 256) return false;
-    PsParams p{};
+    PsPlan p{};
     return plan_for(M, N, K, device, p);
 }
 
 bool ps_group_supported(int M, int n, const int64_t *N, int64_t K, int device)
 {
     if (M < 1 || M > 16 || K < 256) return false;
-    PsParams p{};
+    PsParams<kMaxGroup> p{};
     return group_plan(M, n, N, K, device, p);
 }
 

@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
                           "tq2_matvec_impl", "tq2_matvec_requant", "tq2_gemm",
                           "tq2_affine4_matvec", "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version",
-                          "tq2_test_matvec_stall", "tq2_matvec_grouped_requant"}
+                          "tq2_test_matvec_stall", "tq2_matvec_grouped_requant", "tq2_test_gemm_stall"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
 
@@ -135,6 +135,19 @@ def test_stall_hook_rejects_bad_arguments(L):
     assert stall(M=17) == SHAPE
     assert stall(M=3) == ARG      # impl 1 takes M <= 2
     assert stall(y=A2) == ALIGN   # fp32 y
+    assert stall(M=0, x=NUL, y=NUL) == OK
+
+
+def test_gemm_stall_hook_rejects_bad_arguments(L):
+    def stall(x=A16, M=16, qs=A16, d=A16, N=128, K=512, y=A16, s=0.0, st=A16, stage=0, lim=100):
+        return L.tq2_test_gemm_stall(x, M, qs, d, N, K, y, s, st, S, stage, lim)
+    assert stall(stage=-1) == ARG
+    assert stall(lim=0) == ARG
+    assert stall(lim=200001) == ARG
+    assert stall(st=NUL) == NULL
+    assert stall(K=300) == SHAPE
+    assert stall(s=-1.0) == ARG
+    assert stall(y=A2) == ALIGN
     assert stall(M=0, x=NUL, y=NUL) == OK
 
 

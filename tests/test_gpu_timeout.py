@@ -85,3 +85,36 @@ def test_stall_argument_checks(T):
         tq2.test_matvec_stall(dev(case.x).view(1, -1).repeat(3, 1), qs, d, st, stall_stage=0,
                               wait_limit_us=100)
     assert e.value.status == 5  # M = 3: impl 1 takes M <= 2
+
+
+# The tcgen05 GEMM: (M, N, K, stall stages) with the CTA's x stages counted
+# within its share of K -- one CTA per 128-row tile and all of K (8 stages),
+# split K over clusters of 8 CTAs (the partial-sum hand-off; 4 stages each),
+# and two activation tiles over clusters of 4 (2 stages each).
+@pytest.mark.parametrize("M,N,K,stages", [
+    (16, 16384, 1024, (0, 1, 7)),
+    (16, 512, 4096, (0, 1, 3)),
+    (200, 2048, 1024, (0, 1)),
+])
+@pytest.mark.parametrize("prologue", [False, True])
+def test_gemm_stall_reports_timeout_then_recovers(T, M, N, K, stages, prologue):
+    import quantized_gemv_tq2_gb300 as tq2
+    case = Case(seed=7300 + M + K // 256, M=M, N=N, K=K, heavy=prologue, prologue=prologue)
+    x, qs, d = case.device()
+    rows = sample_rows(N, 64, seed=M)
+    y_ref, tol = case.reference(rows)
+    for stall in stages:
+        st = T.zeros(1, dtype=T.int32, device="cuda")
+        out = GuardedOutput(M, N)
+        tq2.test_gemm_stall(x, qs, d, st, stall_stage=stall, wait_limit_us=LIMIT_US, act_scale=case.s, y=out.y)
+        T.cuda.synchronize()  # raises if the context was lost
+        assert int(st.item()) & TQ2_FLAG_TIMEOUT, f"stage {stall}: no timeout reported"
+        out.check(f"gemm stall {stall}")
+        if stall == 0:  # every CTA has a stage 0: no CTA may have stored y
+            assert bool(T.all(out.y.view(T.int32) == out.canary)), "y written after a timeout"
+        st2 = T.zeros(1, dtype=T.int32, device="cuda")
+        y = tq2.gemm(x, qs, d, act_scale=case.s, status=st2, impl=1)
+        T.cuda.synchronize()
+        assert int(st2.item()) == 0
+        assert_within_tolerance(host(y).astype(np.float64)[:, rows], y_ref, tol,
+                                f"gemm M={M} {N}x{K} after stall {stall}")
