@@ -415,6 +415,58 @@ def cpu_info():
     return cores, model
 
 
+def run_manifest(torch, st):
+    """What produced this line: the source tree and input hashes, the seed,
+    the GPU, driver, toolkit and library versions, and the host CPU."""
+    import glob
+    import hashlib
+    import platform
+
+    def run(cmd):
+        try:
+            return subprocess.run(cmd, capture_output=True, text=True, timeout=20, cwd=ROOT).stdout.strip()
+        except Exception:
+            return None
+
+    src = hashlib.sha256()
+    pkg = os.path.join(ROOT, "quantized_gemv_tq2_gb300")
+    files = sorted(glob.glob(os.path.join(pkg, "csrc", "*")) + [os.path.join(ROOT, "include", "tq2.h"),
+                   os.path.join(pkg, "__init__.py"), os.path.join(pkg, "build.py"), os.path.abspath(__file__)])
+    for f in files:
+        src.update(os.path.relpath(f, ROOT).encode())
+        src.update(open(f, "rb").read())
+    # inputs: the packed weights, scales and x of layer 0 (seeded; the other
+    # layers come from the same generator with their own linear index)
+    inp = hashlib.sha256()
+    for i, (L, name, N, K) in enumerate(st["lin"]):
+        if L != 0:
+            break
+        inp.update(st["qs"][i].cpu().numpy().tobytes())
+        inp.update(st["d"][i].cpu().numpy().tobytes())
+        xh = st["x_host"].numpy()
+        inp.update(xh[st["x_off"][i]:st["x_off"][i] + K].tobytes())
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    nvcc = run([os.environ.get("NVCC", "nvcc"), "--version"])
+    smi = run(["nvidia-smi", "--query-gpu=driver_version,name", "--format=csv,noheader"])
+    cores, model = cpu_info()
+    return {
+        "source_sha256": src.hexdigest(),
+        "git_sha": run(["git", "rev-parse", "HEAD"]) or None,
+        "seed": SEED,
+        "input_sha256_layer0": inp.hexdigest(),
+        "gpu": props.name,
+        "sm_count": props.multi_processor_count,
+        "compute_capability": f"{props.major}.{props.minor}",
+        "memory_bytes": props.total_memory,
+        "driver": smi.splitlines()[0].split(",")[0].strip() if smi else None,
+        "nvcc": nvcc.splitlines()[-1].strip() if nvcc else None,
+        "torch": torch.__version__,
+        "torch_cuda": torch.version.cuda,
+        "python": platform.python_version(),
+        "host": f"{platform.machine()}, {model}, {cores} cores in the affinity mask",
+    }
+
+
 def cpu_baseline_oracle(budget_s=10.0, stack_host=None):
     """The CPU oracle (plain C, fp64, as it stands) timed on the host: one
     thread on layer 0 of the stack, and every core of the process's affinity
@@ -665,7 +717,7 @@ def run_gpu(args):
         "pct_of_peak": round(100 * per_gpu / peak, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "tq2::matvec_mma_kernel<1> (q, o, gate, up, down: 160 launches) and "
+            "kernel": "tq2::matvec_mma_kernel<1, 1, 1, false> (q, o, gate, up, down: 160 launches) and "
                       "tq2::matvec_smalln_kernel<1,1> (k, v: 64 launches): all 224 launches of a step",
             "achieved": round(per_gpu, 2),
             "peak": peak,
@@ -692,6 +744,7 @@ def run_gpu(args):
         },
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "manifest": run_manifest(torch, st),
     }
     if extras:
         line["extras"] = extras

@@ -75,6 +75,8 @@ typedef enum { TQ2_F32 = 0, TQ2_F16 = 1 } tq2_dtype;
 #define TQ2_FLAG_NONFINITE 2u /* from_dense: NaN/Inf in W, or max|W| overflows fp16 */
 #define TQ2_FLAG_INEXACT 4u   /* from_dense: some W != d*(code-1) (lossy recovery) */
 #define TQ2_FLAG_TIMEOUT 8u   /* matvec: a bounded device wait ran out; y is invalid */
+#define TQ2_FLAG_BOUNDS 16u   /* debug builds (TQ2_BOUNDS_CHECK) only: a kernel computed an index
+                                 outside its buffer and skipped that access; the result is invalid */
 
 /*
  * tq2_pack -- codes int8 [N,K] -> qs uint8 [N,K/4].

@@ -22,12 +22,13 @@ __all__ = [
     "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "gemm", "affine4_matvec",
     "matvec_workspace_size",
     "status_string", "version",
-    "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT",
+    "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT", "FLAG_BOUNDS",
+    "bounds_checked",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_PS", "IMPL_GEMM", "IMPL_SMALLN",
 ]
 
 F32, F16 = 0, 1
-FLAG_BAD_CODE, FLAG_NONFINITE, FLAG_INEXACT, FLAG_TIMEOUT = 1, 2, 4, 8
+FLAG_BAD_CODE, FLAG_NONFINITE, FLAG_INEXACT, FLAG_TIMEOUT, FLAG_BOUNDS = 1, 2, 4, 8, 16
 # (3 and 5 are retired kernel numbers: TQ2_ERR_ARG)
 IMPL_AUTO, IMPL_MMA, IMPL_SIMT, IMPL_PS, IMPL_GEMM, IMPL_SMALLN = 0, 1, 2, 4, 6, 7
 HEADER = os.path.join(os.path.dirname(_build.PKG), "include", "tq2.h")
@@ -45,17 +46,25 @@ class TQ2Error(RuntimeError):
         super().__init__(msg)
 
 
+def bounds_checked() -> bool:
+    """True when this process uses the bounds-checked debug library
+    (environment TQ2_BOUNDS_CHECK=1, read at the first load)."""
+    return os.environ.get("TQ2_BOUNDS_CHECK", "0") not in ("", "0")
+
+
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load the CUDA library (building it in-tree first if it is missing)."""
+    """Load the CUDA library (building it in-tree first if it is missing):
+    the release build, or the bounds-checked one when TQ2_BOUNDS_CHECK=1."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        check = bounds_checked()
+        path = _build.lib_path(check)
         if not os.path.exists(path):
             if not build_if_missing:
                 raise RuntimeError(f"CUDA library not built: {path}")
-            _build.build()
+            _build.build(bounds_check=check)
         L = ctypes.CDLL(path)
         P, I64, I32, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
                               ctypes.c_size_t)

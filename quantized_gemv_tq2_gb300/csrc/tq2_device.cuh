@@ -7,12 +7,29 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "../../include/tq2.h"
+
 namespace tq2 {
 namespace dev {
 
 // Longest any mbarrier wait may take before the kernel gives up and reports
 // TQ2_FLAG_TIMEOUT (normal waits are microseconds).
 constexpr unsigned long long kTimeoutNs = 200ull * 1000 * 1000;
+
+// Checked indexing of the debug build (TQ2_BOUNDS_CHECK): TQ2_IN(cond, status)
+// is cond, and when cond is false it also sets TQ2_FLAG_BOUNDS in the status
+// word (if any), so that the caller skips the access and the host learns of
+// it; nothing traps.  The release build compiles every check to true.
+__device__ __forceinline__ bool flag_bounds(uint32_t *status)
+{
+    if (status) atomicOr(status, TQ2_FLAG_BOUNDS);
+    return false;
+}
+#ifdef TQ2_BOUNDS_CHECK
+#define TQ2_IN(cond, status) ((cond) ? true : ::tq2::dev::flag_bounds(status))
+#else
+#define TQ2_IN(cond, status) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -233,6 +250,24 @@ __device__ __forceinline__ float lds_f32(uint32_t addr)
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
+}
+
+// Shared-memory reads checked, in debug builds (TQ2_BOUNDS_CHECK), against a
+// CTA's dynamic shared memory [lo, hi): an address outside gives zero and
+// TQ2_FLAG_BOUNDS.  Release builds compile them to the plain loads.
+struct SmemWindow {
+    uint32_t lo, hi;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ uint4 lds128_c(const SmemWindow &w, uint32_t addr)
+{
+    return TQ2_IN(addr >= w.lo && addr + 16u <= w.hi, w.status) ? lds128(addr) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ float lds_f32_c(const SmemWindow &w, uint32_t addr)
+{
+    return TQ2_IN(addr >= w.lo && addr + 4u <= w.hi, w.status) ? lds_f32(addr) : 0.0f;
 }
 
 // Static int8 fake-quant code (gemma4 wNa8o8 page, "Implemented"):

@@ -163,6 +163,9 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // full[S], empty[S]
     uint8_t *ring = smem + p.off_ring;
+    uint32_t *const st_w = p.a.status;  // TQ2_FLAG_BOUNDS of debug builds
+    const SmemWindow win{smem_addr(smem), smem_addr(smem) + (uint32_t)p.smem_total, st_w};
+    const uint32_t ring_end = smem_addr(ring) + (uint32_t)(S * p.stage_bytes);
     const unsigned long long lim = (kHook && p.a.wait_limit_ns) ? p.a.wait_limit_ns : kTimeoutNs;
 
     // Let the next kernel in the stream start its own weight prefetch.
@@ -205,18 +208,21 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
             if (!p.tma2d) {
                 // whole rows [rg0*16, rg0*16 + rows): one contiguous copy
                 const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
-                if (lane == 0) {
+                if (lane == 0 && TQ2_IN((r0 + rg0 * 16) * row_bytes + bytes <= N * row_bytes && dst0 + bytes <= ring_end,
+                                        st_w)) {
                     mbar_arrive_expect_tx(full, bytes);
                     bulk_g2s(dst0, qs_g + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
                 }
             } else {
                 // 16 rows x 1024 bytes (columns past the row end read as zero);
                 // a partial group is split into boxes of 8, 4, 2, 1 rows
-                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)rows * 1024u);
+                const bool in = TQ2_IN(dst0 + (uint32_t)rows * 1024u <= ring_end, st_w);
+                if (lane == 0 && in) mbar_arrive_expect_tx(full, (uint32_t)rows * 1024u);
                 __syncwarp();
                 const int y0 = (int)(r0 + rg0 * 16);
                 const int x = kc * 128;
-                if (rows == 16) {
+                if (!in) {
+                } else if (rows == 16) {
                     if (lane == 0) tensor2d_g2s(dst0, &p.tmap[kT > 1 ? mi : 0][0], x, y0, full, pol);
                 } else {
                     int roff = 0, box = 0;
@@ -260,7 +266,8 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
     // zero this warp's slots of the cross-warp partial sums
     for (int i = lane; i < nrg * kM * 16; i += 32) {
         const int rg = i / (kM * 16), rest = i - rg * (kM * 16);
-        red[(rg * kConsumerWarps + warp) * kM * 16 + rest] = 0.0f;
+        const int ri = (rg * kConsumerWarps + warp) * kM * 16 + rest;
+        if (TQ2_IN(ri < p.max_rg * kConsumerWarps * kM * 16, st_w)) red[ri] = 0.0f;
     }
     // d slice of this CTA's rows (contiguous in memory), fp32.  All loads of
     // a batch are issued before the first store so their latencies overlap;
@@ -275,12 +282,13 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = base + j * kConsumerThreads + tid;
-                v[j] = (i < nd) ? dsrc[i] : (uint16_t)0;
+                v[j] = (i < nd && TQ2_IN(r0 * B + i < N * B, st_w)) ? dsrc[i] : (uint16_t)0;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = base + j * kConsumerThreads + tid;
-                if (i < nd) dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
+                if (i < nd && TQ2_IN(r * p.dstr + b < p.max_rg * 16 * p.dstr, st_w))
+                    dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
                 r += q_step;
                 b += r_step;
                 if (b >= B) {
@@ -313,7 +321,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         uint4 xpre[kM][2];
 #pragma unroll
         for (int m = 0; m < kM; ++m) {
-            if (tid < nw) {
+            if (tid < nw && TQ2_IN((int64_t)m * K + (int64_t)c * (256 * kChunkBlocks) + tid * 16 + 16 <= kM * K, st_w)) {
                 xpre[m][0] = *reinterpret_cast<const uint4 *>(x_src(c, m));
                 xpre[m][1] = *reinterpret_cast<const uint4 *>(x_src(c, m) + 8);
             } else {
@@ -354,6 +362,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
                     const uint32_t sel = (cc & 1) ? 0x7632u : 0x5410u;
                     const uint32_t lo = __byte_perm(raw[cc >> 1], raw[4 + (cc >> 1)], sel);
                     const uint32_t hi = __byte_perm(raw[2 + (cc >> 1)], raw[6 + (cc >> 1)], sel);
+                    if (TQ2_IN(dst + (uint32_t)(cc * 64) + 8u <= smem_addr(xs) + (uint32_t)(B * 512 * kM), st_w))
                     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst + (uint32_t)(cc * 64)), "r"(lo),
                                  "r"(hi)
                                  : "memory");
@@ -367,7 +376,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         }
 #pragma unroll
         for (int m = 0; m < kM; ++m)
-            if (tid < nw && (lane & 15) == 0) xsum[b * kM + m] = sum[m];
+            if (tid < nw && (lane & 15) == 0 && TQ2_IN(b * kM + m < B * kM, st_w)) xsum[b * kM + m] = sum[m];
     };
     if (p.n_kc == 1) {
         x_store(0);
@@ -386,6 +395,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
                   const int m = (kM == 2 && L >= B * 16) ? 1 : 0;  // kM <= 2: no division
                   const int rem = L - m * B * 16;
                   const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(rem >> 4) * 256 + (rem & 15) * 16;
+                  if (!TQ2_IN(src + 16 <= p.a.x + kM * K, st_w)) src = p.a.x;
                   xv[j][0] = *reinterpret_cast<const uint4 *>(src);
                   xv[j][1] = *reinterpret_cast<const uint4 *>(src + 8);
               }
@@ -432,6 +442,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
                     const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
                     const uint32_t lo = __byte_perm(raw[c >> 1], raw[4 + (c >> 1)], sel);
                     const uint32_t hi = __byte_perm(raw[2 + (c >> 1)], raw[6 + (c >> 1)], sel);
+                    if (TQ2_IN(dst + (uint32_t)(c * 64) + 8u <= smem_addr(xs) + (uint32_t)(B * 512 * kM), st_w))
                     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst + (uint32_t)(c * 64)), "r"(lo),
                                  "r"(hi)
                                  : "memory");
@@ -445,7 +456,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
           }
 #pragma unroll
           for (int j = 0; j < kXBatch; ++j)
-            if (bm[j] >= 0 && (lane & 15) == 0) xsum[bm[j]] = sum[j];
+            if (bm[j] >= 0 && (lane & 15) == 0 && TQ2_IN(bm[j] < B * kM, st_w)) xsum[bm[j]] = sum[j];
         }
     }
     consumer_barrier();
@@ -467,8 +478,11 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         vg8 += __shfl_xor_sync(0xffffffffu, vg8, 1);
         if ((t & 1) == 0 && (t >> 1) < kM) {
             float *rp = red + ((rg * kConsumerWarps + warp) * kM + (t >> 1)) * 16;
-            rp[g] = vg;
-            rp[g + 8] = vg8;
+            if (TQ2_IN(((rg * kConsumerWarps + warp) * kM + (t >> 1) + 1) * 16 <= p.max_rg * kConsumerWarps * kM * 16,
+                       st_w)) {
+                rp[g] = vg;
+                rp[g + 8] = vg8;
+            }
         }
     };
 
@@ -492,7 +506,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         float xi[kUpw];
 #pragma unroll
         for (int u = 0; u < kUpw; ++u)
-            xi[u] = -lds_f32(xs_thr + (uint32_t)(warp + u * kConsumerWarps) * (4u * kM)) * 5.9604644775390625e-08f;
+            xi[u] = -lds_f32_c(win, xs_thr + (uint32_t)(warp + u * kConsumerWarps) * (4u * kM)) * 5.9604644775390625e-08f;
         const uint32_t x_warp = x_thr + (uint32_t)warp * x_blk;
         const uint32_t a_warp = a_thr + (uint32_t)(warp * 64);
         const uint32_t d_warp = d_thr + (uint32_t)(warp * 4);
@@ -502,7 +516,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 #pragma unroll
             for (int u = 0; u < kUpw; ++u) {
                 const uint32_t pa = a_warp + (uint32_t)(sl * p.stage_bytes + u * kConsumerWarps * 64);
-                const uint4 wa = lds128(pa), wb = lds128(pa + a_half);
+                const uint4 wa = lds128_c(win, pa), wb = lds128_c(win, pa + a_half);
                 W0[u][0] = wa.x; W0[u][1] = wa.y; W0[u][2] = wa.z; W0[u][3] = wa.w;
                 W1[u][0] = wb.x; W1[u][1] = wb.y; W1[u][2] = wb.z; W1[u][3] = wb.w;
             }
@@ -511,8 +525,8 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 #pragma unroll
             for (int u = 0; u < kUpw; ++u) {
                 const uint32_t pd = d_warp + (uint32_t)rg * rg_stride_d + (uint32_t)(u * kConsumerWarps * 4);
-                dg[u] = lds_f32(pd);
-                dg8[u] = lds_f32(pd + d_half);
+                dg[u] = lds_f32_c(win, pd);
+                dg8[u] = lds_f32_c(win, pd + d_half);
             }
         };
         int sl = 0, ph = 0;
@@ -535,7 +549,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 #pragma unroll
             for (int u = 0; u < kUpw; ++u) {
                 const uint32_t px = x_warp + (uint32_t)(u * kConsumerWarps) * x_blk;
-                const uint4 xa = lds128(px), xb = lds128(px + x_half);
+                const uint4 xa = lds128_c(win, px), xb = lds128_c(win, px + x_half);
                 const uint32_t BX[4][2] = {{xa.x, xa.y}, {xa.z, xa.w}, {xb.x, xb.y}, {xb.z, xb.w}};
                 float c[4][4];
 #pragma unroll
@@ -616,13 +630,13 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
                 for (int u = 0; u < kUpw; ++u) {
                     const int kb = kb0 + warp + u * kConsumerWarps;
                     const uint32_t pa = st + (uint32_t)((warp + u * kConsumerWarps) * 64);
-                    const uint4 wa = lds128(pa), wb = lds128(pa + a_half);
+                    const uint4 wa = lds128_c(win, pa), wb = lds128_c(win, pa + a_half);
                     const uint32_t px = x_thr + (uint32_t)kb * x_blk;
-                    const uint4 xa = lds128(px), xb = lds128(px + x_half);
+                    const uint4 xa = lds128_c(win, px), xb = lds128_c(win, px + x_half);
                     const uint32_t pd = d_thr + (uint32_t)rg * rg_stride_d + (uint32_t)kb * 4u;
-                    dg[u] = lds_f32(pd);
-                    dg8[u] = lds_f32(pd + d_half);
-                    xi[u] = -lds_f32(xs_thr + (uint32_t)kb * (4u * kM)) * 5.9604644775390625e-08f;
+                    dg[u] = lds_f32_c(win, pd);
+                    dg8[u] = lds_f32_c(win, pd + d_half);
+                    xi[u] = -lds_f32_c(win, xs_thr + (uint32_t)kb * (4u * kM)) * 5.9604644775390625e-08f;
                     W0[u][0] = wa.x; W0[u][1] = wa.y; W0[u][2] = wa.z; W0[u][3] = wa.w;
                     W1[u][0] = wb.x; W1[u][1] = wb.y; W1[u][2] = wb.z; W1[u][3] = wb.w;
                     BX[u][0][0] = xa.x; BX[u][0][1] = xa.y; BX[u][1][0] = xa.z; BX[u][1][1] = xa.w;
@@ -672,15 +686,15 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
                     cur_rg = rg;
                 }
                 const uint32_t pa = st + (uint32_t)(j * 16 * p.rb + bl * 64);
-                const uint4 wa = lds128(pa);
-                const uint4 wb = lds128(pa + a_half);
+                const uint4 wa = lds128_c(win, pa);
+                const uint4 wb = lds128_c(win, pa + a_half);
                 const uint32_t px = x_thr + (uint32_t)kb * x_blk;
-                const uint4 xa = lds128(px);
-                const uint4 xb = lds128(px + x_half);
+                const uint4 xa = lds128_c(win, px);
+                const uint4 xb = lds128_c(win, px + x_half);
                 const uint32_t pd = d_thr + (uint32_t)rg * rg_stride_d + (uint32_t)kb * 4u;
-                const float dg = lds_f32(pd);
-                const float dg8 = lds_f32(pd + d_half);
-                const float xi = -lds_f32(xs_thr + (uint32_t)kb * (4u * kM)) * 5.9604644775390625e-08f;
+                const float dg = lds_f32_c(win, pd);
+                const float dg8 = lds_f32_c(win, pd + d_half);
+                const float xi = -lds_f32_c(win, xs_thr + (uint32_t)kb * (4u * kM)) * 5.9604644775390625e-08f;
                 float c0[4], c1[4], c2[4], c3[4];
                 {
                     const uint32_t w0 = wa.x, w1 = wb.x, s0 = w0 >> 8, s1 = w1 >> 8;
@@ -760,6 +774,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         if (prologue) s *= p.a.act_scale;
         s = requant_out(s, p.mats[mi].out_scale, p.mats[mi].inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
+        if (!TQ2_IN(o < kM * N && rg < p.max_rg, st_w)) continue;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(y_g)[o] = __float2half_rn(s);
         else

@@ -173,6 +173,7 @@ __device__ __forceinline__ void stage_x(const PsPlan &p, int kb0, int nbx, uint3
             bb[i] = bx;
             if (m < M) {
                 const uint16_t *src = p.a.x + (int64_t)m * K + (int64_t)(kb0 + bx) * 256 + 16 * wi;
+                if (!TQ2_IN(src + 16 <= p.a.x + (int64_t)M * K, p.a.status)) src = p.a.x;
                 v[i][0] = *reinterpret_cast<const uint4 *>(src);
                 v[i][1] = *reinterpret_cast<const uint4 *>(src + 8);
             }
@@ -234,9 +235,11 @@ __device__ __forceinline__ void stage_x(const PsPlan &p, int kb0, int nbx, uint3
             if (live) {
                 const int mi = mm[i], nt = mi >> 3, Mt = min(8, M - 8 * nt);
                 const uint32_t dst = frag + frag_off(bb[i], nt, jw, 0, t, mi & 7, M);
-                sts128(dst, e[0], e[1], e[2], e[3]);                                // classes 0, 1
-                sts128(dst + (uint32_t)(64 * Mt), e[4], e[5], e[6], e[7]);        // classes 2, 3
-                if (wi == 0) {
+                if (TQ2_IN(dst + (uint32_t)(64 * Mt) + 16u <= frag + (uint32_t)(p.xblocks * 512 * M), p.a.status)) {
+                    sts128(dst, e[0], e[1], e[2], e[3]);                          // classes 0, 1
+                    sts128(dst + (uint32_t)(64 * Mt), e[4], e[5], e[6], e[7]);  // classes 2, 3
+                }
+                if (wi == 0 && TQ2_IN(bb[i] * 8 * NT + mi < p.xblocks * 8 * NT, p.a.status)) {
                     const float sc = big ? 5.9604644775390625e-08f : 3.814697265625e-06f;  // 2^-24, 2^-18
                     const float rs = big ? 16777216.0f : 262144.0f;
                     xinfo[bb[i] * 8 * NT + mi] = make_float2(-sum * sc, rs);
@@ -250,7 +253,8 @@ __device__ __forceinline__ void stage_x(const PsPlan &p, int kb0, int nbx, uint3
 // rows g and g + 8 are (wa, wb); the block's B fragments start at fb, this
 // lane's entry of word jw, half 0, at fb + xo[jw], of half 1 at + h1; two
 // accumulator chains, merged on return.
-__device__ __forceinline__ void unit_mma(float (&c)[4], const uint32_t (&wa)[4], const uint32_t (&wb)[4],
+__device__ __forceinline__ void unit_mma(const SmemWindow &win, float (&c)[4], const uint32_t (&wa)[4],
+                                         const uint32_t (&wb)[4],
                                          uint32_t fb, const uint32_t (&xo)[4], uint32_t h1, float2 init)
 {
     float ca[4] = {init.x, init.y, init.x, init.y};
@@ -258,8 +262,8 @@ __device__ __forceinline__ void unit_mma(float (&c)[4], const uint32_t (&wa)[4],
 #pragma unroll
     for (int jw = 0; jw < 4; ++jw) {
         const uint32_t w0 = wa[jw], w1 = wb[jw], s0 = w0 >> 8, s1 = w1 >> 8;
-        const uint4 f0 = lds128(fb + xo[jw]);
-        const uint4 f1 = lds128(fb + xo[jw] + h1);
+        const uint4 f0 = lds128_c(win, fb + xo[jw]);
+        const uint4 f1 = lds128_c(win, fb + xo[jw] + h1);
         float (&cc)[4] = (jw < 2) ? ca : cb;
         mma_16816(cc, w0 & 0x00030003u, w1 & 0x00030003u, s0 & 0x00030003u, s1 & 0x00030003u, f0.x, f0.y);
         mma_16816(cc, w0 & 0x000C000Cu, w1 & 0x000C000Cu, s0 & 0x000C000Cu, s1 & 0x000C000Cu, f0.z, f0.w);
@@ -300,6 +304,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // full[S], empty[S]
     uint8_t *ring = smem + p.off_ring;
+    uint32_t *const st_w = p.a.status;  // TQ2_FLAG_BOUNDS of debug builds
+    const SmemWindow win{smem_addr(smem), smem_addr(smem) + (uint32_t)p.smem_total, st_w};
+    const uint32_t ring_end = smem_addr(ring) + (uint32_t)(S * p.stage_bytes);
 
     // Let the next kernel in the stream start its own weight prefetch.
     asm volatile("griddepcontrol.launch_dependents;");
@@ -337,17 +344,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
             const uint32_t dst0 = smem_addr(ring + (size_t)slot * p.stage_bytes);
             if (!p.tma2d) {
                 const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
-                if (lane == 0) {
+                if (lane == 0 && TQ2_IN((r0 + rg0 * 16) * row_bytes + bytes <= N * row_bytes && dst0 + bytes <= ring_end,
+                                        st_w)) {
                     mbar_arrive_expect_tx(full, bytes);
                     bulk_g2s(dst0, qs_g + (r0 + rg0 * 16) * row_bytes, bytes, full, pol);
                 }
             } else {
                 // boxes of 16 rows x (kcb*64) bytes; the last group split into 8/4/2/1
-                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)rows * (uint32_t)p.rb);
+                const bool in = TQ2_IN(dst0 + (uint32_t)rows * (uint32_t)p.rb <= ring_end, st_w);
+                if (lane == 0 && in) mbar_arrive_expect_tx(full, (uint32_t)rows * (uint32_t)p.rb);
                 __syncwarp();
                 const int x = kc * p.kcb * 8;
                 int roff = 0, box = 0;
-                while (roff + 16 <= rows) {
+                while (in && roff + 16 <= rows) {
                     if (lane == box) tensor2d_g2s(dst0 + roff * p.rb, &p.tmap[mi][0], x, (int)(r0 + rg0 * 16 + roff), full, pol);
                     roff += 16;
                     ++box;
@@ -389,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     const uint32_t frag = smem_addr(smem + p.off_frag);
     const bool prologue = p.a.act_scale != 0.0f;
 
-    for (int i = tid; i < nrg * kWarps * 16 * M; i += kConsumers) red[i] = 0.0f;
+    for (int i = tid; i < nrg * kWarps * 16 * M; i += kConsumers)
+        if (TQ2_IN(i < p.max_rg * kWarps * 16 * M, st_w)) red[i] = 0.0f;
     for (int i = tid; i < p.xblocks * 8 * NT; i += kConsumers) xinfo[i] = make_float2(0.0f, 0.0f);
     {
         const int nd = nrows * B;
@@ -399,14 +409,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = base + j * kConsumers + tid;
-                v[j] = (i < nd) ? dsrc[i] : (uint16_t)0;
+                v[j] = (i < nd && TQ2_IN(r0 * B + i < N * B, st_w)) ? dsrc[i] : (uint16_t)0;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = base + j * kConsumers + tid;
                 if (i < nd) {
                     const int r = i / B, b = i - r * B;
-                    dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
+                    if (TQ2_IN(r * p.dstr + b < p.max_rg * 16 * p.dstr, st_w))
+                        dsm[r * p.dstr + b] = __half2float(__ushort_as_half(v[j]));
                 }
             }
         }
@@ -436,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
         for (int nt = 0; nt < NT; ++nt) {
             const int col = 8 * nt + 2 * t;
             float *rp = red + ((rg * kWarps + warp) * 16) * M;
+            if (!TQ2_IN(rg < p.max_rg, st_w)) continue;
             if (col < M) {
                 rp[g * M + col] += acc[nt][0];
                 rp[(g + 8) * M + col] += acc[nt][2];
@@ -481,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
         do {                                                                               \
             _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
                 const uint32_t pa_ = au(u_) + (uint32_t)((SL) * p.stage_bytes);           \
-                const uint4 va_ = lds128(pa_), vb_ = lds128(pa_ + a_half);                 \
+                const uint4 va_ = lds128_c(win, pa_), vb_ = lds128_c(win, pa_ + a_half);                 \
                 W[u_][0] = va_.x; W[u_][1] = va_.y; W[u_][2] = va_.z; W[u_][3] = va_.w;    \
                 V[u_][0] = vb_.x; V[u_][1] = vb_.y; V[u_][2] = vb_.z; V[u_][3] = vb_.w;    \
             }                                                                              \
@@ -491,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
 #define TQ2_PS_LOAD_SCALES(RG)                                                             \
         do {                                                                               \
             _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
-                dg[u_] = lds_f32(du(u_) + (uint32_t)(RG) * d_rg);                          \
-                dg8[u_] = lds_f32(du(u_) + (uint32_t)(RG) * d_rg + d_half);                \
+                dg[u_] = lds_f32_c(win, du(u_) + (uint32_t)(RG) * d_rg);                          \
+                dg8[u_] = lds_f32_c(win, du(u_) + (uint32_t)(RG) * d_rg + d_half);                \
             }                                                                              \
         } while (0)
         int sl = 0, ph = 0;
@@ -513,18 +525,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
             for (int u = 0; u < kU; ++u) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float4 xi;
-                    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                                 : "=f"(xi.x), "=f"(xi.y), "=f"(xi.z), "=f"(xi.w)
-                                 : "r"(xiu(u) + (uint32_t)(64 * nt)));
+                    const uint4 xw = lds128_c(win, xiu(u) + (uint32_t)(64 * nt));
+                    const float4 xi = make_float4(__uint_as_float(xw.x), __uint_as_float(xw.y),
+                                                  __uint_as_float(xw.z), __uint_as_float(xw.w));
                     float c0[4] = {xi.x, xi.z, xi.x, xi.z};
                     float c1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c2[4] = {0.0f, 0.0f, 0.0f, 0.0f},
                           c3[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int jw = 0; jw < 4; ++jw) {
                         const uint32_t w0 = W[u][jw], w1 = V[u][jw], s0 = w0 >> 8, s1 = w1 >> 8;
-                        const uint4 f0 = lds128(fbu(u) + xo[nt][jw]);
-                        const uint4 f1 = lds128(fbu(u) + xo[nt][jw] + h1[nt]);
+                        const uint4 f0 = lds128_c(win, fbu(u) + xo[nt][jw]);
+                        const uint4 f1 = lds128_c(win, fbu(u) + xo[nt][jw] + h1[nt]);
                         mma_16816(c0, w0 & 0x00030003u, w1 & 0x00030003u, s0 & 0x00030003u, s1 & 0x00030003u, f0.x, f0.y);
                         mma_16816(c1, w0 & 0x000C000Cu, w1 & 0x000C000Cu, s0 & 0x000C000Cu, s1 & 0x000C000Cu, f0.z, f0.w);
                         mma_16816(c2, w0 & 0x00300030u, w1 & 0x00300030u, s0 & 0x00300030u, s1 & 0x00300030u, f1.x, f1.y);
@@ -549,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
             if (ok && s + 1 < n_stages) TQ2_PS_LOAD_SCALES(s + 1);
             // row group s: this warp's partials (each row group once per warp)
             float *rp = red + ((s * kWarps + warp) * 16) * M;
+            if (!TQ2_IN(s < p.max_rg, st_w)) rp = red;  // (flagged: y is not stored)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int col = 8 * nt + 2 * t;
@@ -609,18 +621,20 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
                     cur_rg = rg;
                 }
                 const uint32_t pa = st + (uint32_t)(j * 16 * p.rb + bl * 64);
-                const uint4 va = lds128(pa), vb = lds128(pa + a_half);
+                const uint4 va = lds128_c(win, pa), vb = lds128_c(win, pa + a_half);
                 const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
                 const int kb = kb0 + bl, bx = kbx0 + bl;
-                const float d0 = dsm[(rg * 16 + g) * p.dstr + kb];
-                const float d8 = dsm[(rg * 16 + g + 8) * p.dstr + kb];
+                const float d0 = lds_f32_c(win, smem_addr(dsm + (rg * 16 + g) * p.dstr + kb));
+                const float d8 = lds_f32_c(win, smem_addr(dsm + (rg * 16 + g + 8) * p.dstr + kb));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int Mt = min(8, M - 8 * nt);
                     const uint32_t fb = frag + (uint32_t)(bx * 512 * M);
-                    const float4 xi = *reinterpret_cast<const float4 *>(&xinfo[bx * 8 * NT + 8 * nt + 2 * t]);
+                    const uint4 xw = lds128_c(win, smem_addr(&xinfo[bx * 8 * NT + 8 * nt + 2 * t]));
+                    const float4 xi = make_float4(__uint_as_float(xw.x), __uint_as_float(xw.y),
+                                                  __uint_as_float(xw.z), __uint_as_float(xw.w));
                     float c[4];
-                    unit_mma(c, wa, wb, fb, xo[nt], (uint32_t)(64 * Mt), make_float2(xi.x, xi.z));
+                    unit_mma(win, c, wa, wb, fb, xo[nt], (uint32_t)(64 * Mt), make_float2(xi.x, xi.z));
                     acc[nt][0] = fmaf(c[0], xi.y * d0, acc[nt][0]);
                     acc[nt][1] = fmaf(c[1], xi.w * d0, acc[nt][1]);
                     acc[nt][2] = fmaf(c[2], xi.y * d8, acc[nt][2]);
@@ -665,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
         if (prologue) s *= p.a.act_scale;
         s = requant_out(s, p.mats[mi].out_scale, p.mats[mi].inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
+        if (!TQ2_IN(o < (int64_t)M * N && rg < p.max_rg, st_w)) continue;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(y_g)[o] = __float2half_rn(s);
         else

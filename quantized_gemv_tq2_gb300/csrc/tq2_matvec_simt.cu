@@ -34,12 +34,14 @@ matvec_simt_kernel(MatvecArgs a)
 #pragma unroll
         for (int m = 0; m < kM; ++m) acc[m] = 0.0f;
         for (int64_t c = lane; c < nchunks; c += 32) {
+            if (!TQ2_IN(n * KB + c * 16 + 16 <= a.N * KB && n * B + c / 4 < a.N * B, a.status)) continue;
             const uint4 v = *reinterpret_cast<const uint4 *>(a.qs + n * KB + c * 16);
             const float dv = __half2float(__ushort_as_half(a.d[n * B + c / 4]));
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int m = 0; m < kM; ++m) {
                 const uint16_t *xr = a.x + (int64_t)m * a.K + c * 64;
+                if (!TQ2_IN((int64_t)m * a.K + c * 64 + 64 <= (int64_t)a.M * a.K, a.status)) continue;
                 float part = 0.0f;
 #pragma unroll 1
                 for (int wi = 0; wi < 4; ++wi) {
@@ -65,7 +67,7 @@ matvec_simt_kernel(MatvecArgs a)
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
             if (prologue) s *= a.act_scale;
             s = dev::requant_out(s, a.out_scale, a.inv_out);
-            if (lane == 0) {
+            if (lane == 0 && TQ2_IN((int64_t)m * a.N + n < (int64_t)a.M * a.N, a.status)) {
                 if (a.y_f16)
                     reinterpret_cast<__half *>(a.y)[(int64_t)m * a.N + n] = __float2half_rn(s);
                 else

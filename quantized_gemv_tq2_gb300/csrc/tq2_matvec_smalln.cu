@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_smalln_kernel(const Matvec
 #pragma unroll
         for (int i = 0; i < kW; ++i) {
             const int w = tid + i * kThreads;
-            const bool v = r < nrows && w < nw;
+            const bool v = r < nrows && w < nw && TQ2_IN(r0 + r < N, a.status);
             cw[r][i] = v ? __ldg(reinterpret_cast<const uint32_t *>(a.qs + (r0 + r) * (K / 4)) + w) : 0x55555555u;
             dv[r][i] = v ? h2f(__ldg(a.d + (r0 + r) * B + (w >> 4))) : 0.0f;
         }
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_smalln_kernel(const Matvec
 #pragma unroll
         for (int i = 0; i < kW; ++i) {
             const int w = tid + i * kThreads;
-            if (w < nw) {
+            if (w < nw && TQ2_IN((int64_t)m * K + (int64_t)w * 16 + 16 <= (int64_t)kM * K, a.status)) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)m * K + (int64_t)w * 16);
                 xv[m][i][0] = src[0];
                 xv[m][i][1] = src[1];
@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_smalln_kernel(const Matvec
         if (prologue) s *= a.act_scale;
         s = requant_out(s, a.out_scale, a.inv_out);
         const int64_t o = (int64_t)m * N + r0 + r;
+        if (!TQ2_IN(o < (int64_t)kM * N, a.status)) return;
         if (a.y_f16)
             reinterpret_cast<__half *>(a.y)[o] = __float2half_rn(s);
         else
