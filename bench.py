@@ -860,6 +860,81 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PHASES = ("entry", "wait returned", "x staged", "first stage read", "stage loop done", "y stored",
+          "producer done")
+
+
+def run_phases(args):
+    """Where one call's time goes, in the steady state: back-to-back
+    tq2_matvec calls (the class-column kernel) of one shape over distinct
+    weight sets totalling >= 4x L2, replayed in a CUDA graph, on the trace
+    build (TQ2_TRACE=1: globaltimer stamps per CTA at each phase).  Prints
+    one JSON line: for the last call, each phase's time after the previous
+    call's last y store (median / min / max over its CTAs), the per-CTA
+    phase lengths, and the call time of the replay (the stamps make calls
+    ~0.3 us slower: not a bench value)."""
+    import numpy as np
+    import torch
+    import quantized_gemv_tq2_gb300 as tq2
+    assert tq2.traced(), "--phases needs the trace build: run with TQ2_TRACE=1"
+    N, K = CASES[args.phases]
+    M = args.M
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(SEED)
+    per = N * K // 4 + 2 * N * (K // 256)
+    copies = max(4, int(4 * L2_BYTES // per) + 1)
+    def packed():  # valid codes {0, 1, 2}, four per byte
+        c = torch.randint(0, 3, (N, K // 4, 4), dtype=torch.uint8, device=dev, generator=g)
+        return (c[..., 0] + 4 * c[..., 1] + 16 * c[..., 2] + 64 * c[..., 3]).contiguous()
+
+    qs = [packed() for _ in range(copies)]
+    d = [(torch.rand(N, K // 256, device=dev, generator=g) * 0.045 + 0.005).half() for _ in range(copies)]
+    x = torch.randn(M, K, device=dev, generator=g).half()
+    ys = [torch.empty(M, N, device=dev) for _ in range(copies)]
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for q, dd, y in zip(qs, d, ys):
+            tq2.matvec(x, q, dd, y=y, impl=tq2.IMPL_MMA)
+        st.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            for q, dd, y in zip(qs, d, ys):
+                tq2.matvec(x, q, dd, y=y, impl=tq2.IMPL_MMA)
+        for _ in range(3):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        graph.replay()
+        e1.record(st)
+        e1.synchronize()
+    us_call = e0.elapsed_time(e1) * 1e3 / copies
+    tr = tq2.trace_read().astype(np.int64)
+    ctas = int((tr[0, :, 0] > 0).sum())
+    tr = tr[:, :ctas]
+    last = 0 if tr[0, :, 5].max() > tr[1, :, 5].max() else 1  # the last call of the replay
+    cur, prev = tr[last], tr[1 - last]
+    t0 = prev[:, 5].max()  # the previous call's last y store
+
+    def stats(v):
+        return {"median_us": round(float(np.median(v)) / 1e3, 3), "min_us": round(float(v.min()) / 1e3, 3),
+                "max_us": round(float(v.max()) / 1e3, 3)}
+
+    stamped = [bool((cur[:, i] > 0).all()) for i in range(7)]
+
+    out = {
+        "phases": args.phases, "N": N, "K": K, "M": M, "ctas": ctas, "weight_sets": copies,
+        "us_per_call_trace_build": round(us_call, 3),
+        "after_previous_y_store": {PHASES[i]: stats(cur[:, i] - t0) if stamped[i] else None for i in range(7)},
+        "per_cta": {
+            name: stats(cur[:, j] - cur[:, i]) if stamped[i] and stamped[j] else None
+            for name, i, j in (("wait -> x staged", 1, 2), ("x staged -> first stage read", 2, 3),
+                               ("first stage read -> loop done", 3, 4), ("loop done -> y stored", 4, 5))
+        },
+        "call_span_us": round(float(cur[:, 5].max() - t0) / 1e3, 3),
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -878,7 +953,11 @@ def main():
     ap.add_argument("--case-impl", type=int, default=0)
     ap.add_argument("--affine4-group", type=int, default=0,
                     help="with --case: run tq2_affine4_matvec with this group size instead")
+    ap.add_argument("--phases", choices=sorted(CASES),
+                    help="per-phase time budget of back-to-back calls of this shape (trace build: TQ2_TRACE=1)")
     args = ap.parse_args()
+    if args.phases:
+        return run_phases(args)
     if args.case:
         return run_case(args)
     if args.warmup < 3:

@@ -347,6 +347,26 @@ TQ2_API tq2_status tq2_test_gemm_stall(const uint16_t *x, int64_t M, const uint8
                                        int64_t N, int64_t K, float *y, float act_scale, uint32_t *d_status,
                                        tq2_stream_t stream, int stall_stage, int wait_limit_us);
 
+/*
+ * tq2_trace_size, tq2_trace_read -- diagnostics of the trace build (the
+ * library compiled with TQ2_TRACE; the pages have no counterpart).  That
+ * build's class-column kernel (impl 1, single calls) stamps the GPU's
+ * globaltimer (ns) per CTA at 8 phase points into a static device array of
+ * two slots, which consecutive launches use in turn (launch parity; in a
+ * CUDA graph, the parity of the capture order): [slot 2][CTA 1024][phase 8]
+ * uint64, phases 0 entry, 1 the wait on the previous kernel returned, 2 x
+ * staged, 3 the first stage's codes read, 4 the stage loop done, 5 y stored,
+ * 6 the producer's last copy issued, 7 unused.  Only CTAs below 1024 stamp.
+ *   tq2_trace_size  the array's size in bytes; 0 in other builds.
+ *   tq2_trace_read  copies it to host_dst (host memory, at least
+ *                   tq2_trace_size() bytes), synchronously after the device's
+ *                   work; TQ2_ERR_ARG in other builds or for a smaller
+ *                   buffer, TQ2_ERR_NULL for a NULL pointer.
+ * The stamps cost about 0.3 us per call; time nothing with the trace build.
+ */
+TQ2_API size_t tq2_trace_size(void);
+TQ2_API tq2_status tq2_trace_read(void *host_dst, size_t bytes);
+
 /* The CUDA error behind the most recent TQ2_ERR_CUDA returned to the calling
  * host thread ("no error" if none): name and description, static storage. */
 TQ2_API const char *tq2_last_cuda_error(void);

@@ -23,7 +23,7 @@ __all__ = [
     "matvec_workspace_size",
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT", "FLAG_BOUNDS",
-    "bounds_checked",
+    "bounds_checked", "traced", "trace_read",
     "IMPL_AUTO", "IMPL_MMA", "IMPL_SIMT", "IMPL_PS", "IMPL_GEMM", "IMPL_SMALLN",
 ]
 
@@ -52,6 +52,12 @@ def bounds_checked() -> bool:
     return os.environ.get("TQ2_BOUNDS_CHECK", "0") not in ("", "0")
 
 
+def traced() -> bool:
+    """True when this process uses the trace library (environment
+    TQ2_TRACE=1, read at the first load; the bounds-checked one wins)."""
+    return not bounds_checked() and os.environ.get("TQ2_TRACE", "0") not in ("", "0")
+
+
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
     """Load the CUDA library (building it in-tree first if it is missing):
     the release build, or the bounds-checked one when TQ2_BOUNDS_CHECK=1."""
@@ -59,12 +65,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        check = bounds_checked()
-        path = _build.lib_path(check)
+        variant = "check" if bounds_checked() else ("trace" if traced() else "release")
+        path = _build.lib_path(variant=variant)
         if not os.path.exists(path):
             if not build_if_missing:
                 raise RuntimeError(f"CUDA library not built: {path}")
-            _build.build(bounds_check=check)
+            _build.build(variant=variant)
         L = ctypes.CDLL(path)
         P, I64, I32, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
                               ctypes.c_size_t)
@@ -81,6 +87,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_test_matvec_stall.argtypes = [P, I64, P, P, I64, I64, P, P, P, I32, I32]
         L.tq2_test_gemm_stall.argtypes = [P, I64, P, P, I64, I64, P, F, P, P, I32, I32]
         L.tq2_matvec_workspace_size.argtypes = [I64, I64, I64]
+        L.tq2_trace_size.argtypes = []
+        L.tq2_trace_size.restype = SZ
+        L.tq2_trace_read.argtypes = [P, SZ]
         L.tq2_matvec_workspace_size.restype = SZ
         L.tq2_status_string.argtypes = [I32]
         L.tq2_status_string.restype = ctypes.c_char_p
@@ -90,7 +99,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
                    "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_matvec_grouped_requant", "tq2_gemm",
                    "tq2_affine4_matvec",
-                   "tq2_test_matvec_stall", "tq2_test_gemm_stall", "tq2_version"):
+                   "tq2_test_matvec_stall", "tq2_test_gemm_stall", "tq2_trace_read", "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
         return L
@@ -349,6 +358,19 @@ def test_gemm_stall(x, qs, d, status, stall_stage: int, wait_limit_us: int, act_
                                       _stream_ptr(stream), int(stall_stage), int(wait_limit_us)),
            "tq2_test_gemm_stall")
     return y
+
+
+def trace_read():
+    """The trace build's phase stamps (tq2_trace_read) as a numpy uint64
+    array [2 slots, 1024 CTAs, 8 phases]; raises outside the trace build."""
+    import numpy as np
+    L = load()
+    n = int(L.tq2_trace_size())
+    if n == 0:
+        raise RuntimeError("not the trace build (set TQ2_TRACE=1 before the first load)")
+    buf = np.zeros(n // 8, dtype=np.uint64)
+    _check(L.tq2_trace_read(buf.ctypes.data_as(ctypes.c_void_p), n), "tq2_trace_read")
+    return buf.reshape(2, -1, 8)
 
 
 def matvec_workspace_size(M: int, N: int, K: int) -> int:

@@ -235,6 +235,16 @@ tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_t *qs, c
     return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, d_status, stream, impl);
 }
 
+size_t tq2_trace_size(void) { return tq2::trace_bytes(); }
+
+tq2_status tq2_trace_read(void *host_dst, size_t bytes)
+{
+    if (tq2::trace_bytes() == 0) return TQ2_ERR_ARG;  // not a trace build
+    if (host_dst == nullptr) return TQ2_ERR_NULL;
+    if (bytes < tq2::trace_bytes()) return TQ2_ERR_ARG;
+    return from_cuda(tq2::trace_read(host_dst, bytes));
+}
+
 tq2_status tq2_test_matvec_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
                                  int64_t K, float *y, uint32_t *d_status, tq2_stream_t stream, int stall_stage,
                                  int wait_limit_us)

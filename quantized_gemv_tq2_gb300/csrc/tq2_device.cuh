@@ -252,6 +252,26 @@ __device__ __forceinline__ float lds_f32(uint32_t addr)
     return v;
 }
 
+// Phase trace of the trace build (TQ2_TRACE): globaltimer stamps of the
+// class-column kernel per CTA, in two slots that consecutive launches take in
+// turn (a launch's parity), read by tq2_trace_read.  Phases: 0 entry, 1 the
+// wait on the previous kernel returned, 2 x staged, 3 the first stage's
+// codes read, 4 the stage loop done, 5 y stored, 6 the producer's last copy
+// issued.  Release builds compile the stamps out.
+constexpr int kTraceCtas = 1024, kTracePhases = 8;
+#ifdef TQ2_TRACE
+// (g_trace is defined in the translation unit of the traced kernel)
+#define TQ2_STAMP(seq, phase)                                                                      \
+    do {                                                                                           \
+        if (blockIdx.x < ::tq2::dev::kTraceCtas)                                                    \
+            ::tq2::dev::g_trace[(seq) & 1][blockIdx.x][phase] = ::tq2::dev::globaltimer();         \
+    } while (0)
+#else
+#define TQ2_STAMP(seq, phase) \
+    do {                      \
+    } while (0)
+#endif
+
 // Shared-memory reads checked, in debug builds (TQ2_BOUNDS_CHECK), against a
 // CTA's dynamic shared memory [lo, hi): an address outside gives zero and
 // TQ2_FLAG_BOUNDS.  Release builds compile them to the plain loads.

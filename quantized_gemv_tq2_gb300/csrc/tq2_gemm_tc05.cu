@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     // cluster hand-off waits keep kTimeoutNs, so that a short test limit
     // never lets a CTA leave while its peers or its MMAs still need it)
     const unsigned long long lim = p.a.wait_limit_ns ? p.a.wait_limit_ns : kTimeoutNs;
+    uint32_t *const st_w = p.a.status;  // TQ2_FLAG_BOUNDS of debug builds
+    const SmemWindow win{smem_addr(smem), smem_addr(smem) + (uint32_t)p.smem_total, st_w};
 
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 break;
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            if (lane == 0) {
+            if (lane == 0 && TQ2_IN(wring + (uint32_t)((slot + 1) * kWStageBytes) <= win.hi, st_w)) {
                 const uint32_t full = wfull0 + 8u * slot;
                 mbar_arrive_expect_tx(full, (uint32_t)kWStageBytes);
                 tensor2d_g2s(wring + (uint32_t)(slot * kWStageBytes), &p.wmap, 8 * (w0 + s), (int)n0, full, pol);
@@ -225,9 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 continue;
             }
             const uint32_t full = bfull0 + 8u * slot;
-            if (lane == 0) mbar_arrive_expect_tx(full, kBStageBytes);
+            const bool in = TQ2_IN(bring + (uint32_t)(slot + 1) * kBStageBytes <= win.hi, st_w);
+            if (lane == 0 && in) mbar_arrive_expect_tx(full, kBStageBytes);
             __syncwarp();
-            if (lane < 2)
+            if (lane < 2 && in)
                 tensor2d_g2s(bring + (uint32_t)slot * kBStageBytes + (uint32_t)lane * kBoxBytes, &p.xmap,
                              256 * w0 + 16 * kKs * s + 64 * lane, m0, full, pol);
             __syncwarp();
@@ -303,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
 
     for (int i = uw * 32 + lane; i < kRows * B; i += kUnpackWarps * 32) {
         const int r = i / B, b = i - r * B;  // row-major reads of d
-        dsm[b * kRows + r] = (n0 + r < N) ? p.a.d[(n0 + r) * (int64_t)B + b] : (uint16_t)0;
+        if (TQ2_IN(i < p.B * kRows, st_w))
+            dsm[b * kRows + r] = (n0 + r < N) ? p.a.d[(n0 + r) * (int64_t)B + b] : (uint16_t)0;
     }
     named_barrier(3, kUnpackWarps * 32);  // d staged
     named_barrier(1, kTmemThreads);       // (a)
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 if (alive) {
                     const uint32_t xb = bring + (uint32_t)r * (2u * BN * 128u);
                     for (int c = (uw & 3) * 32 + lane; c < 2 * BN * 8; c += (kUnpackWarps / 2) * 32) {
-                        const uint4 v = lds128(xb + (uint32_t)c * 16u);
+                        const uint4 v = lds128_c(win, xb + (uint32_t)c * 16u);
                         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -337,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                             const __half2 h = __floats2half2_rn(fq_code(f.x, p.a.inv_scale), fq_code(f.y, p.a.inv_scale));
                             w[e] = *reinterpret_cast<const uint32_t *>(&h);
                         }
+                        if (TQ2_IN(xb + (uint32_t)c * 16u + 16u <= win.hi, st_w))
                         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xb + (uint32_t)c * 16u),
                                      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                                      : "memory");
@@ -366,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
             if (alive) {
                 const uint32_t lbase = wring + (uint32_t)(slot * kWStageBytes + row * 64);
-                c0 = lds128(lbase + (uint32_t)(u0 << 4));
-                c1 = lds128(lbase + (uint32_t)((u0 + 1) << 4));
+                c0 = lds128_c(win, lbase + (uint32_t)(u0 << 4));
+                c1 = lds128_c(win, lbase + (uint32_t)((u0 + 1) << 4));
             }
             const __half hd = __ushort_as_half(dsm[(w0 + (g >> 1)) * kRows + row]);  // block of the group
             const __half2 dd = __halves2half2(hd, hd);
@@ -377,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 uint32_t v[32];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) expand_word(wd[4 * h2 + i], dd, &v[8 * i]);
-                if (alive) tmem_st32(tlane + (uint32_t)(a * kAColsPerSlot + 32 * h2), v);
+                if (alive && TQ2_IN(a * kAColsPerSlot + 32 * h2 + 32 <= kDCol, st_w))
+                    tmem_st32(tlane + (uint32_t)(a * kAColsPerSlot + 32 * h2), v);
             }
             if (alive) {
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -400,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         if (prologue) v *= p.a.act_scale;
         v = requant_out(v, p.a.out_scale, p.a.inv_out);
         const int64_t o = (int64_t)m * N + nn;
+        if (!TQ2_IN(o < (int64_t)M * N, st_w)) return;
         if (p.a.y_f16)
             reinterpret_cast<__half *>(p.a.y)[o] = __float2half_rn(v);
         else
@@ -436,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (c0 + j < c_end) part[(c0 + j) * kRows + row] = __uint_as_float(r[j]);
+            if (c0 + j < c_end && TQ2_IN(smem_addr(&part[(c0 + j) * kRows + row]) + 4u <= win.hi, st_w))
+                part[(c0 + j) * kRows + row] = __uint_as_float(r[j]);
     }
     tc_fence_before();
     named_barrier(2, kTmemThreads);       // (b): TMEM read, the MMA warp may free it
@@ -469,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         for (int i = tid_u; i < cols * kRows; i += kUnpackWarps * 32) {
             const int c = c_lo + i / kRows, rr = i % kRows;
             const uint32_t off = (uint32_t)((c * kRows + rr) * 4);
+            if (!TQ2_IN(off + 4u <= (uint32_t)(BN * kRows * 4) && part_s + off + 4u <= win.hi, st_w)) continue;
             float v = 0.0f;
             for (int q2 = 0; q2 < S; ++q2) {
                 uint32_t ra;

@@ -103,6 +103,12 @@ cudaError_t launch_unpack(const uint8_t *qs, int64_t N, int64_t K, int8_t *codes
 cudaError_t launch_from_dense(const void *W, int w_f16, int64_t N, int64_t K, uint8_t *qs,
                               uint16_t *d, uint32_t *status, cudaStream_t s);
 
+// The trace build's phase stamps of the class-column kernel (TQ2_TRACE):
+// their size in bytes (0 in other builds), and a copy of them to host memory
+// (cudaErrorNotSupported in other builds).
+size_t trace_bytes();
+cudaError_t trace_read(void *dst, size_t bytes);
+
 // Number of SMs of the current device (cached per device).
 int sm_count(int device);
 

@@ -95,6 +95,17 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return v;
 }
 
+// checked forms for the debug build (TQ2_BOUNDS_CHECK); plain loads otherwise
+__device__ __forceinline__ uint2 lds64_c(const SmemWindow &w, uint32_t addr)
+{
+    return TQ2_IN(addr >= w.lo && addr + 8u <= w.hi, w.status) ? lds64(addr) : make_uint2(0u, 0u);
+}
+
+__device__ __forceinline__ uint32_t lds32_c(const SmemWindow &w, uint32_t addr)
+{
+    return TQ2_IN(addr >= w.lo && addr + 4u <= w.hi, w.status) ? lds32(addr) : 0u;
+}
+
 __device__ __forceinline__ uint32_t pack_h2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 
 __device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
@@ -125,6 +136,10 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
     // ring start rounded up to 1024 bytes (the 128-byte swizzle pattern repeats every 1 KB)
     const uint32_t ring = (smem_addr(smem + p.off_ring) + 1023u) & ~1023u;
 
+    uint32_t *const st_w = p.status;  // TQ2_FLAG_BOUNDS of debug builds
+    const SmemWindow win{smem_addr(smem), smem_addr(smem) + (uint32_t)p.smem_total, st_w};
+    const uint32_t ring_end = ring + (uint32_t)(S * kStageBytes);
+
     asm volatile("griddepcontrol.launch_dependents;");
 
     if (tid == 0) {
@@ -153,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
             // one 16 KB copy: 8 blocks x 16 rows x 128 bytes (blocks past K
             // and rows past N read as zero and count in full)
             const uint32_t full = smem_addr(&bars[slot]);
-            if (lane == 0) {
+            if (lane == 0 && TQ2_IN(ring + (uint32_t)((slot + 1) * kStageBytes) <= ring_end && ring_end <= win.hi,
+                                    st_w)) {
                 mbar_arrive_expect_tx(full, (uint32_t)kStageBytes);
                 tensor3d_g2s(ring + (uint32_t)(slot * kStageBytes), &p.tq, 0, (int)(r0 + rg * 16), kc * 8, full, pol);
             }
@@ -193,17 +209,19 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
         const uint4 *zv4 = reinterpret_cast<const uint4 *>(p.z + r0 * ng);
         auto put = [&](int e, uint16_t sh, uint16_t zh) {
             const int r = e / ng;
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(szs + (uint32_t)(r * szstr + (e - r * ng)) * 4u),
-                         "r"(pack_h2(sh, zh))
-                         : "memory");
+            if (TQ2_IN(r * szstr + (e - r * ng) < p.max_rg * 16 * szstr, st_w))
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(szs + (uint32_t)(r * szstr + (e - r * ng)) * 4u),
+                             "r"(pack_h2(sh, zh))
+                             : "memory");
         };
         for (int base = 0; base < nvec; base += kConsumers * kSzBatch) {
             uint4 a[kSzBatch], b[kSzBatch];
 #pragma unroll
             for (int j = 0; j < kSzBatch; ++j) {
                 const int v = base + j * kConsumers + tid;
-                a[j] = v < nvec ? sv4[v] : make_uint4(0, 0, 0, 0);
-                b[j] = v < nvec ? zv4[v] : make_uint4(0, 0, 0, 0);
+                const bool in = v < nvec && TQ2_IN(r0 * ng + 8 * (int64_t)v + 8 <= N * ng, st_w);
+                a[j] = in ? sv4[v] : make_uint4(0, 0, 0, 0);
+                b[j] = in ? zv4[v] : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int j = 0; j < kSzBatch; ++j) {
@@ -219,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                 }
             }
         }
-        for (int e = nvec * 8 + tid; e < ne; e += kConsumers) put(e, p.s[r0 * ng + e], p.z[r0 * ng + e]);
+        for (int e = nvec * 8 + tid; e < ne; e += kConsumers)
+            if (TQ2_IN(r0 * ng + e < N * ng, st_w)) put(e, p.s[r0 * ng + e], p.z[r0 * ng + e]);
         for (int e = ne + tid; e < nrg * 16 * ng; e += kConsumers) put(e, 0, 0);
     }
 
@@ -245,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                     const int m = (kM == 2 && mb >= p.B) ? 1 : 0;
                     const int b = mb - m * p.B;
                     const uint16_t *src = p.x + (int64_t)m * K + (int64_t)b * 256 + j * 64 + t * 16;
+                    if (!TQ2_IN(src + 16 <= p.x + (int64_t)kM * K, st_w)) src = p.x;
                     lo[u] = *reinterpret_cast<const uint4 *>(src);
                     hi[u] = *reinterpret_cast<const uint4 *>(src + 8);
                 }
@@ -271,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                     for (int c = 0; c < 4; ++c) {
                         const uint32_t e = (uint32_t)((4 * m + c) * 4 + t);
                         const uint32_t dst = xf + ((uint32_t)((b * 4 + j) * 16 * kM) + e) * 8u;
+                        if (TQ2_IN(dst + 8u <= xf + (uint32_t)(p.B * 4 * 16 * kM * 8), st_w))
                         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(pack_h2(h[c], h[c + 4])),
                                      "r"(pack_h2(h[8 + c], h[12 + c]))
                                      : "memory");
@@ -280,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2);
                 if (kJpg >= 2) sum += __shfl_xor_sync(0xffffffffu, sum, 4);
                 if (kJpg >= 4) sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-                if (valid && t == 0 && j % kJpg == 0) xg[m * ng + (b * 256 + j * 64) / kG] = sum;
+                if (valid && t == 0 && j % kJpg == 0 && TQ2_IN(m * ng + (b * 256 + j * 64) / kG < kM * ng, st_w))
+                    xg[m * ng + (b * 256 + j * 64) / kG] = sum;
             }
         }
     }
@@ -318,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t off = (uint32_t)((((2 * j + (t >> 1)) ^ rw) << 4) + (t & 1) * 8);
-                wl[j] = lds64(cb + (uint32_t)rw * 128u + off);
-                wh[j] = lds64(cb + (uint32_t)(rw + 8) * 128u + off);
-                bx[j] = (lane < 16 * kM) ? lds64(xf + ((uint32_t)((kb * 4 + j) * 16 * kM) + (uint32_t)lane) * 8u)
+                wl[j] = lds64_c(win, cb + (uint32_t)rw * 128u + off);
+                wh[j] = lds64_c(win, cb + (uint32_t)(rw + 8) * 128u + off);
+                bx[j] = (lane < 16 * kM) ? lds64_c(win, xf + ((uint32_t)((kb * 4 + j) * 16 * kM) + (uint32_t)lane) * 8u)
                                          : make_uint2(0u, 0u);
             }
 #pragma unroll
@@ -348,12 +370,13 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
                 const float dlo = pcls ? (c[2][0] + c[3][1] * 0.0625f) : (c[0][0] + c[1][1] * 0.0625f);
                 const float dhi = pcls ? (c[2][2] + c[3][3] * 0.0625f) : (c[0][2] + c[1][3] * 0.0625f);
                 const int grp = kb * kGpb + gi;
-                const uint32_t plo = lds32(szs + (uint32_t)((rg * 16 + rw) * szstr + grp) * 4u);
-                const uint32_t phi = lds32(szs + (uint32_t)((rg * 16 + rw + 8) * szstr + grp) * 4u);
+                const uint32_t plo = lds32_c(win, szs + (uint32_t)((rg * 16 + rw) * szstr + grp) * 4u);
+                const uint32_t phi = lds32_c(win, szs + (uint32_t)((rg * 16 + rw + 8) * szstr + grp) * 4u);
                 const float slo = h2f((uint16_t)(plo & 0xffffu)), zlo = h2f((uint16_t)(plo >> 16));
                 const float shi = h2f((uint16_t)(phi & 0xffffu)), zhi = h2f((uint16_t)(phi >> 16));
                 // the zero-point term once per row and activation row (class pair 0)
-                const float xs = (mine && pcls == 0) ? xg[(mine ? mrow : 0) * ng + grp] : 0.0f;
+                const float xs = (mine && pcls == 0 && TQ2_IN(mrow * ng + grp < kM * ng, st_w))
+                                     ? xg[(mine ? mrow : 0) * ng + grp] : 0.0f;
                 acc_lo = fmaf(slo * 16777216.0f, dlo, acc_lo);
                 acc_lo = fmaf(-(slo * zlo), xs, acc_lo);
                 acc_hi = fmaf(shi * 16777216.0f, dhi, acc_hi);
@@ -371,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
             // this warp's partial of each (activation row, row) goes to red
             const float vlo = acc_lo + __shfl_xor_sync(0xffffffffu, acc_lo, 1);
             const float vhi = acc_hi + __shfl_xor_sync(0xffffffffu, acc_hi, 1);
-            if (pcls == 0 && mine) {
+            if (pcls == 0 && mine && TQ2_IN(((rg * kWarps + warp) * kM + mrow + 1) * 16 <= p.max_rg * kWarps * kM * 16,
+                                            st_w)) {
                 red[((rg * kWarps + warp) * kM + mrow) * 16 + rw] = vlo;
                 red[((rg * kWarps + warp) * kM + mrow) * 16 + rw + 8] = vhi;
             }
@@ -392,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_affine4_kernel(const __gri
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) v += red[((rgi * kWarps + w) * kM + m) * 16 + ri];
         const int64_t o = (int64_t)m * N + r0 + r;
+        if (!TQ2_IN(o < (int64_t)kM * N && rgi < p.max_rg, st_w)) continue;
         if (p.y_f16)
             reinterpret_cast<__half *>(p.y)[o] = __float2half_rn(v);
         else

@@ -53,6 +53,14 @@
 #include "tq2_device.cuh"
 #include "tq2_internal.cuh"
 
+#ifdef TQ2_TRACE
+namespace tq2 {
+namespace dev {
+__device__ unsigned long long g_trace[2][kTraceCtas][kTracePhases];
+}  // namespace dev
+}  // namespace tq2
+#endif
+
 namespace tq2 {
 namespace {
 
@@ -98,6 +106,7 @@ struct MmaPlan {
     int dstr;        // fp32 stride of the d slice rows (B + 1, odd)
     int off_bar, off_red, off_dsm, off_xsum, off_xs, off_ring, smem_total;
     int n_mats;
+    int seq;         // launch sequence number (the trace build's slot parity)
 };
 
 // Kernel parameters for up to kG matrices with kT sets of tensor maps (1, or
@@ -168,6 +177,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
     const uint32_t ring_end = smem_addr(ring) + (uint32_t)(S * p.stage_bytes);
     const unsigned long long lim = (kHook && p.a.wait_limit_ns) ? p.a.wait_limit_ns : kTimeoutNs;
 
+    if (tid == 0) TQ2_STAMP(p.seq, 0);
     // Let the next kernel in the stream start its own weight prefetch.
     asm volatile("griddepcontrol.launch_dependents;");
 
@@ -241,6 +251,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
             __syncwarp();
             issued = s + 1;
         }
+        if (lane == 0) TQ2_STAMP(p.seq, 6);
         // No copy may still be writing shared memory when the CTA exits.
         // (Slots are refilled only after every consumer has waited for and
         // read the previous stage, so the last copy of a slot is the only one
@@ -301,6 +312,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
 
     // x depends on the previous kernel in the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) TQ2_STAMP(p.seq, 1);
 
     // x -> fragment order.  Entry (block b, half h, column cc = 4m + c, t)
     // is 16 bytes = words 2h and 2h+1 of the t-th quarter of the block, each
@@ -460,6 +472,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         }
     }
     consumer_barrier();
+    if (tid == 0) TQ2_STAMP(p.seq, 2);
 
     const int g = lane >> 2, t = lane & 3;
     const int gg = g % (4 * kM);          // x-fragment column this thread supplies
@@ -539,6 +552,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
             load_codes(0);
             load_scales(0);
         }
+        if (tid == 0) TQ2_STAMP(p.seq, 3);
         for (int s = 0; ok && s < n_stages; ++s) {
             // unit by unit: four class accumulators starting at zero, then
             // their scaled sums (the "-1" of q - 1 enters as d_b * (-X_b *
@@ -602,6 +616,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
             ok = alive = false;
         }
         ready_lane = false;
+        if (tid == 0 && s == 0) TQ2_STAMP(p.seq, 3);
         if (ok && s + 1 < n_stages) {
             // test the next stage now; its latency overlaps this stage's math
             const int nslot = (slot + 1 == S) ? 0 : slot + 1;
@@ -760,6 +775,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
     }
     if (cur_rg >= 0) flush(cur_rg);
     }
+    if (tid == 0) TQ2_STAMP(p.seq, 4);
     consumer_barrier();
     if (*abort_flag) return;  // y is invalid; TQ2_FLAG_TIMEOUT was reported
 
@@ -780,10 +796,19 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         else
             reinterpret_cast<float *>(y_g)[o] = s;
     }
+#ifdef TQ2_TRACE
+    consumer_barrier();  // every y store of the CTA issued
+    if (tid == 0) TQ2_STAMP(p.seq, 5);
+#endif
 }
 
 // ------------------------------------------------------------------ host side
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Launch sequence numbers (the parity picks a trace slot; in a CUDA graph
+// every node keeps the number it was captured with).
+std::atomic<int> g_seq{0};
+int next_seq() { return g_seq.fetch_add(1, std::memory_order_relaxed); }
 
 // Shared-memory plan for G CTAs within max_dyn bytes of dynamic shared
 // memory; returns false if it cannot fit.
@@ -958,6 +983,7 @@ cudaError_t launch_impl(const MatvecArgs &a, int device)
 {
     MmaParams<1, 1> p{};
     p.a = a;
+    p.seq = next_seq();
     if (!plan_for(kM, a.N, a.K, device, max_dynamic_smem<kM>(device), p))
         return cudaErrorInvalidConfiguration;
     p.n_mats = 1;
@@ -1058,6 +1084,27 @@ cudaError_t launch_matvec_mma(const MatvecArgs &a, int device)
     if (a.M == 1) return launch_impl<1>(a, device);
     if (a.M == 2) return launch_impl<2>(a, device);
     return cudaErrorInvalidValue;
+}
+
+size_t trace_bytes()
+{
+#ifdef TQ2_TRACE
+    return sizeof(unsigned long long) * 2 * dev::kTraceCtas * dev::kTracePhases;
+#else
+    return 0;
+#endif
+}
+
+cudaError_t trace_read(void *dst, size_t bytes)
+{
+#ifdef TQ2_TRACE
+    if (bytes < trace_bytes()) return cudaErrorInvalidValue;
+    return cudaMemcpyFromSymbol(dst, dev::g_trace, trace_bytes());
+#else
+    (void)dst;
+    (void)bytes;
+    return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace tq2

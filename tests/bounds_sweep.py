@@ -102,10 +102,58 @@ def grouped():
     print("grouped calls: clear, parity green", flush=True)
 
 
+def affine4():
+    n_calls = 0
+    cases = [(M, N, K, G) for K in (256, 512, 2048) for N in (1, 15, 16, 17, 33, 70) for M in (1, 2, 3, 16)
+             for G in (64, 128, 256)]
+    cases += [(M, 16384, 4096, 128) for M in (1, 2)] + [(1, 4096, 16384, 64), (2, 4096, 4096, 256)]
+    for M, N, K, G in cases:
+        qs_h, s_h, z_h = syn.affine4_weights(M + N + K + G, N, K, G)
+        x_h = syn.activations(M + N, M, K)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y = tq2.affine4_matvec(dev(x_h), dev(qs_h), dev(s_h), dev(z_h), G, status=st)
+        check_status(st, f"affine4 M={M} N={N} K={K} G={G}")
+        if N > 2048:
+            rows = sample_rows(N, 32, seed=N)
+            y_ref, tol = oracle.affine4_rows(x_h, qs_h, s_h, z_h, K, G, rows)
+            yg = host(y).astype(np.float64)[:, rows]
+        else:
+            y_ref, tol = oracle.affine4(x_h, qs_h, s_h, z_h, K, G)
+            yg = host(y).astype(np.float64)
+        assert_within_tolerance(yg, y_ref, tol, f"affine4 M={M} N={N} K={K} G={G}")
+        n_calls += 1
+    print(f"affine-int4: clear, parity green ({n_calls} calls)", flush=True)
+
+
+def gemm():
+    n_calls = 0
+    cases = [(17, 128, 256), (64, 100, 512), (130, 257, 768), (300, 300, 1024), (16, 512, 4096),
+             (16, 16384, 1024), (200, 2048, 1024), (2048, 256, 4096), (512, 4096, 4096)]
+    for M, N, K in cases:
+        for prologue in (False, True):
+            seed = M + N + K + int(prologue)
+            codes = syn.codes(seed, N, K)
+            qs_h, _ = oracle.pack(codes)
+            d_h = syn.scales(seed, N, K // 256)
+            x_h = syn.activations(seed, M, K, heavy=prologue)
+            s = float(syn.act_scale(seed)) if prologue else 0.0
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            y = tq2.gemm(dev(x_h), dev(qs_h), dev(d_h), act_scale=s, status=st, impl=1)
+            check_status(st, f"gemm M={M} N={N} K={K} prologue={prologue}")
+            rows = sample_rows(N, 48, seed=M) if N > 512 else np.arange(N)
+            y_ref, tol = oracle.matvec_rows(x_h, qs_h, d_h, K, rows, act_scale=s)
+            assert_within_tolerance(host(y).astype(np.float64)[:, rows], y_ref, tol,
+                                    f"gemm M={M} N={N} K={K} prologue={prologue}")
+            n_calls += 1
+    print(f"tcgen05 GEMM: clear, parity green ({n_calls} calls)", flush=True)
+
+
 if __name__ == "__main__":
     assert tq2.bounds_checked(), "run with TQ2_BOUNDS_CHECK=1"
     tq2.load()
     tiny_sweep()
     layer_shapes()
     grouped()
+    affine4()
+    gemm()
     print("OK")

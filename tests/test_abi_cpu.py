@@ -25,9 +25,16 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) >= {"tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_grouped",
                           "tq2_matvec_impl", "tq2_matvec_requant", "tq2_gemm",
                           "tq2_affine4_matvec", "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version",
-                          "tq2_test_matvec_stall", "tq2_matvec_grouped_requant", "tq2_test_gemm_stall"}
+                          "tq2_test_matvec_stall", "tq2_matvec_grouped_requant", "tq2_test_gemm_stall",
+                          "tq2_trace_size", "tq2_trace_read"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
+
+
+def test_trace_entry_points_outside_the_trace_build(L):
+    assert L.tq2_trace_size() == 0
+    buf = ctypes.create_string_buffer(64)
+    assert L.tq2_trace_read(ctypes.cast(buf, P), 64) == ARG
 
 
 def test_version_and_status_strings(L):
