@@ -125,8 +125,21 @@ TQ2_API tq2_status tq2_from_dense(const void *W, tq2_dtype w_dtype, int64_t N, i
  * Accuracy: |y - exact| <= 1e-3 * sum_k |d_b x'_k| + 1e-6 per element; the
  * result is bit-identical from run to run.
  * Alignment: x and qs 16-byte aligned; d 2-byte; y 4-byte (fp32) / 2-byte.
- * workspace / workspace_bytes: scratch for plans that need it; the current
- * kernels need none (tq2_matvec_workspace_size returns 0) and ignore it.
+ * workspace / workspace_bytes: optional device scratch (workspace_bytes 0:
+ * none; else workspace non-NULL (TQ2_ERR_NULL) and 16-byte aligned
+ * (TQ2_ERR_ALIGN)).  With act_scale > 0 and a workspace, the call may run
+ * the prologue as a pass of its own: x is converted once into the workspace
+ * (2 M K bytes: the codes as fp16) and the kernel reads the codes, instead
+ * of every CTA converting the x it reads.  It does so where that was
+ * measured faster: with the tcgen05 GEMM for N > 512 or M > 64, and with
+ * the pre-scaled kernel (impl 4) for M >= 9 and K >= 8192; with a
+ * workspace the automatic choice also takes the GEMM for M = 8 when
+ * K >= 8192 and N > 512.  A workspace smaller than the pass needs is then
+ * TQ2_ERR_ARG (nothing enqueued).  A kernel gives the same bits either
+ * way (the codes are those it would compute itself).  The workspace must not overlap x, qs, d or y;
+ * it is written and read by the call's kernels in stream order, so a
+ * workspace may be reused by the next call on the same stream, but not by
+ * calls that may run concurrently (other streams) until this one is done.
  * d_status: optional; TQ2_FLAG_TIMEOUT is set if a bounded device wait ran
  * out (y is then invalid).
  * Weights and scales are prefetched before the kernel waits on the previous
@@ -192,7 +205,11 @@ TQ2_API tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int6
                                               float act_scale, const float *out_scale, uint32_t *d_status,
                                               tq2_stream_t stream);
 
-/* Bytes of workspace tq2_matvec needs for this shape (0 for every shape today). */
+/* Bytes of workspace with which tq2_matvec runs the prologue as a pass of
+ * its own for this shape (2 M K), or 0 where it would not use one (and for
+ * invalid shapes).  tq2_matvec_impl with impl 4 or 6 may use one where
+ * tq2_matvec does not: 2 M K bytes (tq2_gemm_workspace_size) suffice for
+ * every impl. */
 TQ2_API size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -251,12 +268,15 @@ TQ2_API tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_
  * (out_scale) of tq2_matvec_requant.
  *   x          device, fp16 [M, K] row-major, 16-byte aligned, read only.
  *   M          >= 0 (up to 2^30); qs, d, N, K, y, y_dtype, act_scale,
- *              out_scale, d_status, stream as tq2_matvec_requant (y [M, N]).
+ *              out_scale, workspace, workspace_bytes, d_status, stream as
+ *              tq2_matvec_requant (y [M, N]; the workspace size from
+ *              tq2_gemm_workspace_size).
  *   impl       0 = automatic, 1 = the tcgen05 GEMM (5th-generation tensor
  *              cores: weights expanded once per 128-row tile into exact fp16
  *              (q - 1) * d_b in tensor memory, x tiles by TMA, fp32
- *              accumulation over all of K; the prologue fake-quantises each
- *              x tile in shared memory), 2 = the matvec kernels on 16-row
+ *              accumulation over all of K; without a workspace the
+ *              prologue fake-quantises each x tile in shared memory, in
+ *              every weight tile), 2 = the matvec kernels on 16-row
  *              slices of x.  Automatic takes the GEMM for M > 16, the slices
  *              otherwise.
  * Errors and accuracy as tq2_matvec (TQ2_ERR_SHAPE for M out of range;
@@ -264,7 +284,12 @@ TQ2_API tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_
  */
 TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
                             int64_t K, void *y, tq2_dtype y_dtype, float act_scale, float out_scale,
-                            uint32_t *d_status, tq2_stream_t stream, int impl);
+                            void *workspace, size_t workspace_bytes, uint32_t *d_status, tq2_stream_t stream,
+                            int impl);
+
+/* Bytes of workspace with which tq2_gemm runs the prologue as a pass of its
+ * own (2 M K: enough for every impl), or 0 for an invalid shape. */
+TQ2_API size_t tq2_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
  * tq2_affine4_matvec -- the affine-int4 sibling on the same skeleton

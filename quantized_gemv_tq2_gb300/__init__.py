@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "TQ2Error", "lib", "load", "declared_symbols",
     "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "gemm", "affine4_matvec",
-    "matvec_workspace_size",
+    "matvec_workspace_size", "gemm_workspace_size",
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT", "FLAG_BOUNDS",
     "bounds_checked", "traced", "trace_read",
@@ -82,7 +82,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_matvec_requant.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
         L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P]
         L.tq2_matvec_grouped_requant.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P, P]
-        L.tq2_gemm.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, P, I32]
+        L.tq2_gemm.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
         L.tq2_affine4_matvec.argtypes = [P, I64, P, P, P, I64, I64, I64, P, I32, P, P]
         L.tq2_test_matvec_stall.argtypes = [P, I64, P, P, I64, I64, P, P, P, I32, I32]
         L.tq2_test_gemm_stall.argtypes = [P, I64, P, P, I64, I64, P, F, P, P, I32, I32]
@@ -91,6 +91,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_trace_size.restype = SZ
         L.tq2_trace_read.argtypes = [P, SZ]
         L.tq2_matvec_workspace_size.restype = SZ
+        L.tq2_gemm_workspace_size.argtypes = [I64, I64, I64]
+        L.tq2_gemm_workspace_size.restype = SZ
         L.tq2_status_string.argtypes = [I32]
         L.tq2_status_string.restype = ctypes.c_char_p
         L.tq2_version.argtypes = []
@@ -148,6 +150,28 @@ def _check(status: int, where: str):
         raise TQ2Error(status, where)
 
 
+def _workspace(workspace, act_scale, nbytes_fn, device, stream):
+    """(pointer, bytes) of the scratch a call may use for the prologue as a
+    pass of its own: "auto" allocates what the library asks for (nothing
+    without the prologue, or where the library would not use it), None
+    passes none (each kernel then converts x itself), a tensor is passed
+    as is.  Returns the tensor too, to keep it alive for the call."""
+    if workspace is None or (isinstance(workspace, str) and (act_scale == 0.0)):
+        return ctypes.c_void_p(0), 0, None
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a CUDA tensor")
+        nbytes = int(nbytes_fn())
+        if nbytes == 0:
+            return ctypes.c_void_p(0), 0, None
+        torch = _torch()
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        if stream is not None and not isinstance(stream, int):
+            workspace.record_stream(stream)  # freed for reuse only after that stream's work
+    _need_cuda(workspace)
+    return _ptr(workspace), workspace.numel() * workspace.element_size(), workspace
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -201,9 +225,11 @@ def from_dense(W, qs=None, d=None, status=None, stream=None):
 
 
 def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, status=None,
-           stream=None, impl: int = IMPL_AUTO, workspace=None, out_scale: float = 0.0):
+           stream=None, impl: int = IMPL_AUTO, workspace="auto", out_scale: float = 0.0):
     """y [M,N] = ternary matvec of x [M,K] fp16 with packed qs/d (tq2_matvec);
-    out_scale > 0 requantises y to int8 at store (tq2_matvec_requant)."""
+    out_scale > 0 requantises y to int8 at store (tq2_matvec_requant).
+    workspace: scratch for the prologue as a pass of its own ("auto": what
+    tq2_matvec_workspace_size asks for; None: none; or a CUDA tensor)."""
     torch = _torch()
     if x.dim() == 1:
         x = x.view(1, -1)
@@ -218,9 +244,9 @@ def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, statu
         y = torch.empty((M, N), dtype=dt, device=qs.device)
     ycode = F32 if y.dtype == torch.float32 else F16
     _need_cuda(x, qs, d, y, status)
-    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) \
-        if workspace is not None else (ctypes.c_void_p(0), 0)
     L = load()
+    ws_ptr, ws_bytes, _ws = _workspace(workspace, act_scale, lambda: L.tq2_matvec_workspace_size(M, N, K),
+                                       qs.device, stream)
     if out_scale != 0.0:
         st = L.tq2_matvec_requant(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode,
                                   float(act_scale), float(out_scale), ws_ptr, ws_bytes, _ptr(status),
@@ -278,9 +304,10 @@ def matvec_grouped(x, qs_list, d_list, y_list=None, y_dtype=None, act_scale: flo
 
 
 def gemm(x, qs, d, y=None, y_dtype=None, act_scale: float = 0.0, out_scale: float = 0.0, status=None,
-         stream=None, impl: int = 0):
+         stream=None, impl: int = 0, workspace="auto"):
     """y [M,N] for any M (prefill): tq2_gemm; impl 0 auto, 1 the tcgen05 GEMM,
-    2 the matvec kernels on 16-row slices."""
+    2 the matvec kernels on 16-row slices.  workspace as for matvec
+    (tq2_gemm_workspace_size)."""
     torch = _torch()
     M, K = x.shape
     N = qs.shape[0]
@@ -291,8 +318,12 @@ def gemm(x, qs, d, y=None, y_dtype=None, act_scale: float = 0.0, out_scale: floa
         y = torch.empty((M, N), dtype=dt, device=qs.device)
     ycode = F32 if y.dtype == torch.float32 else F16
     _need_cuda(x, qs, d, y, status)
-    _check(load().tq2_gemm(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
-                           float(out_scale), _ptr(status), _stream_ptr(stream), int(impl)), "tq2_gemm")
+    L = load()
+    ws_ptr, ws_bytes, _ws = _workspace(workspace, act_scale, lambda: L.tq2_gemm_workspace_size(M, N, K),
+                                       qs.device, stream)
+    _check(L.tq2_gemm(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
+                      float(out_scale), ws_ptr, ws_bytes, _ptr(status), _stream_ptr(stream), int(impl)),
+           "tq2_gemm")
     return y
 
 
@@ -375,3 +406,7 @@ def trace_read():
 
 def matvec_workspace_size(M: int, N: int, K: int) -> int:
     return int(load().tq2_matvec_workspace_size(M, N, K))
+
+
+def gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load().tq2_gemm_workspace_size(M, N, K))

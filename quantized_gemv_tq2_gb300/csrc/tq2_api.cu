@@ -76,16 +76,73 @@ tq2_status current_device(int *dev)
 }
 
 // The tcgen05 GEMM beats the pre-scaled kernel (crossovers measured, see
-// the dispatch in matvec_common; the same with and without the prologue).
-bool gemm_preferred(int M, int64_t N, int64_t K)
+// the dispatch in matvec_common; the same with and without the prologue
+// when each kernel converts x itself).  With the prologue run as a pass of
+// its own (`pass`: act_scale > 0 and a workspace) the GEMM also wins for
+// down-sized K at M = 8: 27.3 against 30.5 us (at M = 6: 27.3 against 24.1).
+bool gemm_preferred(int M, int64_t N, int64_t K, bool pass = false)
 {
-    return (M >= 9 && (K >= 8192 || N <= 512)) || (M >= 12 && N < 8192);
+    return (M >= 9 && (K >= 8192 || N <= 512)) || (M >= 12 && N < 8192) || (pass && M >= 8 && K >= 8192 && N > 512);
+}
+
+// Scratch for the prologue as a pass of its own (tq2_prologue.cu): the
+// M x K codes as fp16.
+size_t codes_bytes(int64_t M, int64_t K)
+{
+    return (M > 0 && K > 0) ? (size_t)(2 * M * K) : 0;
+}
+
+// Whether converting x once (a pass of its own) beats each CTA of kernel
+// `which` (1, 2, 4, 6 or 7 as in tq2_matvec_impl) converting the x it
+// reads.  Measured on GB300, us per call back to back over distinct weights,
+// each CTA converting / the pass:
+//   GEMM, M = 1..16: gate/up 16384x4096 30.5-30.8 / 24.1-24.7, down
+//     4096x16384 33.9-34.0 / 27.1-27.7, q/o 4096x4096 11.3-11.4 /
+//     10.6-11.0, k/v 256x4096 7.2-7.3 / 7.6-8.0 (two weight tiles: little
+//     to save); prefill gate/up M = 32 / 128 / 512 / 2048: 35.5 / 57.7 /
+//     169.0 / 590.3 against 25.4 / 29.4 / 67.9 / 237.0, k/v M = 32 / 128:
+//     8.3 / 13.2 against 8.6 / 11.4;
+//   pre-scaled kernel, M = 9..16: down 39.5-55.4 / 36.4-50.0; q/o, k/v and
+//     gate/up within 0.9 either way;
+//   the kernels for M <= 8 lose 1-5 us: their CTAs start behind the pass's
+//     instead of beside the previous kernel's.
+bool prepass_pays(int which, int M, int64_t N, int64_t K)
+{
+    if (which == 6) return N > 512 || M > 64;
+    if (which == 4) return M >= 9 && K >= 8192;
+    return false;
+}
+
+// The workspace arguments: 0 bytes is none; otherwise non-NULL, 16-byte aligned.
+tq2_status check_workspace(const void *ws, size_t ws_bytes)
+{
+    if (ws_bytes == 0) return TQ2_OK;
+    if (ws == nullptr) return TQ2_ERR_NULL;
+    if (!aligned(ws, 16)) return TQ2_ERR_ALIGN;
+    return TQ2_OK;
+}
+
+// With act_scale > 0 and a workspace, and where it pays for kernel `which`:
+// convert x into the workspace (enqueued on a.stream) and point the kernel's
+// x at the codes.  TQ2_ERR_ARG (nothing enqueued) when the workspace is too
+// small for the pass the call would run.
+tq2_status maybe_convert_first(tq2::MatvecArgs &a, int which, void *ws, size_t ws_bytes, int dev)
+{
+    if (a.act_scale == 0.0f || ws_bytes == 0 || !prepass_pays(which, a.M, a.N, a.K)) return TQ2_OK;
+    if (ws_bytes < codes_bytes(a.M, a.K)) return TQ2_ERR_ARG;
+    cudaError_t e = tq2::launch_fq_codes(a.x, (int64_t)a.M * a.K, a.inv_scale, static_cast<uint16_t *>(ws), a.stream,
+                                         dev);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return from_cuda(e);
+    a.x = static_cast<const uint16_t *>(ws);
+    a.x_codes = 1;
+    return TQ2_OK;
 }
 
 tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                          int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
-                         float out_scale, uint32_t *d_status, tq2_stream_t stream, int impl,
-                         int stall_stage = -1, unsigned long long wait_limit_ns = 0)
+                         float out_scale, void *ws, size_t ws_bytes, uint32_t *d_status, tq2_stream_t stream,
+                         int impl, int stall_stage = -1, unsigned long long wait_limit_ns = 0)
 {
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
@@ -101,6 +158,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(d, 2)) return TQ2_ERR_ALIGN;
     if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
     if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    if ((st = check_workspace(ws, ws_bytes)) != TQ2_OK) return st;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t ybytes = (size_t)(M * N) * (y_dtype == TQ2_F32 ? 4 : 2);
@@ -142,7 +200,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     // (M = 9 starts the pre-scaled kernel's second n-tile of 8 rows).
     int which = impl;
     if (impl == 0) {
-        const bool gemm_wins = gemm_preferred(a.M, N, K);
+        const bool gemm_wins = gemm_preferred(a.M, N, K, act_scale != 0.0f && ws_bytes != 0);
         if (a.M <= 2 && tq2::smalln_matvec_preferred(a.M, N, K, dev)) which = 7;
         else if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
         else if (gemm_wins && tq2::gemm_tc05_supported(a.M, N, K, dev)) which = 6;
@@ -157,6 +215,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     } else if (impl == 7 && !tq2::smalln_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
     }
+    if ((st = maybe_convert_first(a, which, ws, ws_bytes, dev)) != TQ2_OK) return st;
     cudaError_t e = (which == 1)   ? tq2::launch_matvec_mma(a, dev)
                     : (which == 4) ? tq2::launch_matvec_ps(a, dev)
                     : (which == 6) ? tq2::launch_gemm_tc05(a, dev)
@@ -210,9 +269,8 @@ tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, const uin
                       void *workspace, size_t workspace_bytes, uint32_t *d_status,
                       tq2_stream_t stream)
 {
-    (void)workspace;
-    (void)workspace_bytes;
-    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, 0.0f, d_status, stream, 0);
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, 0.0f, workspace, workspace_bytes, d_status,
+                         stream, 0);
 }
 
 tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
@@ -220,9 +278,8 @@ tq2_status tq2_matvec_impl(const uint16_t *x, int64_t M, const uint8_t *qs, cons
                            void *workspace, size_t workspace_bytes, uint32_t *d_status,
                            tq2_stream_t stream, int impl)
 {
-    (void)workspace;
-    (void)workspace_bytes;
-    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, 0.0f, d_status, stream, impl);
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, 0.0f, workspace, workspace_bytes, d_status,
+                         stream, impl);
 }
 
 tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
@@ -230,9 +287,8 @@ tq2_status tq2_matvec_requant(const uint16_t *x, int64_t M, const uint8_t *qs, c
                               float out_scale, void *workspace, size_t workspace_bytes,
                               uint32_t *d_status, tq2_stream_t stream, int impl)
 {
-    (void)workspace;
-    (void)workspace_bytes;
-    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, d_status, stream, impl);
+    return matvec_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, workspace, workspace_bytes, d_status,
+                         stream, impl);
 }
 
 size_t tq2_trace_size(void) { return tq2::trace_bytes(); }
@@ -252,7 +308,7 @@ tq2_status tq2_test_matvec_stall(const uint16_t *x, int64_t M, const uint8_t *qs
     if (stall_stage < 0) return TQ2_ERR_ARG;
     if (wait_limit_us < 1 || wait_limit_us > 200000) return TQ2_ERR_ARG;
     if (d_status == nullptr) return TQ2_ERR_NULL;
-    return matvec_common(x, M, qs, d, N, K, y, TQ2_F32, 0.0f, 0.0f, d_status, stream, 1, stall_stage,
+    return matvec_common(x, M, qs, d, N, K, y, TQ2_F32, 0.0f, 0.0f, nullptr, 0, d_status, stream, 1, stall_stage,
                          (unsigned long long)wait_limit_us * 1000ull);
 }
 
@@ -340,7 +396,8 @@ tq2_status matvec_grouped_common(const uint16_t *x, int64_t M, int64_t K, int n_
     }
     // otherwise one call per matrix, same x, same stream
     for (int j = 0; j < n; ++j) {
-        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, gs[j], d_status, stream, 0);
+        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, gs[j], nullptr, 0, d_status,
+                           stream, 0);
         if (st != TQ2_OK) return st;
     }
     return TQ2_OK;
@@ -371,8 +428,9 @@ tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, i
 namespace {
 
 tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
-                       void *y, tq2_dtype y_dtype, float act_scale, float out_scale, uint32_t *d_status,
-                       tq2_stream_t stream, int impl, int stall_stage = -1, unsigned long long wait_limit_ns = 0)
+                       void *y, tq2_dtype y_dtype, float act_scale, float out_scale, void *ws, size_t ws_bytes,
+                       uint32_t *d_status, tq2_stream_t stream, int impl, int stall_stage = -1,
+                       unsigned long long wait_limit_ns = 0)
 {
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
@@ -388,6 +446,7 @@ tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const ui
     if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(d, 2)) return TQ2_ERR_ALIGN;
     if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
     if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    if ((st = check_workspace(ws, ws_bytes)) != TQ2_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t ebytes = (y_dtype == TQ2_F32 ? 4 : 2);
     if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * ebytes, s));
@@ -417,6 +476,7 @@ tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const ui
         a.stream = s;
         a.stall_stage = stall_stage;
         a.wait_limit_ns = wait_limit_ns;
+        if ((st = maybe_convert_first(a, 6, ws, ws_bytes, dev)) != TQ2_OK) return st;
         cudaError_t e = tq2::launch_gemm_tc05(a, dev);
         if (e == cudaSuccess) e = cudaGetLastError();
         return from_cuda(e);
@@ -424,7 +484,7 @@ tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const ui
     for (int64_t m0 = 0; m0 < M; m0 += 16) {
         const int64_t mc = (M - m0 < 16) ? (M - m0) : 16;
         st = matvec_common(x + m0 * K, mc, qs, d, N, K, static_cast<uint8_t *>(y) + (size_t)(m0 * N) * ebytes,
-                           y_dtype, act_scale, out_scale, d_status, stream, 0);
+                           y_dtype, act_scale, out_scale, ws, ws_bytes, d_status, stream, 0);
         if (st != TQ2_OK) return st;
     }
     return TQ2_OK;
@@ -435,10 +495,11 @@ tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const ui
 extern "C" {
 
 tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
-                    void *y, tq2_dtype y_dtype, float act_scale, float out_scale, uint32_t *d_status,
-                    tq2_stream_t stream, int impl)
+                    void *y, tq2_dtype y_dtype, float act_scale, float out_scale, void *workspace,
+                    size_t workspace_bytes, uint32_t *d_status, tq2_stream_t stream, int impl)
 {
-    return gemm_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, d_status, stream, impl);
+    return gemm_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, workspace, workspace_bytes, d_status,
+                       stream, impl);
 }
 
 tq2_status tq2_test_gemm_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
@@ -448,7 +509,7 @@ tq2_status tq2_test_gemm_stall(const uint16_t *x, int64_t M, const uint8_t *qs, 
     if (stall_stage < 0) return TQ2_ERR_ARG;
     if (wait_limit_us < 1 || wait_limit_us > 200000) return TQ2_ERR_ARG;
     if (d_status == nullptr) return TQ2_ERR_NULL;
-    return gemm_common(x, M, qs, d, N, K, y, TQ2_F32, act_scale, 0.0f, d_status, stream, 1, stall_stage,
+    return gemm_common(x, M, qs, d, N, K, y, TQ2_F32, act_scale, 0.0f, nullptr, 0, d_status, stream, 1, stall_stage,
                        (unsigned long long)wait_limit_us * 1000ull);
 }
 
@@ -493,10 +554,17 @@ tq2_status tq2_affine4_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, c
 
 size_t tq2_matvec_workspace_size(int64_t M, int64_t N, int64_t K)
 {
-    (void)M;
-    (void)N;
-    (void)K;
-    return 0;
+    if (M < 1 || M > 16 || check_nk(N, K) != TQ2_OK || N == 0 || K == 0) return 0;
+    // the automatic plan runs the pass with the GEMM only (the pre-scaled
+    // kernel would use it at M >= 9 with K >= 8192, where the GEMM runs)
+    return (gemm_preferred((int)M, N, K, true) && prepass_pays(6, (int)M, N, K)) ? codes_bytes(M, K) : 0;
+}
+
+size_t tq2_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 1 || M > ((int64_t)1 << 30) || check_nk(N, K) != TQ2_OK || N == 0 || K == 0) return 0;
+    if (M > kMaxElems / (N > K ? N : K)) return 0;
+    return codes_bytes(M, K);
 }
 
 const char *tq2_status_string(tq2_status status)

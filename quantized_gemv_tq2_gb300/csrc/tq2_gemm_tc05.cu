@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     const uint32_t sempty0 = afull0 + 8u * SB;
     const uint32_t dfull = sempty0 + 8u * SB;
     const uint32_t pready = dfull + 8u, pdone = pready + 8u;  // split K: peers' partials written / read
-    const bool prologue = p.a.act_scale != 0.0f;
+    // the x tiles are fake-quantised here unless x already holds the codes
+    const bool prologue = p.a.act_scale != 0.0f && !p.a.x_codes;
     // the x ring must be 1024-byte aligned for the 128-byte swizzle (the plan
     // reserves the slack; both rings move together)
     const uint32_t wring = (smem_addr(smem + p.off_w) + 1023u) & ~1023u;
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     if (!dok && lane == 0) report_timeout(p, abort_flag);
     tc_fence_after();
     auto store_y = [&](int m, int64_t nn, float v) {
-        if (prologue) v *= p.a.act_scale;
+        if (p.a.act_scale != 0.0f) v *= p.a.act_scale;
         v = requant_out(v, p.a.out_scale, p.a.inv_out);
         const int64_t o = (int64_t)m * N + nn;
         if (!TQ2_IN(o < (int64_t)M * N, st_w)) return;

@@ -32,7 +32,19 @@ struct MatvecArgs {
     // for it runs out and the timeout path runs.
     unsigned long long wait_limit_ns = 0;
     int stall_stage = -1;
+    // 1: x already holds the prologue's codes (fp16 integers in [-128, 127],
+    // written by launch_fq_codes), so the kernel does not convert it again;
+    // it still multiplies its sums by act_scale at the store.
+    int x_codes = 0;
 };
+
+// The prologue as a pass of its own: codes[i] = fp16(clamp(rint(x[i] *
+// inv_scale), -128, 127)) for i < n (n a multiple of 8; x and codes 16-byte
+// aligned), the same fp32 decision every kernel takes when it converts x
+// itself.  Waits for the previous kernel on the stream before reading x and
+// lets the next kernel launch (and fetch its weights) as soon as it runs.
+cudaError_t launch_fq_codes(const uint16_t *x, int64_t n, float inv_scale, uint16_t *codes, cudaStream_t stream,
+                            int device);
 
 // Tensor-core path (mma.sync on masked code words, TMA bulk staging).
 // Returns false when the shape is outside what the kernel supports

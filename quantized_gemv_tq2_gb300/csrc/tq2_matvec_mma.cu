@@ -273,6 +273,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
     uint8_t *xs = smem + p.off_xs;
     const int B = p.B;
     const bool prologue = p.a.act_scale != 0.0f;
+    const bool convert = prologue && !p.a.x_codes;  // x holds fp16 values, not yet codes
 
     // zero this warp's slots of the cross-warp partial sums
     for (int i = lane; i < nrg * kM * 16; i += 32) {
@@ -350,7 +351,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
             if (tid < nw) {
                 uint32_t raw[8] = {xpre[m][0].x, xpre[m][0].y, xpre[m][0].z, xpre[m][0].w,
                                    xpre[m][1].x, xpre[m][1].y, xpre[m][1].z, xpre[m][1].w};
-                if (prologue) {
+                if (convert) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[q]));
@@ -429,7 +430,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
                 bm[j] = b * kM + m;
                 uint32_t raw[8] = {xv[j][0].x, xv[j][0].y, xv[j][0].z, xv[j][0].w,
                                    xv[j][1].x, xv[j][1].y, xv[j][1].z, xv[j][1].w};
-                if (prologue) {
+                if (convert) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[q]));

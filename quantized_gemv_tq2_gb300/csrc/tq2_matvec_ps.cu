@@ -150,7 +150,7 @@ __device__ __forceinline__ void stage_x(const PsPlan &p, int kb0, int nbx, uint3
 {
     const int M = p.a.M;
     const int64_t K = p.a.K;
-    const bool prologue = p.a.act_scale != 0.0f;
+    const bool convert = p.a.act_scale != 0.0f && !p.a.x_codes;  // x holds fp16 values, not yet codes
     const int hw = lane >> 4, wi = lane & 15;
     const int t = wi >> 2, jw = wi & 3;
     const uint32_t half_mask = hw ? 0xFFFF0000u : 0x0000FFFFu;
@@ -195,7 +195,7 @@ __device__ __forceinline__ void stage_x(const PsPlan &p, int kb0, int nbx, uint3
 #pragma unroll
                 for (int q = 0; q < 8; ++q) r[q] = 0u;
             }
-            if (prologue) {
+            if (convert) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r[q]));

@@ -28,6 +28,7 @@ matvec_simt_kernel(MatvecArgs a)
     const int64_t B = a.K / 256;      // blocks per row
     const int64_t nchunks = a.K / 64; // 16-byte chunks (64 codes) per row
     const bool prologue = a.act_scale != 0.0f;
+    const bool convert = prologue && !a.x_codes;  // x holds fp16 values, not yet codes
     for (int64_t n = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); n < a.N;
          n += (int64_t)gridDim.x * warps) {
         float acc[kM];
@@ -52,7 +53,7 @@ matvec_simt_kernel(MatvecArgs a)
                     for (int j = 0; j < 16; ++j) {
                         const uint16_t hb = (uint16_t)(xw[j >> 1] >> (16 * (j & 1)));
                         float xf = __half2float(__ushort_as_half(hb));
-                        if (prologue) xf = fq_code(xf, a.inv_scale);
+                        if (convert) xf = fq_code(xf, a.inv_scale);
                         const float wv = (float)((int)((w4[wi] >> (2 * j)) & 3u) - 1);
                         part = fmaf(xf, wv, part);
                     }

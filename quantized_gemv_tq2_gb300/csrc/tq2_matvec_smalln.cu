@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_smalln_kernel(const Matvec
     const int nw = (int)(K / 16);   // 16-code words per row
     const int B = (int)(K / 256);
     const bool prologue = a.act_scale != 0.0f;
+    const bool convert = prologue && !a.x_codes;  // x holds fp16 values, not yet codes
 
     asm volatile("griddepcontrol.launch_dependents;");
 
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_smalln_kernel(const Matvec
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float lo = h2f((uint16_t)(hw[j] & 0xffffu)), hi = h2f((uint16_t)(hw[j] >> 16));
-                if (prologue) {
+                if (convert) {
                     lo = fq_code(lo, a.inv_scale);
                     hi = fq_code(hi, a.inv_scale);
                 }

@@ -130,7 +130,8 @@ def gemm():
     cases = [(17, 128, 256), (64, 100, 512), (130, 257, 768), (300, 300, 1024), (16, 512, 4096),
              (16, 16384, 1024), (200, 2048, 1024), (2048, 256, 4096), (512, 4096, 4096)]
     for M, N, K in cases:
-        for prologue in (False, True):
+        # prologue in every tile (no workspace), or as a pass of its own where it pays
+        for prologue, ws in ((False, None), (True, None), (True, "auto")):
             seed = M + N + K + int(prologue)
             codes = syn.codes(seed, N, K)
             qs_h, _ = oracle.pack(codes)
@@ -138,12 +139,12 @@ def gemm():
             x_h = syn.activations(seed, M, K, heavy=prologue)
             s = float(syn.act_scale(seed)) if prologue else 0.0
             st = torch.zeros(1, dtype=torch.int32, device="cuda")
-            y = tq2.gemm(dev(x_h), dev(qs_h), dev(d_h), act_scale=s, status=st, impl=1)
-            check_status(st, f"gemm M={M} N={N} K={K} prologue={prologue}")
+            y = tq2.gemm(dev(x_h), dev(qs_h), dev(d_h), act_scale=s, status=st, impl=1, workspace=ws)
+            check_status(st, f"gemm M={M} N={N} K={K} prologue={prologue} workspace={ws}")
             rows = sample_rows(N, 48, seed=M) if N > 512 else np.arange(N)
             y_ref, tol = oracle.matvec_rows(x_h, qs_h, d_h, K, rows, act_scale=s)
             assert_within_tolerance(host(y).astype(np.float64)[:, rows], y_ref, tol,
-                                    f"gemm M={M} N={N} K={K} prologue={prologue}")
+                                    f"gemm M={M} N={N} K={K} prologue={prologue} workspace={ws}")
             n_calls += 1
     print(f"tcgen05 GEMM: clear, parity green ({n_calls} calls)", flush=True)
 

@@ -26,7 +26,7 @@ def test_every_declared_symbol_is_exported(L):
                           "tq2_matvec_impl", "tq2_matvec_requant", "tq2_gemm",
                           "tq2_affine4_matvec", "tq2_matvec_workspace_size", "tq2_status_string", "tq2_version",
                           "tq2_test_matvec_stall", "tq2_matvec_grouped_requant", "tq2_test_gemm_stall",
-                          "tq2_trace_size", "tq2_trace_read"}
+                          "tq2_trace_size", "tq2_trace_read", "tq2_gemm_workspace_size"}
     for n in names:
         assert hasattr(L, n), n  # dlsym succeeds
 
@@ -45,10 +45,44 @@ def test_version_and_status_strings(L):
     assert tq2.matvec_workspace_size(1, 4096, 4096) == 0
 
 
-def mv(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, st=NUL, impl=None):
+def test_workspace_sizes():
+    """2 M K bytes (the prologue's codes as fp16) where the automatic plan
+    runs the prologue as a pass of its own: with the tcgen05 GEMM when it
+    has more than 4 weight tiles (N > 512) -- down-sized K from M = 8, the
+    other GEMM-preferred shapes -- else 0; tq2_gemm_workspace_size is 2 M K
+    for every valid shape (enough for every plan)."""
+    ws = tq2.matvec_workspace_size
+    assert ws(1, 16384, 4096) == 0 and ws(2, 4096, 16384) == 0   # the M <= 2 kernels
+    assert ws(6, 4096, 16384) == 0                               # the pre-scaled kernel
+    assert ws(8, 4096, 16384) == 2 * 8 * 16384                   # the GEMM, given the pass
+    assert ws(9, 4096, 16384) == 2 * 9 * 16384
+    assert ws(12, 4096, 4096) == 2 * 12 * 4096
+    assert ws(11, 4096, 4096) == 0                               # the pre-scaled kernel at K = 4096
+    assert ws(16, 256, 4096) == 0                                # the GEMM on two weight tiles
+    assert ws(16, 16384, 4096) == 0                              # the pre-scaled kernel
+    assert ws(0, 32, 256) == 0 and ws(17, 32, 256) == 0 and ws(8, 4096, 300) == 0
+    gs = tq2.gemm_workspace_size
+    assert gs(1, 32, 256) == 512 and gs(2048, 16384, 4096) == 2 * 2048 * 4096
+    assert gs(0, 32, 256) == 0 and gs(5, 32, 300) == 0 and gs(5, 0, 256) == 0 and gs(2 ** 31, 32, 256) == 0
+
+
+def mv(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, st=NUL, impl=None, ws=NUL, wsb=0):
     if impl is None:
-        return L.tq2_matvec(x, M, qs, d, N, K, y, yd, s, NUL, 0, st, S)
-    return L.tq2_matvec_impl(x, M, qs, d, N, K, y, yd, s, NUL, 0, st, S, impl)
+        return L.tq2_matvec(x, M, qs, d, N, K, y, yd, s, ws, wsb, st, S)
+    return L.tq2_matvec_impl(x, M, qs, d, N, K, y, yd, s, ws, wsb, st, S, impl)
+
+
+def test_workspace_arguments_are_checked(L):
+    """A workspace of > 0 bytes must be a non-NULL, 16-byte aligned pointer
+    (0 bytes: none, whatever the pointer)."""
+    assert mv(L, ws=NUL, wsb=64, s=0.5) == NULL
+    assert mv(L, ws=A2, wsb=64, s=0.5) == ALIGN
+    assert mv(L, ws=NUL, wsb=64) == NULL       # checked with or without the prologue
+    assert mv(L, ws=A2, wsb=64, impl=4, M=9) == ALIGN
+    assert rq(L, ws=A2, wsb=64) == ALIGN
+    assert gm(L, ws=NUL, wsb=64) == NULL
+    assert gm(L, ws=A2, wsb=64, s=0.5) == ALIGN
+    assert gm(L, ws=A2, wsb=0, M=0, x=NUL, y=NUL) == OK  # an empty call checks nothing more
 
 
 def test_matvec_rejects_bad_shapes(L):
@@ -74,8 +108,8 @@ def test_matvec_rejects_bad_dtype_and_args(L):
     assert mv(L, impl=4, M=17) == SHAPE  # the pre-scaled kernel takes M <= 16, as the API
 
 
-def rq(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, so=0.5, st=NUL, impl=0):
-    return L.tq2_matvec_requant(x, M, qs, d, N, K, y, yd, s, so, NUL, 0, st, S, impl)
+def rq(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, so=0.5, st=NUL, impl=0, ws=NUL, wsb=0):
+    return L.tq2_matvec_requant(x, M, qs, d, N, K, y, yd, s, so, ws, wsb, st, S, impl)
 
 
 def test_requant_rejects_bad_arguments(L):
@@ -94,8 +128,8 @@ def test_requant_rejects_bad_arguments(L):
     assert rq(L, N=0, qs=NUL, d=NUL, y=NUL, so=0.0) == OK
 
 
-def gm(L, x=A16, M=64, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, so=0.0, st=NUL, impl=0):
-    return L.tq2_gemm(x, M, qs, d, N, K, y, yd, s, so, st, S, impl)
+def gm(L, x=A16, M=64, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, so=0.0, st=NUL, impl=0, ws=NUL, wsb=0):
+    return L.tq2_gemm(x, M, qs, d, N, K, y, yd, s, so, ws, wsb, st, S, impl)
 
 
 def test_gemm_rejects_bad_arguments(L):

@@ -23,12 +23,12 @@ def T():
     return torch
 
 
-def _gemm(T, case, impl, y_dtype=0, out_scale=0.0):
+def _gemm(T, case, impl, y_dtype=0, out_scale=0.0, workspace="auto"):
     import quantized_gemv_tq2_gb300 as tq2
     x, qs, d = case.device()
     st = T.zeros(1, dtype=T.int32, device="cuda")
     out = GuardedOutput(case.M, case.N, y_dtype)  # canaries on both sides of y
-    tq2.gemm(x, qs, d, y=out.y, act_scale=case.s, out_scale=out_scale, status=st, impl=impl)
+    tq2.gemm(x, qs, d, y=out.y, act_scale=case.s, out_scale=out_scale, status=st, impl=impl, workspace=workspace)
     T.cuda.synchronize()
     assert int(st.item()) == 0
     out.check(f"gemm impl={impl} M={case.M} N={case.N} K={case.K}")
@@ -70,10 +70,13 @@ def test_gemm_one_hot_is_exact(T):
         assert np.array_equal(y, ye), f"impl={impl}: {int((y != ye).sum())} elements differ"
 
 
-@pytest.mark.parametrize("M,N,K", [(40, 200, 2048), (130, 257, 768), (300, 128, 4096)])
+@pytest.mark.parametrize("M,N,K", [(40, 200, 2048), (130, 257, 768), (300, 128, 4096), (24, 1100, 1024)])
 def test_gemm_prologue_and_requant(T, M, N, K):
-    """The fused int8 prologue (x fake-quantised in shared memory on the
-    tcgen05 path) and the requantisation at store, both paths."""
+    """The int8 prologue -- x fake-quantised in shared memory in every tile
+    of the tcgen05 path (no workspace), or converted once by a pass of its
+    own where that pays (a workspace: M > 64 or N > 512) -- and the
+    requantisation at store, both paths; the two prologue plans give the
+    same bits."""
     from test_gpu_requant import check_requant
     case = Case(seed=9 + M, M=M, N=N, K=K, heavy=True, prologue=True)
     y_ref, tol = case.reference()
@@ -81,6 +84,7 @@ def test_gemm_prologue_and_requant(T, M, N, K):
     for impl in (1, 0, 2):
         y = _gemm(T, case, impl)
         assert_within_tolerance(y, y_ref, tol, f"prologue impl={impl}")
+        assert np.array_equal(y, _gemm(T, case, impl, workspace=None)), f"plans differ, impl={impl}"
         for yd in (0, 1):
             yq = _gemm(T, case, impl, y_dtype=yd, out_scale=s_o)
             check_requant(yq.astype(np.float32 if yd == 0 else np.float16), y_ref, tol, s_o, yd,
