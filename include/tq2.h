@@ -292,6 +292,33 @@ TQ2_API tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, con
 TQ2_API size_t tq2_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
+ * tq2_gemm_static_ws -- tq2_gemm for callers that must not allocate: the
+ * workspace of the prologue's pass is a static device array inside this
+ * library (16 MiB per device: the codes of M x K <= 2^23 activations).
+ * None of the pages has a counterpart: this is an interface convenience
+ * around the same kernels, with the same results bit for bit as tq2_gemm
+ * given a workspace of tq2_gemm_workspace_size bytes.
+ *   Arguments, results and errors as tq2_gemm without the workspace
+ *   arguments; in addition, with act_scale > 0 and M x K > 2^23:
+ *   TQ2_ERR_SHAPE (nothing enqueued; tq2_gemm with a workspace of the
+ *   caller's has no such limit).
+ * Set-up: the first call with act_scale > 0 on a device takes the array's
+ * address there (cudaGetSymbolAddress, which may load the library's module;
+ * its failure returns TQ2_ERR_CUDA) and keeps it; make that first call before
+ * capturing a stream into a CUDA graph.  A later cudaDeviceReset invalidates
+ * the kept address: do not use this call after one.
+ * Nothing here allocates, and nothing in the array needs to start at zero:
+ * each call writes every code it reads before reading it.
+ * Concurrency: calls on one stream are ordered (each call's pass waits for
+ * the previous kernel on the stream before it writes); calls that may
+ * overlap -- on different streams, or from several host threads without
+ * stream order between them -- race on the one array and must not be made.
+ */
+TQ2_API tq2_status tq2_gemm_static_ws(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
+                                      int64_t K, void *y, tq2_dtype y_dtype, float act_scale, float out_scale,
+                                      uint32_t *d_status, tq2_stream_t stream, int impl);
+
+/*
  * tq2_affine4_matvec -- the affine-int4 sibling on the same skeleton
  * ("Custom Metal kernels" page, the note on asymmetric (zero-point) int4: a
  * fused affine-int4 matvec factors the zero point out, acc += s * (dot -

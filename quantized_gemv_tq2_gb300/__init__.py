@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "TQ2Error", "lib", "load", "declared_symbols",
-    "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "gemm", "affine4_matvec",
+    "pack", "unpack", "from_dense", "matvec", "matvec_grouped", "gemm", "gemm_static_ws", "affine4_matvec",
     "matvec_workspace_size", "gemm_workspace_size",
     "status_string", "version",
     "F32", "F16", "FLAG_BAD_CODE", "FLAG_NONFINITE", "FLAG_INEXACT", "FLAG_TIMEOUT", "FLAG_BOUNDS",
@@ -92,6 +92,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_trace_read.argtypes = [P, SZ]
         L.tq2_matvec_workspace_size.restype = SZ
         L.tq2_gemm_workspace_size.argtypes = [I64, I64, I64]
+        L.tq2_gemm_static_ws.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, P, I32]
         L.tq2_gemm_workspace_size.restype = SZ
         L.tq2_status_string.argtypes = [I32]
         L.tq2_status_string.restype = ctypes.c_char_p
@@ -100,7 +101,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_last_cuda_error.restype = ctypes.c_char_p
         for fn in ("tq2_pack", "tq2_unpack", "tq2_from_dense", "tq2_matvec", "tq2_matvec_impl",
                    "tq2_matvec_requant", "tq2_matvec_grouped", "tq2_matvec_grouped_requant", "tq2_gemm",
-                   "tq2_affine4_matvec",
+                   "tq2_gemm_static_ws", "tq2_affine4_matvec",
                    "tq2_test_matvec_stall", "tq2_test_gemm_stall", "tq2_trace_read", "tq2_version"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
@@ -324,6 +325,26 @@ def gemm(x, qs, d, y=None, y_dtype=None, act_scale: float = 0.0, out_scale: floa
     _check(L.tq2_gemm(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
                       float(out_scale), ws_ptr, ws_bytes, _ptr(status), _stream_ptr(stream), int(impl)),
            "tq2_gemm")
+    return y
+
+
+def gemm_static_ws(x, qs, d, y=None, y_dtype=None, act_scale: float = 0.0, out_scale: float = 0.0, status=None,
+                   stream=None, impl: int = 0):
+    """tq2_gemm_static_ws: gemm whose prologue pass uses the library's static
+    scratch (M * K <= 2**23 with the prologue) instead of a workspace."""
+    torch = _torch()
+    M, K = x.shape
+    N = qs.shape[0]
+    if x.dtype != torch.float16 or d.dtype != torch.float16 or qs.dtype != torch.uint8:
+        raise TypeError("x and d must be float16, qs uint8")
+    if y is None:
+        dt = torch.float32 if (y_dtype in (None, F32, torch.float32)) else torch.float16
+        y = torch.empty((M, N), dtype=dt, device=qs.device)
+    ycode = F32 if y.dtype == torch.float32 else F16
+    _need_cuda(x, qs, d, y, status)
+    _check(load().tq2_gemm_static_ws(_ptr(x), M, _ptr(qs), _ptr(d), N, K, _ptr(y), ycode, float(act_scale),
+                                     float(out_scale), _ptr(status), _stream_ptr(stream), int(impl)),
+           "tq2_gemm_static_ws")
     return y
 
 

@@ -427,11 +427,13 @@ tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, i
 
 namespace {
 
-tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
-                       void *y, tq2_dtype y_dtype, float act_scale, float out_scale, void *ws, size_t ws_bytes,
-                       uint32_t *d_status, tq2_stream_t stream, int impl, int stall_stage = -1,
-                       unsigned long long wait_limit_ns = 0)
+// The host-side checks of tq2_gemm (no CUDA call); TQ2_OK with *done set
+// when the call has nothing to do.
+tq2_status gemm_check(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
+                      void *y, tq2_dtype y_dtype, float act_scale, float out_scale, void *ws, size_t ws_bytes,
+                      uint32_t *d_status, int impl, bool *done)
 {
+    *done = true;
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
     if (M < 0 || M > ((int64_t)1 << 30)) return TQ2_ERR_SHAPE;
@@ -447,6 +449,18 @@ tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const ui
     if (!aligned(y, y_dtype == TQ2_F32 ? 4 : 2)) return TQ2_ERR_ALIGN;
     if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
     if ((st = check_workspace(ws, ws_bytes)) != TQ2_OK) return st;
+    *done = false;
+    return TQ2_OK;
+}
+
+tq2_status gemm_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N, int64_t K,
+                       void *y, tq2_dtype y_dtype, float act_scale, float out_scale, void *ws, size_t ws_bytes,
+                       uint32_t *d_status, tq2_stream_t stream, int impl, int stall_stage = -1,
+                       unsigned long long wait_limit_ns = 0)
+{
+    bool done = true;
+    tq2_status st = gemm_check(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, ws, ws_bytes, d_status, impl, &done);
+    if (st != TQ2_OK || done) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t ebytes = (y_dtype == TQ2_F32 ? 4 : 2);
     if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * ebytes, s));
@@ -500,6 +514,27 @@ tq2_status tq2_gemm(const uint16_t *x, int64_t M, const uint8_t *qs, const uint1
 {
     return gemm_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, workspace, workspace_bytes, d_status,
                        stream, impl);
+}
+
+tq2_status tq2_gemm_static_ws(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,
+                              int64_t K, void *y, tq2_dtype y_dtype, float act_scale, float out_scale,
+                              uint32_t *d_status, tq2_stream_t stream, int impl)
+{
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    bool done = true;
+    tq2_status st = gemm_check(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, nullptr, 0, d_status, impl, &done);
+    if (st != TQ2_OK || done) return st;
+    if (act_scale > 0.0f && K > 0) {
+        // the codes of M x K activations must fit the static scratch
+        if (M > (int64_t)(tq2::kStaticScratchBytes / 2) / K) return TQ2_ERR_SHAPE;
+        int dev = 0;
+        st = current_device(&dev);
+        if (st != TQ2_OK) return st;
+        if ((st = from_cuda(tq2::static_codes_scratch(dev, &ws))) != TQ2_OK) return st;
+        ws_bytes = tq2::kStaticScratchBytes;
+    }
+    return gemm_common(x, M, qs, d, N, K, y, y_dtype, act_scale, out_scale, ws, ws_bytes, d_status, stream, impl);
 }
 
 tq2_status tq2_test_gemm_stall(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d, int64_t N,

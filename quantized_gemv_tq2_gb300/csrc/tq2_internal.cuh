@@ -46,6 +46,11 @@ struct MatvecArgs {
 cudaError_t launch_fq_codes(const uint16_t *x, int64_t n, float inv_scale, uint16_t *codes, cudaStream_t stream,
                             int device);
 
+// The static scratch of tq2_gemm_static_ws: 16 MiB (the codes of 2^23
+// activations), its address taken once per device (cudaGetSymbolAddress).
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
+cudaError_t static_codes_scratch(int device, void **ptr);
+
 // Tensor-core path (mma.sync on masked code words, TMA bulk staging).
 // Returns false when the shape is outside what the kernel supports
 // (M > 2 or shared memory would not fit); nothing is launched then.

@@ -12,6 +12,8 @@
 // bits.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "tq2_device.cuh"
 #include "tq2_internal.cuh"
 
@@ -56,7 +58,29 @@ __global__ void __launch_bounds__(kFqThreads) fq_codes_kernel(const uint4 *__res
     }
 }
 
+// Scratch of the entry point that allocates nothing (tq2_gemm_static_ws):
+// one array per device, in the library's own module, for the codes of at
+// most kStaticScratchBytes / 2 activations.
+static __device__ __align__(256) uint16_t g_static_codes[kStaticScratchBytes / 2];
+
+std::atomic<uintptr_t> g_static_codes_addr[64];
+
 }  // namespace
+
+cudaError_t static_codes_scratch(int device, void **ptr)
+{
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    uintptr_t v = g_static_codes_addr[device].load(std::memory_order_acquire);
+    if (v == 0) {  // once per device: the array's address in this device's context
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_codes);
+        if (e != cudaSuccess) return e;
+        v = reinterpret_cast<uintptr_t>(p);
+        g_static_codes_addr[device].store(v, std::memory_order_release);
+    }
+    *ptr = reinterpret_cast<void *>(v);
+    return cudaSuccess;
+}
 
 cudaError_t launch_fq_codes(const uint16_t *x, int64_t n, float inv_scale, uint16_t *codes, cudaStream_t stream,
                             int device)
