@@ -322,32 +322,38 @@ def _bf16_peak():
 def prefill_gemm(torch, tq2, st, stream, M_list=(512, 2048)):
     """tq2_gemm (tcgen05) on the layer shapes with M activation rows (a prompt
     chunk): us per call and TFLOP/s (2 M N K), against the measured dense
-    bf16 tensor peak (fp16 runs at the same rate)."""
+    bf16 tensor peak (fp16 runs at the same rate).  Also with the int8
+    prologue, run as a pass of its own into a workspace ("_prologue") and
+    inside every weight tile with no workspace ("_prologue_in_tile")."""
     import tq2_synth as syn
     peak, src = _bf16_peak()
     out = {"peak_tflops": peak, "peak_source": src}
     dev = st["X"].device
+    s_act = float(syn.act_scale(SEED, linear=0))
     for gname, names in SHAPE_GROUPS.items():
         i = [j for j, (L, n, N, K) in enumerate(st["lin"]) if n in names][0]
         N, K = st["lin"][i][2], st["lin"][i][3]
         for M in M_list:
             x = torch.from_numpy(syn.activations(SEED + 11, M, K, linear=0)).to(dev)
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            with torch.cuda.stream(stream):
-                for _ in range(3):
-                    tq2.gemm(x, st["qs"][i], st["d"][i], y=y)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                reps = 20
-                e0.record(stream)
-                for _ in range(reps):
-                    tq2.gemm(x, st["qs"][i], st["d"][i], y=y)
-                e1.record(stream)
-            stream.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
-            out[f"{gname}_M{M}"] = dict(us_per_call=us, tflops=tf, frac_of_peak=tf / peak)
-            del x, y
+            ws = torch.empty(tq2.gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            for tag, kw in (("", dict(workspace=None)), ("_prologue", dict(act_scale=s_act, workspace=ws)),
+                            ("_prologue_in_tile", dict(act_scale=s_act, workspace=None))):
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        tq2.gemm(x, st["qs"][i], st["d"][i], y=y, **kw)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    reps = 20
+                    e0.record(stream)
+                    for _ in range(reps):
+                        tq2.gemm(x, st["qs"][i], st["d"][i], y=y, **kw)
+                    e1.record(stream)
+                stream.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / reps
+                tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+                out[f"{gname}_M{M}{tag}"] = dict(us_per_call=us, tflops=tf, frac_of_peak=tf / peak)
+            del x, y, ws
     return out
 
 
@@ -769,8 +775,10 @@ CASES = {"gateup": (16384, 4096), "down": (4096, 16384), "qo": (4096, 4096), "kv
 def run_case(args):
     """A small case for ncu: `copies` distinct weight sets of one shape (more
     than L2 in total for the big shapes), `launches` eager tq2_matvec calls
-    (tq2_gemm when M > 16) round-robin over them.  Prints the mean wall time per call (not a bench
-    value: the calls are eager and may run under a profiler)."""
+    (tq2_gemm when M > 16) round-robin over them, with the int8 prologue when
+    --act-scale > 0 (and a workspace: its pass where that pays).  Prints the
+    mean wall time per call (not a bench value: the calls are eager and may
+    run under a profiler)."""
     import torch
     import quantized_gemv_tq2_gb300 as tq2
     import tq2_synth as syn
@@ -807,13 +815,13 @@ def run_case(args):
     for i in range(args.launches):
         qs, d = ws[i % len(ws)]
         if args.M > 16:  # prefill-sized M: tq2_gemm
-            tq2.gemm(x, qs, d, y=y)
+            tq2.gemm(x, qs, d, y=y, act_scale=args.act_scale)
         else:
-            tq2.matvec(x, qs, d, y=y, impl=args.case_impl)
+            tq2.matvec(x, qs, d, y=y, impl=args.case_impl, act_scale=args.act_scale)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / args.launches
     print(json.dumps({"case": args.case, "N": N, "K": K, "M": args.M, "copies": args.copies,
-                      "launches": args.launches, "impl": args.case_impl,
+                      "launches": args.launches, "impl": args.case_impl, "act_scale": args.act_scale,
                       "wall_us_per_call_eager": round(dt * 1e6, 2)}))
 
 
@@ -951,6 +959,8 @@ def main():
     ap.add_argument("--copies", type=int, default=8)
     ap.add_argument("--launches", type=int, default=8)
     ap.add_argument("--case-impl", type=int, default=0)
+    ap.add_argument("--act-scale", type=float, default=0.0,
+                    help="with --case: the int8 prologue's scale (0: none)")
     ap.add_argument("--affine4-group", type=int, default=0,
                     help="with --case: run tq2_affine4_matvec with this group size instead")
     ap.add_argument("--phases", choices=sorted(CASES),
