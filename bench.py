@@ -214,15 +214,15 @@ def grouped_stack(st):
     return calls, nbytes
 
 
-def capture_grouped(torch, tq2, calls, stream):
+def capture_grouped(torch, tq2, calls, stream, act_scale=0.0, workspace=None):
     with torch.cuda.stream(stream):
         for x, qs, d, ys in calls:  # eager warm-up
-            tq2.matvec_grouped(x, qs, d, y_list=ys)
+            tq2.matvec_grouped(x, qs, d, y_list=ys, act_scale=act_scale, workspace=workspace)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for x, qs, d, ys in calls:
-                tq2.matvec_grouped(x, qs, d, y_list=ys)
+                tq2.matvec_grouped(x, qs, d, y_list=ys, act_scale=act_scale, workspace=workspace)
     stream.synchronize()
     return g
 
@@ -307,6 +307,48 @@ def shape_graphs(torch, tq2, st, stream, M_list=(1,), impl=0, groups=None, heavy
                                    repeats=repeats)
             del g, ys
         del pool
+    return out
+
+
+def grouped_sweep(torch, tq2, st, stream, M_list=(2, 4, 8, 9, 12, 16), repeats=11):
+    """tq2_matvec_grouped on q/k/v and on gate/up at M activation rows, back
+    to back over distinct weight groups totalling at least 4x L2 (the stack's
+    own, then copies), with and without the int8 prologue (one shared
+    workspace: x converted once per group where the group runs as
+    consecutive calls).  us per group (median of the replays) and GB/s of
+    the group's algorithmic bytes."""
+    import tq2_synth as syn
+    out = {}
+    dev = st["X"].device
+    K = 4096
+    for gname, names in (("qkv", ("q", "k", "v")), ("gateup", ("gate", "up"))):
+        by_layer = {}  # the stack's seven linears per layer, in order
+        for i, (L, n, N, K_) in enumerate(st["lin"]):
+            by_layer.setdefault(i // 7, {})[n] = i
+        groups = [[(st["qs"][lay[n]], st["d"][lay[n]]) for n in names] for lay in by_layer.values()]
+        Ns = [st["lin"][by_layer[0][n]][2] for n in names]
+        per = sum(N * K // 4 + 2 * N * (K // 256) for N in Ns)
+        j = 0
+        while len(groups) * per < 4 * L2_BYTES:
+            groups.append([(q.clone(), d.clone()) for q, d in groups[j]])
+            j += 1
+        s_act = float(syn.act_scale(SEED, linear=0))
+        for M in M_list:
+            x = torch.from_numpy(syn.activations(SEED + 13, M, K, linear=0, heavy=True)).to(dev)
+            ys = [[torch.empty((M, N), dtype=torch.float32, device=dev) for N in Ns] for _ in groups]
+            calls = [(x, [q for q, _ in g], [d for _, d in g], y) for g, y in zip(groups, ys)]
+            ws = torch.empty(2 * M * K, dtype=torch.uint8, device=dev)
+            nbytes = sum(linear_bytes(M, N, K) for N in Ns)
+            for tag, s, w in (("", 0.0, None), ("_prologue", s_act, ws)):
+                g = capture_grouped(torch, tq2, calls, stream, act_scale=s, workspace=w)
+                time_graph(torch, g, stream, 2, 1)
+                per_rep = sorted(1e3 * time_graph(torch, g, stream, 1, 0) / len(groups) for _ in range(repeats))
+                med = statistics.median(per_rep)
+                out[f"{gname}_M{M}{tag}"] = dict(us_per_group=med, gbs=nbytes / (med * 1e-6) / 1e9,
+                                                 distinct_groups=len(groups))
+                del g
+            del ys, calls, ws
+        del groups
     return out
 
 
@@ -688,6 +730,7 @@ def run_gpu(args):
         sweep_h = shape_graphs(torch, tq2, st, stream, M_list=(1, 2, 4, 8, 16),
                                groups=("gateup_16384x4096", "down_4096x16384"), heavy=True, prologue=True)
         extras["m_sweep_heavy_prologue"] = {f"{k[0]}_M{k[1]}": v for k, v in sweep_h.items()}
+        extras["grouped_m_sweep"] = grouped_sweep(torch, tq2, st, stream)
         extras["prefill_gemm"] = prefill_gemm(torch, tq2, st, stream)
         extras["affine4_m1"] = affine4_shapes(torch, tq2, stream)
 

@@ -172,20 +172,38 @@ TQ2_API tq2_status tq2_matvec(const uint16_t *x, int64_t M, const uint8_t *qs, c
  *              aligned), and the row counts N_j >= 0 (N_j = 0: y_j untouched).
  *   y_dtype, act_scale, d_status, stream  as tq2_matvec (one act_scale for
  *              the shared x).
+ *   workspace, workspace_bytes  optional, as for tq2_matvec; the size from
+ *              tq2_matvec_grouped_workspace_size.
  *
  * Results equal n_mats tq2_matvec calls with the same x.  They run as ONE
  * kernel launch (the CTAs split between the matrices in proportion to their
  * rows; x staged and the wait on the previous kernel paid once) when M <= 2
- * (the class-column kernel, any K), or when 3 <= M <= 8 and each matrix alone
- * would run the pre-scaled kernel (not the GEMM; any K); otherwise as
- * consecutive calls on the stream.  Errors: as tq2_matvec for every matrix (checked
- * before anything is enqueued); TQ2_ERR_ARG for n_mats out of range;
- * TQ2_ERR_NULL for a NULL array.
+ * (the class-column kernel, any K); when 3 <= M <= 8 and each matrix alone
+ * would run the pre-scaled kernel (not the GEMM; any K); and when
+ * 9 <= M <= 16, K < 8192 and either M <= 11 or some matrix has N_j <= 512
+ * (the pre-scaled kernel: q/k/v at M = 9..16 in 8.8-12.1 us against
+ * 21.6-22.8 us as separate calls on GB300).  Otherwise they run as
+ * consecutive calls on the stream.  In that case, with act_scale > 0 and a
+ * workspace, x is fake-quantised ONCE into the workspace for all the
+ * matrices (the recipe's one input quantisation shared by q/k/v, and by
+ * gate/up), and each call reads the codes; each kernel gives the same bits
+ * as converting x itself, but with a workspace a matrix's single call may
+ * take the GEMM where it otherwise would not (as for tq2_matvec).  Errors:
+ * as tq2_matvec for every matrix (checked before anything is enqueued);
+ * TQ2_ERR_ARG for n_mats out of range or a workspace smaller than the pass
+ * needs; TQ2_ERR_NULL for a NULL array.
  */
 TQ2_API tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats,
                                       const uint8_t *const *qs, const uint16_t *const *d,
                                       const int64_t *N, void *const *y, tq2_dtype y_dtype,
-                                      float act_scale, uint32_t *d_status, tq2_stream_t stream);
+                                      float act_scale, void *workspace, size_t workspace_bytes,
+                                      uint32_t *d_status, tq2_stream_t stream);
+
+/* Bytes of workspace with which tq2_matvec_grouped (and _requant) converts x
+ * once for the group (2 M K: when the matrices run as consecutive calls,
+ * M >= 3), or 0 (also for invalid arguments).  N: HOST array of n_mats row
+ * counts. */
+TQ2_API size_t tq2_matvec_grouped_workspace_size(int64_t M, int64_t K, int n_mats, const int64_t *N);
 
 /*
  * tq2_matvec_grouped_requant -- tq2_matvec_grouped with the static int8
@@ -202,8 +220,8 @@ TQ2_API tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, i
 TQ2_API tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, int n_mats,
                                               const uint8_t *const *qs, const uint16_t *const *d,
                                               const int64_t *N, void *const *y, tq2_dtype y_dtype,
-                                              float act_scale, const float *out_scale, uint32_t *d_status,
-                                              tq2_stream_t stream);
+                                              float act_scale, const float *out_scale, void *workspace,
+                                              size_t workspace_bytes, uint32_t *d_status, tq2_stream_t stream);
 
 /* Bytes of workspace with which tq2_matvec runs the prologue as a pass of
  * its own for this shape (2 M K), or 0 where it would not use one (and for

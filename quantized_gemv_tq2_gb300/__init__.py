@@ -80,8 +80,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         L.tq2_matvec.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P]
         L.tq2_matvec_impl.argtypes = [P, I64, P, P, I64, I64, P, I32, F, P, SZ, P, P, I32]
         L.tq2_matvec_requant.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
-        L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P]
-        L.tq2_matvec_grouped_requant.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P, P]
+        L.tq2_matvec_grouped.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, SZ, P, P]
+        L.tq2_matvec_grouped_requant.argtypes = [P, I64, I64, I32, P, P, P, P, I32, F, P, P, SZ, P, P]
+        L.tq2_matvec_grouped_workspace_size.argtypes = [I64, I64, I32, P]
+        L.tq2_matvec_grouped_workspace_size.restype = SZ
         L.tq2_gemm.argtypes = [P, I64, P, P, I64, I64, P, I32, F, F, P, SZ, P, P, I32]
         L.tq2_affine4_matvec.argtypes = [P, I64, P, P, P, I64, I64, I64, P, I32, P, P]
         L.tq2_test_matvec_stall.argtypes = [P, I64, P, P, I64, I64, P, P, P, I32, I32]
@@ -264,11 +266,12 @@ def matvec(x, qs, d, K=None, y=None, y_dtype=None, act_scale: float = 0.0, statu
 
 
 def matvec_grouped(x, qs_list, d_list, y_list=None, y_dtype=None, act_scale: float = 0.0,
-                   status=None, stream=None, out_scales=None):
+                   status=None, stream=None, out_scales=None, workspace="auto"):
     """[y_j] = ternary matvecs of one shared x [M,K] with several packed
     matrices (tq2_matvec_grouped): one launch when the library can group them.
     out_scales (one float per matrix) requantises each y_j to int8 at store
-    with its own scale (tq2_matvec_grouped_requant)."""
+    with its own scale (tq2_matvec_grouped_requant).  workspace as for matvec
+    (tq2_matvec_grouped_workspace_size: x converted once for the group)."""
     torch = _torch()
     if x.dim() == 1:
         x = x.view(1, -1)
@@ -289,17 +292,21 @@ def matvec_grouped(x, qs_list, d_list, y_list=None, y_dtype=None, act_scale: flo
     da = Pn(*[_ptr(d).value for d in d_list])
     ya = Pn(*[_ptr(y).value for y in y_list])
     na = (ctypes.c_int64 * n)(*[q.shape[0] for q in qs_list])
+    L = load()
+    ws_ptr, ws_bytes, _ws = _workspace(
+        workspace, act_scale,
+        lambda: L.tq2_matvec_grouped_workspace_size(M, K, n, ctypes.cast(na, ctypes.c_void_p)), x.device, stream)
     common = (_ptr(x), M, K, n, ctypes.cast(qa, ctypes.c_void_p), ctypes.cast(da, ctypes.c_void_p),
               ctypes.cast(na, ctypes.c_void_p), ctypes.cast(ya, ctypes.c_void_p), ycode, float(act_scale))
     if out_scales is None:
-        st = load().tq2_matvec_grouped(*common, _ptr(status), _stream_ptr(stream))
+        st = L.tq2_matvec_grouped(*common, ws_ptr, ws_bytes, _ptr(status), _stream_ptr(stream))
         _check(st, "tq2_matvec_grouped")
     else:
         if len(out_scales) != n:
             raise ValueError("out_scales needs one scale per matrix")
         sa = (ctypes.c_float * n)(*[float(v) for v in out_scales])
-        st = load().tq2_matvec_grouped_requant(*common, ctypes.cast(sa, ctypes.c_void_p), _ptr(status),
-                                               _stream_ptr(stream))
+        st = L.tq2_matvec_grouped_requant(*common, ctypes.cast(sa, ctypes.c_void_p), ws_ptr, ws_bytes,
+                                          _ptr(status), _stream_ptr(stream))
         _check(st, "tq2_matvec_grouped_requant")
     return y_list
 

@@ -142,7 +142,7 @@ tq2_status maybe_convert_first(tq2::MatvecArgs &a, int which, void *ws, size_t w
 tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const uint16_t *d,
                          int64_t N, int64_t K, void *y, tq2_dtype y_dtype, float act_scale,
                          float out_scale, void *ws, size_t ws_bytes, uint32_t *d_status, tq2_stream_t stream,
-                         int impl, int stall_stage = -1, unsigned long long wait_limit_ns = 0)
+                         int impl, int stall_stage = -1, unsigned long long wait_limit_ns = 0, bool x_codes = false)
 {
     tq2_status st = check_nk(N, K);
     if (st != TQ2_OK) return st;
@@ -184,6 +184,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     a.stream = s;
     a.stall_stage = stall_stage;
     a.wait_limit_ns = wait_limit_ns;
+    a.x_codes = x_codes ? 1 : 0;  // x holds the prologue's codes already (the grouped call's pass)
 
     // impl 0: for M <= 2 and a few output rows per CTA (k/v-sized N) the
     // small-N kernel, else for M <= 2 the class-column mma.sync kernel; for more rows the
@@ -200,7 +201,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     // (M = 9 starts the pre-scaled kernel's second n-tile of 8 rows).
     int which = impl;
     if (impl == 0) {
-        const bool gemm_wins = gemm_preferred(a.M, N, K, act_scale != 0.0f && ws_bytes != 0);
+        const bool gemm_wins = gemm_preferred(a.M, N, K, act_scale != 0.0f && (ws_bytes != 0 || x_codes));
         if (a.M <= 2 && tq2::smalln_matvec_preferred(a.M, N, K, dev)) which = 7;
         else if (a.M <= 2 && tq2::mma_matvec_supported(a.M, N, K, dev)) which = 1;
         else if (gemm_wins && tq2::gemm_tc05_supported(a.M, N, K, dev)) which = 6;
@@ -215,7 +216,7 @@ tq2_status matvec_common(const uint16_t *x, int64_t M, const uint8_t *qs, const 
     } else if (impl == 7 && !tq2::smalln_matvec_supported(a.M, N, K, dev)) {
         return TQ2_ERR_ARG;
     }
-    if ((st = maybe_convert_first(a, which, ws, ws_bytes, dev)) != TQ2_OK) return st;
+    if (!x_codes && (st = maybe_convert_first(a, which, ws, ws_bytes, dev)) != TQ2_OK) return st;
     cudaError_t e = (which == 1)   ? tq2::launch_matvec_mma(a, dev)
                     : (which == 4) ? tq2::launch_matvec_ps(a, dev)
                     : (which == 6) ? tq2::launch_gemm_tc05(a, dev)
@@ -318,9 +319,48 @@ namespace {
 
 // tq2_matvec_grouped and tq2_matvec_grouped_requant (out_scale: host array of
 // n_mats scales, or nullptr for none).
+// How a group of n matrices sharing x runs, before the device's own checks
+// (`pass`: the prologue is on and a workspace given):
+//   0  one launch of the class-column kernel (M <= 2);
+//   1  one launch of the pre-scaled kernel;
+//   2  consecutive single calls (with `pass`, x converted once for all).
+// M = 3..8: one launch unless a matrix's single call would take the GEMM.
+// M = 9..16: one launch saves the GEMM's per-call floor on k/v-sized
+// matrices and beats separate pre-scaled calls up to M = 11; measured on
+// GB300, us per group back to back over distinct weights, consecutive calls
+// against one launch: q/k/v 4096x4096 + 2 x 256x4096 M = 9 / 12 / 16: 21.6 /
+// 22.8 / 22.8 against 8.8 / 10.2 / 12.1 (with the prologue 24.5 / 25.7 /
+// 25.7 against 10.1 / 11.8 / 14.3); gate/up 2 x 16384x4096 M = 9 / 12 / 16:
+// 30.0 / 34.4 / 41.0 against 23.8 / 35.5 / 42.4.  At K >= 8192 the GEMM's
+// single calls are far ahead of the pre-scaled kernel (down-sized K, M >= 9).
+int grouped_plan(int64_t M, int64_t K, int n, const int64_t *N, bool pass)
+{
+    if (M <= 2) return 0;
+    if (M <= 8) {
+        for (int j = 0; j < n; ++j)
+            if (N[j] > 0 && gemm_preferred((int)M, N[j], K, pass)) return 2;
+        return 1;
+    }
+    if (K >= 8192) return 2;
+    if (M <= 11) return 1;
+    for (int j = 0; j < n; ++j)
+        if (N[j] > 0 && N[j] <= 512) return 1;
+    return 2;
+}
+
+// Whether a grouped call with the prologue and a workspace converts x once
+// for the group: when it runs as consecutive calls.  (In one launch each CTA
+// converts the x it reads: the pass measured no faster there, as for single
+// calls at M <= 8.)
+bool grouped_pass(int64_t M, int64_t K, int n, const int64_t *N)
+{
+    return M >= 3 && K > 0 && n > 1 && grouped_plan(M, K, n, N, true) == 2;
+}
+
 tq2_status matvec_grouped_common(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
                                  const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
-                                 float act_scale, const float *out_scale, uint32_t *d_status, tq2_stream_t stream)
+                                 float act_scale, const float *out_scale, void *ws, size_t ws_bytes,
+                                 uint32_t *d_status, tq2_stream_t stream)
 {
     if (n_mats < 1 || n_mats > TQ2_MAX_GROUP) return TQ2_ERR_ARG;
     if (qs == nullptr || d == nullptr || N == nullptr || y == nullptr) return TQ2_ERR_NULL;
@@ -341,6 +381,8 @@ tq2_status matvec_grouped_common(const uint16_t *x, int64_t M, int64_t K, int n_
         ++live;
     }
     if (d_status && !aligned(d_status, 4)) return TQ2_ERR_ALIGN;
+    tq2_status wst = check_workspace(ws, ws_bytes);
+    if (wst != TQ2_OK) return wst;
     if (live == 0) return TQ2_OK;
 
     const uint8_t *gq[TQ2_MAX_GROUP];
@@ -368,10 +410,9 @@ tq2_status matvec_grouped_common(const uint16_t *x, int64_t M, int64_t K, int n_
         // q/k/v grouped against separate calls at M = 4 / 8: 5.0 / 6.4 against
         // 12.9 / 17.1 us, gate/up 16.7 / 19.6 against 20.1 / 25.0 us; at
         // M = 16 gate/up grouped took 42.4 against 41.6 us
-        bool ps_each = M > 2 && M <= 8;
-        for (int j = 0; j < n; ++j) ps_each = ps_each && !gemm_preferred((int)M, gn[j], K);
-        const bool mma = M <= 2 && tq2::mma_group_supported((int)M, n, gn, K, dev);
-        const bool ps = !mma && ps_each && tq2::ps_group_supported((int)M, n, gn, K, dev);
+        const int plan = grouped_plan(M, K, n, gn, act_scale != 0.0f && ws_bytes != 0);
+        const bool mma = plan == 0 && tq2::mma_group_supported((int)M, n, gn, K, dev);
+        const bool ps = plan == 1 && tq2::ps_group_supported((int)M, n, gn, K, dev);
         if (mma || ps) {
             tq2::MatvecArgs a;
             a.x = x;
@@ -394,10 +435,24 @@ tq2_status matvec_grouped_common(const uint16_t *x, int64_t M, int64_t K, int n_
             return from_cuda(e);
         }
     }
-    // otherwise one call per matrix, same x, same stream
+    // otherwise one call per matrix, same x, same stream; with the prologue
+    // and a workspace, x is converted once for all of them (the pages'
+    // recipe: one input quantisation shared by q/k/v, one by gate/up)
+    const bool pass = act_scale != 0.0f && ws_bytes >= codes_bytes(M, K) && grouped_pass(M, K, n, gn);
+    if (act_scale != 0.0f && ws_bytes != 0 && !pass && grouped_pass(M, K, n, gn)) return TQ2_ERR_ARG;  // too small
+    if (pass) {
+        if (n == 1 && (st = current_device(&dev)) != TQ2_OK) return st;  // (n > 1 queried it above)
+        cudaError_t e = tq2::launch_fq_codes(x, M * K, 1.0f / act_scale, static_cast<uint16_t *>(ws),
+                                             reinterpret_cast<cudaStream_t>(stream), dev);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    // without the group's pass (a single matrix, or a group the device
+    // could not launch at once) each call may use the workspace by itself
+    const uint16_t *xc = pass ? static_cast<const uint16_t *>(ws) : x;
     for (int j = 0; j < n; ++j) {
-        st = matvec_common(x, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, gs[j], nullptr, 0, d_status,
-                           stream, 0);
+        st = matvec_common(xc, M, gq[j], gd[j], gn[j], K, gy[j], y_dtype, act_scale, gs[j], pass ? nullptr : ws,
+                           pass ? 0 : ws_bytes, d_status, stream, 0, -1, 0, pass);
         if (st != TQ2_OK) return st;
     }
     return TQ2_OK;
@@ -409,18 +464,29 @@ extern "C" {
 
 tq2_status tq2_matvec_grouped(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
                               const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
-                              float act_scale, uint32_t *d_status, tq2_stream_t stream)
+                              float act_scale, void *workspace, size_t workspace_bytes, uint32_t *d_status,
+                              tq2_stream_t stream)
 {
-    return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, nullptr, d_status, stream);
+    return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, nullptr, workspace,
+                                 workspace_bytes, d_status, stream);
 }
 
 tq2_status tq2_matvec_grouped_requant(const uint16_t *x, int64_t M, int64_t K, int n_mats, const uint8_t *const *qs,
                                       const uint16_t *const *d, const int64_t *N, void *const *y, tq2_dtype y_dtype,
-                                      float act_scale, const float *out_scale, uint32_t *d_status,
-                                      tq2_stream_t stream)
+                                      float act_scale, const float *out_scale, void *workspace,
+                                      size_t workspace_bytes, uint32_t *d_status, tq2_stream_t stream)
 {
     if (out_scale == nullptr) return TQ2_ERR_NULL;
-    return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, out_scale, d_status, stream);
+    return matvec_grouped_common(x, M, K, n_mats, qs, d, N, y, y_dtype, act_scale, out_scale, workspace,
+                                 workspace_bytes, d_status, stream);
+}
+
+size_t tq2_matvec_grouped_workspace_size(int64_t M, int64_t K, int n_mats, const int64_t *N)
+{
+    if (M < 1 || M > 16 || n_mats < 1 || n_mats > TQ2_MAX_GROUP || N == nullptr) return 0;
+    for (int j = 0; j < n_mats; ++j)
+        if (check_nk(N[j], K) != TQ2_OK) return 0;
+    return grouped_pass(M, K, n_mats, N) ? codes_bytes(M, K) : 0;
 }
 
 }  // extern "C"

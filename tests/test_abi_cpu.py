@@ -72,6 +72,28 @@ def mv(L, x=A16, M=1, qs=A16, d=A16, N=32, K=512, y=A16, yd=0, s=0.0, st=NUL, im
     return L.tq2_matvec_impl(x, M, qs, d, N, K, y, yd, s, ws, wsb, st, S, impl)
 
 
+def test_grouped_workspace_sizes(L):
+    """2 M K where the group runs as consecutive calls with one prologue pass
+    (M >= 12 with every N_j > 512, or K >= 8192 at M >= 9, or a matrix that
+    would take the GEMM at 3 <= M <= 8), else 0 (one launch)."""
+    def gs(M, K, Ns):
+        a = (ctypes.c_int64 * len(Ns))(*Ns)
+        return L.tq2_matvec_grouped_workspace_size(M, K, len(Ns), ctypes.cast(a, P))
+    assert gs(1, 4096, (4096, 256, 256)) == 0 and gs(2, 4096, (16384, 16384)) == 0
+    assert gs(8, 4096, (4096, 256, 256)) == 0        # one pre-scaled launch
+    assert gs(9, 4096, (4096, 256, 256)) == 0        # one pre-scaled launch up to M = 16 with k/v in it
+    assert gs(16, 4096, (4096, 256, 256)) == 0
+    assert gs(11, 4096, (16384, 16384)) == 0         # one launch up to M = 11
+    assert gs(12, 4096, (16384, 16384)) == 2 * 12 * 4096
+    assert gs(16, 4096, (16384, 16384)) == 2 * 16 * 4096
+    assert gs(9, 16384, (4096, 256)) == 2 * 9 * 16384  # K >= 8192: the GEMM's single calls
+    assert gs(8, 16384, (4096, 4096)) == 2 * 8 * 16384  # down-sized K takes the GEMM at M = 8 given the pass
+    assert gs(12, 4096, (4096,)) == 0                  # one matrix: a single call
+    assert gs(9, 300, (64,)) == 0 and gs(9, 4096, (-1,)) == 0 and gs(17, 4096, (64,)) == 0
+    assert gs(9, 4096, ()) == 0 and gs(9, 4096, (1, 2, 3, 4, 5)) == 0
+    assert L.tq2_matvec_grouped_workspace_size(9, 4096, 1, NUL) == 0
+
+
 def test_workspace_arguments_are_checked(L):
     """A workspace of > 0 bytes must be a non-NULL, 16-byte aligned pointer
     (0 bytes: none, whatever the pointer)."""
@@ -214,10 +236,11 @@ def test_grouped_rejects_bad_arguments(L):
     cast = lambda a: ctypes.cast(a, ctypes.c_void_p)
     G = lambda **k: L.tq2_matvec_grouped(k.get("x", A16), k.get("M", 1), k.get("K", 512), k.get("n", n),
                                          cast(k.get("qs", good)), cast(k.get("d", good)), cast(k.get("N", Ns)),
-                                         cast(k.get("y", ys)), k.get("yd", 0), k.get("s", 0.0), NUL, S)
+                                         cast(k.get("y", ys)), k.get("yd", 0), k.get("s", 0.0),
+                                         k.get("ws", NUL), k.get("wsb", 0), NUL, S)
     assert G(n=0) == ARG
     assert G(n=5) == ARG                          # more than TQ2_MAX_GROUP
-    assert L.tq2_matvec_grouped(A16, 1, 512, n, NUL, cast(good), cast(Ns), cast(ys), 0, 0.0, NUL, S) == NULL
+    assert L.tq2_matvec_grouped(A16, 1, 512, n, NUL, cast(good), cast(Ns), cast(ys), 0, 0.0, NUL, 0, NUL, S) == NULL
     assert G(K=300) == SHAPE
     assert G(M=17) == SHAPE
     assert G(N=(ctypes.c_int64 * n)(64, -1, 16)) == SHAPE
@@ -227,10 +250,12 @@ def test_grouped_rejects_bad_arguments(L):
     assert G(y=Pn(0x40000, 0, 0x60000)) == NULL
     assert G(x=A2) == ALIGN
     assert G(M=0) == OK                           # nothing to do
+    assert G(ws=NUL, wsb=64) == NULL              # workspace: non-NULL and 16-byte aligned when given
+    assert G(ws=A2, wsb=64, M=9, s=0.5) == ALIGN
     # the requantising variant: one finite, non-negative scale per matrix
     F3 = ctypes.c_float * n
     R = lambda sc, **k: L.tq2_matvec_grouped_requant(k.get("x", A16), k.get("M", 1), 512, n, cast(good), cast(good),
-                                                     cast(Ns), cast(ys), 0, 0.0, sc, NUL, S)
+                                                     cast(Ns), cast(ys), 0, 0.0, sc, NUL, 0, NUL, S)
     assert R(NUL) == NULL
     assert R(cast(F3(0.5, -0.1, 0.2))) == ARG
     assert R(cast(F3(0.5, float("inf"), 0.2))) == ARG

@@ -2,9 +2,12 @@
 matrices sharing x) against the CPU oracle, per matrix: one launch of the
 class-column kernel (M <= 2, any K) and of the pre-scaled kernel (M up to 16,
 K = 4096 and longer), decoder layer shapes, odd sizes and the prologue; the
-fallback to consecutive calls where a matrix would take the GEMM; each
-matrix's own output requantisation; guard bands around every y; and the
-back-to-back graph configuration the benchmark times."""
+fallback to consecutive calls where a matrix would take the GEMM, with one
+prologue pass for the whole group given a workspace; each matrix's own
+output requantisation; guard bands around every y; and the back-to-back
+graph configuration the benchmark times."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -46,9 +49,11 @@ def _mats(seed, Ns, K):
     (3, 1024, (40, 24)),              # M > 2: pre-scaled kernel, one launch
     (4, 4096, (4096, 256, 256)),      # q, k, v at M = 4 (one 16-row group x 16 blocks per stage)
     (8, 4096, (16384, 16384)),        # gate, up at M = 8
-    (16, 4096, (1000, 3000)),         # M > 8: consecutive calls
+    (16, 4096, (1000, 3000)),         # M >= 12, every N > 512: consecutive calls
+    (10, 4096, (1000, 3000)),         # M = 9..11: one pre-scaled launch (two n-tiles)
     (5, 8448, (100, 60)),             # M > 2, K > 4096
-    (12, 4096, (4096, 256, 256)),     # k/v would take the GEMM: consecutive calls
+    (12, 4096, (4096, 256, 256)),     # q/k/v at M = 12: one pre-scaled launch
+    (13, 8448, (100, 600)),           # K >= 8192 at M >= 9: consecutive calls (the GEMM)
 ])
 @pytest.mark.parametrize("prologue", [False, True])
 @pytest.mark.parametrize("yd", [0, 1])
@@ -77,7 +82,8 @@ def test_grouped_matches_oracle(T, M, K, Ns, prologue, yd):
     (2, 8448, (70, 50)),
     (4, 4096, (4096, 256, 256)),
     (8, 4096, (16384, 16384)),
-    (12, 4096, (4096, 256, 256)),     # consecutive calls, each with its own scale
+    (12, 4096, (4096, 256, 256)),     # one pre-scaled launch at M = 12
+    (14, 4096, (1000, 700)),          # consecutive calls, each with its own scale
 ])
 @pytest.mark.parametrize("yd", [0, 1])
 def test_grouped_requant_per_matrix(T, M, K, Ns, yd):
@@ -118,7 +124,7 @@ def test_grouped_prescaled_equals_single_calls(T):
     order of the fp32 block sums, not the result beyond rounding.)"""
     import quantized_gemv_tq2_gb300 as tq2
     K, Ns = 4096, (4096, 256, 256)
-    for M in (3, 4, 8):
+    for M in (3, 4, 8, 9, 12, 16):
         xh = syn.activations(M, M, K)
         x = dev(xh)
         mh = _mats(M, Ns, K)
@@ -193,3 +199,70 @@ def test_grouped_zero_rows_and_graph(T):
     for j, (qs, d) in ((0, mats[0]), (2, mats[1])):
         y_ref, tol = oracle.matvec(host(x), qs, d, 512)
         assert_within_tolerance(host(ys[j]).astype(np.float64), y_ref, tol, f"zero-row group {j}")
+
+
+@pytest.mark.parametrize("M,K,Ns", [
+    (13, 4096, (2048, 1024)),         # consecutive calls (the GEMM each)
+    (16, 4096, (1000, 3000)),
+    (12, 8448, (600, 70, 70)),        # GEMM for q, k and v
+    (8, 8448, (640, 300)),            # M = 8: a matrix takes the GEMM given the pass
+])
+@pytest.mark.parametrize("requant", [False, True])
+def test_grouped_one_prologue_pass(T, M, K, Ns, requant):
+    """With the prologue and a workspace, a group run as consecutive calls
+    converts x once: the workspace then holds the oracle's codes, and each
+    matrix's y is the same bits as its single call (with a workspace of its
+    own) and as the group without a workspace where that runs the same
+    kernel; all within the oracle's tolerance."""
+    import quantized_gemv_tq2_gb300 as tq2
+    seed = 90 + M + K + len(Ns)
+    xh = syn.activations(seed, M, K, heavy=True)
+    s = float(syn.act_scale(seed))
+    mh = _mats(seed, Ns, K)
+    x = dev(xh)
+    mats = [(dev(q), dev(d)) for q, d in mh]
+    scales = [0.21 * (j + 1) for j in range(len(Ns))] if requant else None
+    wsz = tq2.load().tq2_matvec_grouped_workspace_size(
+        M, K, len(Ns), ctypes.cast((ctypes.c_int64 * len(Ns))(*Ns), ctypes.c_void_p))
+    assert wsz == 2 * M * K
+    ws = T.full((wsz + 256,), 0x5A, dtype=T.uint8, device="cuda")
+    st = T.zeros(1, dtype=T.int32, device="cuda")
+    ys = tq2.matvec_grouped(x, [q for q, _ in mats], [d for _, d in mats], act_scale=s, status=st,
+                            out_scales=scales, workspace=ws)
+    singles = [tq2.matvec(x, q, d, act_scale=s, out_scale=(scales[j] if scales else 0.0),
+                          workspace=T.empty(2 * M * K, dtype=T.uint8, device="cuda"))
+               for j, (q, d) in enumerate(mats)]
+    T.cuda.synchronize()
+    assert int(st.item()) == 0
+    codes = host(ws[:2 * M * K].view(T.float16)).astype(np.float64).reshape(M, K)
+    assert np.array_equal(codes, oracle.fakequant_codes(xh, s, mode=0).astype(np.float64))
+    assert np.all(host(ws[2 * M * K:]) == 0x5A)
+    for j, ((qh, dh), y, y1) in enumerate(zip(mh, ys, singles)):
+        what = f"M={M} K={K} matrix {j} N={Ns[j]} requant={requant}"
+        assert np.array_equal(host(y).view(np.int32), host(y1).view(np.int32)), what
+        rows = sample_rows(Ns[j], 96, seed=j) if Ns[j] > 2048 else np.arange(Ns[j])
+        y_ref, tol = oracle.matvec_rows(xh, qh, dh, K, rows, act_scale=s)
+        if requant:
+            check_requant(host(y)[:, rows], y_ref, tol, scales[j], 0, what)
+        else:
+            assert_within_tolerance(host(y)[:, rows].astype(np.float64), y_ref, tol, what)
+    if M >= 9:  # without a workspace the same kernels run, each converting x itself
+        ys0 = tq2.matvec_grouped(x, [q for q, _ in mats], [d for _, d in mats], act_scale=s,
+                                 out_scales=scales, workspace=None)
+        T.cuda.synchronize()
+        for j, (y, y0) in enumerate(zip(ys, ys0)):
+            assert np.array_equal(host(y).view(np.int32), host(y0).view(np.int32)), f"no workspace, matrix {j}"
+
+
+def test_grouped_workspace_too_small(T):
+    import quantized_gemv_tq2_gb300 as tq2
+    M, K, Ns = 12, 4096, (600, 700)
+    mats = [(dev(q), dev(d)) for q, d in _mats(5, Ns, K)]
+    x = dev(syn.activations(5, M, K))
+    ys = [T.full((M, N), 3.0, device="cuda") for N in Ns]
+    with pytest.raises(tq2.TQ2Error) as e:
+        tq2.matvec_grouped(x, [q for q, _ in mats], [d for _, d in mats], y_list=ys, act_scale=0.05,
+                           workspace=T.empty(2 * M * K - 16, dtype=T.uint8, device="cuda"))
+    assert e.value.status == 5
+    T.cuda.synchronize()
+    assert all(np.all(host(y) == 3.0) for y in ys)  # nothing was enqueued
