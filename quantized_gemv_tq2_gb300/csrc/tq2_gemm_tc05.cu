@@ -64,18 +64,57 @@ using namespace dev;
 
 constexpr int kWProducerWarp = 0;
 constexpr int kBProducerWarp = 1;
-constexpr int kMmaWarp = 2;
+constexpr int kMmaWarp = 2;               // tensor memory, MMA issue (even k-steps)
 constexpr int kFirstUnpackWarp = 3;
 constexpr int kUnpackWarps = 8;
-constexpr int kThreads = (kFirstUnpackWarp + kUnpackWarps) * 32;  // 352
-constexpr int kTmemThreads = (kUnpackWarps + 1) * 32;            // MMA warp + unpack warps
+constexpr int kMmaWarp2 = kFirstUnpackWarp + kUnpackWarps;  // MMA issue (odd k-steps), 11, if two issuers
 constexpr int kRows = 128;               // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kKs = 8;                   // k-steps (16 codes) per stage: one A slot, two x boxes
 constexpr int kWStageBytes = 8192;       // 128 rows x 64 bytes of codes (16 k-steps, one 256-block)
-constexpr int kASlots = 4;               // TMEM A ring
+constexpr int kASlots = 4;               // TMEM A ring, at most
 constexpr int kAColsPerSlot = 64;        // 8 k-steps x 8 columns
-constexpr int kDCol = 256;               // D (fp32, BN columns) starts here
-constexpr int kTmemCols = 512;
+
+// MMA issue: one thread issues a tcgen05.mma about every 126 cycles on this
+// part, whatever the operands' source or the accumulator (measured), while
+// a 128 x BN x 16 MMA takes the tensor cores ~BN / 1.7 cycles: one issuing
+// thread bounds every tile narrower than ~200 columns.  So two warps issue:
+// warp kMmaWarp the even k-steps of each stage, warp kMmaWarp2 the odd ones,
+// each into its own accumulator tile (tcgen05 MMAs of different threads are
+// not ordered with one another), and the epilogue sums the two tiles in tile
+// order.  A 256-column tile has room for one accumulator and a long enough
+// MMA: one issuer.
+//
+// Tensor memory per CTA.  A tile of up to 64 activation rows takes half of
+// the SM's 512 columns -- the accumulators first, then the A slots -- so
+// that two CTAs fit on an SM (the next call's CTA starts beside the current
+// one and streams its weights early); wider tiles take all 512 (four A
+// slots at 0..255, the accumulators from 256), one CTA per SM.  The host
+// sizes shared memory so that no more CTAs than that fit on an SM
+// (tcgen05.alloc would otherwise wait for columns that a CTA of another
+// cluster holds).  The epilogue's 32-column loads of a narrow tile run on
+// into later columns, inside the allocation, which no MMA writes by then
+// (masked).
+template <int BN>
+struct Tmem {
+    static constexpr int issuers = BN <= 128 ? 2 : 1;
+    static constexpr int threads = (kMmaWarp2 + issuers - 1) * 32;           // 384 or 352
+    static constexpr int tmem_threads = (kUnpackWarps + issuers) * 32;       // MMA warps + unpack warps
+    static constexpr int nd = issuers;                      // accumulator tiles
+    static constexpr int cols = BN <= 64 ? 256 : 512;
+    static constexpr int dcol = BN <= 64 ? 0 : 256;         // accumulator tile 0
+    static constexpr int acol = BN <= 32 ? 64 : BN <= 64 ? 128 : 0;  // A slot 0
+    static constexpr int slots = BN <= 64 ? (cols - acol) / 64 : 4;
+    static_assert(dcol + (nd - 1) * BN + (BN < 64 ? BN / 2 + 32 : BN) <= cols, "epilogue loads past the columns");
+    static_assert(BN <= 64 ? nd * BN <= acol : acol + slots * 64 <= dcol, "A slots overlap the accumulators");
+    static_assert(acol + slots * 64 <= cols && dcol + nd * BN <= cols, "past the columns");
+    static_assert(slots >= 2 && slots <= 4, "A ring depth");
+};
+
+int tmem_slots(int BN)
+{
+    return BN <= 16 ? Tmem<16>::slots : BN <= 32 ? Tmem<32>::slots : BN <= 64 ? Tmem<64>::slots
+         : BN <= 128 ? Tmem<128>::slots : Tmem<256>::slots;
+}
 constexpr int kMaxStages = 8;
 
 struct GemmParams {
@@ -114,7 +153,7 @@ __device__ __forceinline__ void expand_word(uint32_t w, __half2 dd, uint32_t *o)
 
 // ------------------------------------------------------------------ kernel
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_constant__ GemmParams p)
+__global__ void __launch_bounds__(Tmem<BN>::threads, 1) gemm_tc05_kernel(const __grid_constant__ GemmParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint32_t tmem_base_sh;
@@ -170,9 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             mbar_init(bfull0 + 8u * i, 1);
             mbar_init(bconv0 + 8u * i, kUnpackWarps / 2);  // the half that expands the stage converts it
             mbar_init(afull0 + 8u * i, 4);
-            mbar_init(sempty0 + 8u * i, 1);
+            mbar_init(sempty0 + 8u * i, Tmem<BN>::issuers);  // one commit per issuer
         }
-        mbar_init(dfull, 1);
+        mbar_init(dfull, Tmem<BN>::issuers);
         if (S > 1) {
             mbar_init(pready, (uint32_t)(S - 1));
             mbar_init(pdone, (uint32_t)(S - 1));
@@ -249,18 +288,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
         return;
     }
 
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp || warp == kMmaWarp2) {
         // -------------------------------------------------- TMEM + MMA issue
+        const int w = (warp == kMmaWarp) ? 0 : 1;  // this issuer's k-steps: i % issuers == w
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr(&tmem_base_sh)),
-                     "n"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        if (w == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_addr(&tmem_base_sh)),
+                         "n"(Tmem<BN>::cols));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        }
         tc_fence_before();
-        named_barrier(1, kTmemThreads);  // (a) TMEM address published
+        named_barrier(1, Tmem<BN>::tmem_threads);  // (a) TMEM address published
         tc_fence_after();
         const uint32_t tbase = tmem_base_sh;
-        if (lane == 0) {
+        if (lane == 0 && w < Tmem<BN>::issuers) {
             const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((128u >> 4) << 24);
             // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart (the
             // leading offset is unused in this mode), layout type 2
@@ -275,12 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const uint32_t b0 = bring + (uint32_t)r * kBStageBytes;
+                constexpr int ni = Tmem<BN>::issuers;
 #pragma unroll
-                for (int i = 0; i < kKs; ++i) {
+                for (int i0 = 0; i0 < kKs; i0 += ni) {
+                    const int i = i0 + w;
                     const uint32_t baddr = b0 + (uint32_t)(i >> 2) * kBoxBytes + (uint32_t)(32 * (i & 3));
                     const uint64_t desc = desc_hi | (uint64_t)((baddr & 0x3FFFFu) >> 4);
-                    umma_f16(tbase + kDCol, tbase + (uint32_t)(r * kAColsPerSlot + 8 * i), desc, idesc,
-                             (uint32_t)(g != 0 || i != 0));
+                    umma_f16(tbase + (uint32_t)(Tmem<BN>::dcol + w * BN),
+                             tbase + (uint32_t)(Tmem<BN>::acol + r * kAColsPerSlot + 8 * i), desc, idesc,
+                             (uint32_t)(g != 0 || i0 != 0));  // this issuer's first k-step overwrites its tile
                 }
                 umma_commit(sempty0 + 8u * r);  // A slot and x buffer free once these MMAs completed
             }
@@ -290,9 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             if (!mbar_wait(dfull, 0u)) report_timeout(p, abort_flag);
         }
         __syncwarp();
-        named_barrier(2, kTmemThreads);  // (b) the epilogue has read D
+        named_barrier(2, Tmem<BN>::tmem_threads);  // (b) the epilogue has read D
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(kTmemCols));
+        if (w == 0)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(Tmem<BN>::cols));
         return;
     }
 
@@ -311,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             dsm[b * kRows + r] = (n0 + r < N) ? p.a.d[(n0 + r) * (int64_t)B + b] : (uint16_t)0;
     }
     named_barrier(3, kUnpackWarps * 32);  // d staged
-    named_barrier(1, kTmemThreads);       // (a)
+    named_barrier(1, Tmem<BN>::tmem_threads);       // (a)
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
     const uint32_t tlane = tbase + ((uint32_t)(q * 32) << 16);
@@ -383,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
                 uint32_t v[32];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) expand_word(wd[4 * h2 + i], dd, &v[8 * i]);
-                if (alive && TQ2_IN(a * kAColsPerSlot + 32 * h2 + 32 <= kDCol, st_w))
-                    tmem_st32(tlane + (uint32_t)(a * kAColsPerSlot + 32 * h2), v);
+                if (alive && TQ2_IN(a < Tmem<BN>::slots, st_w))
+                    tmem_st32(tlane + (uint32_t)(Tmem<BN>::acol + a * kAColsPerSlot + 32 * h2), v);
             }
             if (alive) {
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -414,23 +460,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
             reinterpret_cast<float *>(p.a.y)[o] = v;
     };
     // each half of the warps reads BN / 2 columns, 32 at a time (the load of
-    // a narrow tile's last chunk runs past BN into unused columns: masked)
+    // a narrow tile's last chunk runs past BN into unused columns: masked),
+    // summed over the accumulator tiles in tile order
     const int c_beg = half * (BN / 2), c_end = c_beg + BN / 2;
+    auto load_d = [&](int c0, float *v) {
+        uint32_t r[32];
+        tmem_ld32(tlane + (uint32_t)(Tmem<BN>::dcol + c0), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+#pragma unroll 1
+        for (int t = 1; t < Tmem<BN>::nd; ++t) {
+            tmem_ld32(tlane + (uint32_t)(Tmem<BN>::dcol + t * BN + c0), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(r[j]);
+        }
+    };
     if (S == 1) {
         const bool store = (*abort_flag == 0) && n < N;
 #pragma unroll 1
         for (int c0 = c_beg; c0 < c_end; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
-            tmem_ld_wait();
+            float v[32];
+            load_d(c0, v);
             if (store) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (c0 + j < c_end && m0 + c0 + j < M) store_y(m0 + c0 + j, n, __uint_as_float(r[j]));
+                    if (c0 + j < c_end && m0 + c0 + j < M) store_y(m0 + c0 + j, n, v[j]);
             }
         }
         tc_fence_before();
-        named_barrier(2, kTmemThreads);  // (b)
+        named_barrier(2, Tmem<BN>::tmem_threads);  // (b)
         return;
     }
 
@@ -439,16 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
     float *part = reinterpret_cast<float *>(smem + p.off_b);
 #pragma unroll 1
     for (int c0 = c_beg; c0 < c_end; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tlane + (uint32_t)(kDCol + c0), r);
-        tmem_ld_wait();
+        float v[32];
+        load_d(c0, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (c0 + j < c_end && TQ2_IN(smem_addr(&part[(c0 + j) * kRows + row]) + 4u <= win.hi, st_w))
-                part[(c0 + j) * kRows + row] = __uint_as_float(r[j]);
+                part[(c0 + j) * kRows + row] = v[j];
     }
     tc_fence_before();
-    named_barrier(2, kTmemThreads);       // (b): TMEM read, the MMA warp may free it
+    named_barrier(2, Tmem<BN>::tmem_threads);       // (b): TMEM read, the MMA warp may free it
     named_barrier(3, kUnpackWarps * 32);  // every partial of this CTA written
     const uint32_t part_s = smem_addr(part);
     if (uw == 0 && lane < S && lane != rank) {  // tell every peer: my partial is ready
@@ -505,7 +564,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc05_kernel(const __grid_con
 // ------------------------------------------------------------------ host side
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-bool make_plan(int BN, int S, int64_t M, int64_t N, int64_t K, int max_dyn, GemmParams &p)
+// CTAs of a tile width that may share an SM (their tensor memory: Tmem<BN>).
+int ctas_per_sm(int BN) { return BN <= 64 ? 2 : 1; }
+
+// The least dynamic shared memory with which no more than ctas_per_sm(BN)
+// CTAs fit on an SM (static shared memory and the per-CTA reservation only
+// add to it).
+int min_dyn_smem(int BN, int device)
+{
+    static std::atomic<int> smem_per_sm[64];
+    int v = (device >= 0 && device < 64) ? smem_per_sm[device].load() : 0;
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess ||
+            v <= 0) {
+            cudaGetLastError();
+            v = 233472;  // sm_100 / sm_103: 228 KB
+        }
+        if (device >= 0 && device < 64) smem_per_sm[device].store(v);
+    }
+    return v / (ctas_per_sm(BN) + 1) + 1;
+}
+
+bool make_plan(int BN, int S, int64_t M, int64_t N, int64_t K, int max_dyn, int min_dyn, GemmParams &p)
 {
     if (M < 1 || N < 1 || K < 256 || K % 256 != 0 || M > (int64_t)1 << 30) return false;
     if (K > (int64_t)1 << 24) return false;  // d slice and k-step counts stay small
@@ -527,7 +607,8 @@ bool make_plan(int BN, int S, int64_t M, int64_t N, int64_t K, int max_dyn, Gemm
     off = align_up(off, 1024);
     p.off_b = off;
     int sb = (max_dyn - off - 1024 - 2 * kWStageBytes) / bstage;
-    if (sb > kASlots) sb = kASlots;  // one TMEM A slot per stage
+    const int slots = tmem_slots(BN);
+    if (sb > slots) sb = slots;  // one TMEM A slot per stage
     if (sb < 2) return false;
     p.sb = sb;
     off += sb * bstage;
@@ -537,6 +618,7 @@ bool make_plan(int BN, int S, int64_t M, int64_t N, int64_t K, int max_dyn, Gemm
     if (sw < 2) return false;
     p.sw = sw;
     p.smem_total = off + sw * kWStageBytes + 1024;
+    if (p.smem_total < min_dyn) p.smem_total = min_dyn;  // at most ctas_per_sm(BN) CTAs per SM
     return p.smem_total <= max_dyn;
 }
 
@@ -580,13 +662,16 @@ int pick_bn(int64_t M, int64_t N, int device)
 }
 
 // Split of K (cluster size): the largest power of two up to 8 with which the
-// tiles still fit on the SMs at once, and at least one 256-block per CTA.
+// tiles still fit on the SMs at once, one CTA each (a second CTA on an SM
+// shares its tensor cores: splitting further measured slower), and at least
+// one 256-block per CTA.
 int pick_split(int BN, int64_t M, int64_t N, int64_t K, int device)
 {
+    (void)BN;
     const int64_t tiles = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
-    const int64_t nsm = sm_count(device);
+    const int64_t slots = sm_count(device);
     int S = 1;
-    while (S < 8 && tiles * (2 * S) <= nsm && 2 * S <= K / 256) S *= 2;
+    while (S < 8 && tiles * (2 * S) <= slots && 2 * S <= K / 256) S *= 2;
     return S;
 }
 
@@ -596,7 +681,8 @@ cudaError_t launch_gemm(const MatvecArgs &a, int device)
     GemmParams p{};
     p.a = a;
     const int S = pick_split(BN, a.M, a.N, a.K, device);
-    if (!make_plan(BN, S, a.M, a.N, a.K, gemm_max_dyn<BN>(device), p)) return cudaErrorInvalidConfiguration;
+    if (!make_plan(BN, S, a.M, a.N, a.K, gemm_max_dyn<BN>(device), min_dyn_smem(BN, device), p))
+        return cudaErrorInvalidConfiguration;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     {
@@ -622,7 +708,7 @@ cudaError_t launch_gemm(const MatvecArgs &a, int device)
     const int64_t G = (int64_t)p.n_tiles * ((a.M + BN - 1) / BN) * S;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Tmem<BN>::threads);
     cfg.dynamicSmemBytes = (size_t)p.smem_total;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[2];
@@ -646,7 +732,7 @@ bool gemm_tc05_supported(int64_t M, int64_t N, int64_t K, int device)
     const int dyn = bn == 16 ? gemm_max_dyn<16>(device) : bn == 32 ? gemm_max_dyn<32>(device)
                   : bn == 64 ? gemm_max_dyn<64>(device) : bn == 128 ? gemm_max_dyn<128>(device)
                   : gemm_max_dyn<256>(device);
-    return dyn > 0 && make_plan(bn, pick_split(bn, M, N, K, device), M, N, K, dyn, p);
+    return dyn > 0 && make_plan(bn, pick_split(bn, M, N, K, device), M, N, K, dyn, min_dyn_smem(bn, device), p);
 }
 
 cudaError_t launch_gemm_tc05(const MatvecArgs &a, int device)

@@ -88,11 +88,14 @@ def test_stall_argument_checks(T):
 
 
 # The tcgen05 GEMM: (M, N, K, stall stages) with the CTA's x stages counted
-# within its share of K -- one CTA per 128-row tile and all of K (8 stages),
-# split K over clusters of 8 CTAs (the partial-sum hand-off; 4 stages each),
-# and two activation tiles over clusters of 4 (2 stages each).
+# within its share of K -- one CTA per 128-row tile and all of K (160 tiles:
+# more than two CTAs per SM hold, so no split; 8 stages), K split over CTA
+# pairs (two CTAs per SM for a 16-row activation tile; 4 stages each), split
+# K over clusters of 8 CTAs (the partial-sum hand-off; 4 stages each), and
+# two activation tiles over clusters of 4 (2 stages each).
 @pytest.mark.parametrize("M,N,K,stages", [
-    (16, 16384, 1024, (0, 1, 7)),
+    (16, 20480, 1024, (0, 1, 7)),
+    (16, 16384, 1024, (0, 1, 3)),
     (16, 512, 4096, (0, 1, 3)),
     (200, 2048, 1024, (0, 1)),
 ])
