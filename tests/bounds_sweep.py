@@ -128,7 +128,8 @@ def affine4():
 def gemm():
     n_calls = 0
     cases = [(17, 128, 256), (64, 100, 512), (130, 257, 768), (300, 300, 1024), (16, 512, 4096),
-             (16, 16384, 1024), (200, 2048, 1024), (2048, 256, 4096), (512, 4096, 4096)]
+             (16, 16384, 1024), (200, 2048, 1024), (2048, 256, 4096), (512, 4096, 4096),
+             (64, 256, 4096), (32, 512, 2048), (9, 20480, 1024)]
     for M, N, K in cases:
         # prologue in every tile (no workspace), or as a pass of its own where it pays
         for prologue, ws in ((False, None), (True, None), (True, "auto")):

@@ -43,6 +43,9 @@ def _gemm(T, case, impl, y_dtype=0, out_scale=0.0, workspace="auto"):
     (300, 300, 1024),
     (256, 128, 4096),
     (512, 96, 2048),
+    (64, 256, 4096),    # 64-column tile (two A slots, two accumulators), K split over 8-CTA clusters
+    (32, 512, 2048),    # 32-column tile, K split over 8 (one 256-block per CTA)
+    (9, 640, 8448),     # 16-column tile, two accumulators, split K, K not a multiple of 512
 ])
 def test_gemm_small_shapes(T, M, N, K):
     case = Case(seed=M + 3 * N + K, M=M, N=N, K=K)
