@@ -23,22 +23,27 @@
 //     swizzle, which is the K-major SWIZZLE_128B operand layout the MMA reads
 //     (8-row groups 1024 bytes apart; k-step j of a box starts 32 j bytes
 //     into the row); rows past M read as 0;
-//   * warp 2 allocates the 512 TMEM columns (after the wait, so the previous
-//     kernel's tensor memory is free) and one lane issues the MMAs, 8 per
-//     stage, then releases the stage's A slot and x buffer with one commit
-//     (a commit stalls the issuing thread for hundreds of cycles on this
-//     part, so there is one per 8 MMAs);
+//   * warp 2 allocates the TMEM columns (after the wait, so the previous
+//     kernel's tensor memory is free: 256 for tiles of up to 64 columns, so
+//     that two CTAs share an SM, else 512); one lane issues the MMAs of a
+//     stage and releases its A slot and x buffer with one commit (a commit
+//     stalls the issuing thread for hundreds of cycles on this part, so
+//     there is one per stage).  For tiles of up to 128 columns a lane of
+//     warp 11 issues every other k-step into a second accumulator (one
+//     thread issues an MMA only every ~126 cycles), and the epilogue sums
+//     the two;
 //   * warps 3..10 (two per TMEM lane quadrant) stage d, then expand 8 k-steps
 //     at a time: for code pair (2j, 2j+1) of a 16-code word, the fp16 pair
 //     (1024 + q) - 1025 = q - 1 (exact) times d_b, written with tcgen05.st
 //     into a ring of 64-column TMEM slots (one per stage); with the int8
-//     prologue they also fake-quantise each x stage in shared memory first
+//     prologue and no workspace (given one, x arrives as codes from the
+//     conversion pass) they also fake-quantise each x stage in shared memory first
 //     (element-wise, by the half of the warps that expands the stage, a
 //     quarter each, so the halves stay independent) and release it to the MMA
 //     issuer (a generic-to-async proxy fence, then an mbarrier); at the end
 //     they read D (one
-//     column per activation row) and store y, with the optional int8
-//     requantisation at store.
+//     column per activation row; the accumulators summed) and store y, with
+//     the optional int8 requantisation at store.
 // Split K: when the tiles alone would leave SMs idle, a thread-block cluster
 // of S CTAs shares a tile, CTA r taking 256-blocks [r B / S, (r+1) B / S).
 // Each writes its fp32 partial tile to its own shared memory; CTA r then sums
