@@ -311,6 +311,56 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         }
     }
 
+    const int g = lane >> 2, t = lane & 3;
+    const int gg = g % (4 * kM);          // x-fragment column this thread supplies
+    const int mcol = (kM == 2) ? (t >> 1) : 0;  // activation row of columns 2t, 2t+1
+    // per-thread shared-memory byte offsets, hoisted out of the loops
+    const uint32_t a_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
+    const uint32_t a_half = (uint32_t)(8 * p.rb);             // row g -> row g + 8
+    const uint32_t x_thr = smem_addr(xs) + (uint32_t)(gg * 64 + t * 16);
+    const uint32_t x_blk = 512u * kM;                          // per 256-block
+    const uint32_t x_half = 256u * kM;                         // words 0,1 -> 2,3
+    const uint32_t d_thr = smem_addr(dsm) + (uint32_t)(g * p.dstr) * 4u;
+    const uint32_t d_half = (uint32_t)(8 * p.dstr) * 4u;
+    const uint32_t xs_thr = smem_addr(xsum) + (uint32_t)mcol * 4u;
+    const uint32_t rg_stride_d = (uint32_t)(16 * p.dstr) * 4u;
+
+    // K = 4096 fast path (below): this warp's codes and scales of a stage
+    // in registers.  Stage 0's codes are read before the wait on the
+    // previous kernel -- the weights never depend on it, and the warps would
+    // only idle there -- so that the first MMAs issue as soon as x is staged.
+    const bool fast = p.n_kc == 1 && p.rg_s == 1 && p.nbk_full == kUpw * kConsumerWarps;
+    const uint32_t a_warp = a_thr + (uint32_t)(warp * 64);
+    const uint32_t d_warp = d_thr + (uint32_t)(warp * 4);
+    uint32_t W0[kUpw][4], W1[kUpw][4];
+    float dg[kUpw], dg8[kUpw];
+    auto load_codes = [&](int sl) {
+#pragma unroll
+        for (int u = 0; u < kUpw; ++u) {
+            const uint32_t pa = a_warp + (uint32_t)(sl * p.stage_bytes + u * kConsumerWarps * 64);
+            const uint4 wa = lds128_c(win, pa), wb = lds128_c(win, pa + a_half);
+            W0[u][0] = wa.x; W0[u][1] = wa.y; W0[u][2] = wa.z; W0[u][3] = wa.w;
+            W1[u][0] = wb.x; W1[u][1] = wb.y; W1[u][2] = wb.z; W1[u][3] = wb.w;
+        }
+    };
+    auto load_scales = [&](int rg) {
+#pragma unroll
+        for (int u = 0; u < kUpw; ++u) {
+            const uint32_t pd = d_warp + (uint32_t)rg * rg_stride_d + (uint32_t)(u * kConsumerWarps * 4);
+            dg[u] = lds_f32_c(win, pd);
+            dg8[u] = lds_f32_c(win, pd + d_half);
+        }
+    };
+    bool fast_ok = false;
+    if (fast) {
+        fast_ok = n_stages > 0;
+        if (fast_ok && !__all_sync(0xffffffffu, mbar_wait_for(smem_addr(&bars[0]), 0u, lim))) {
+            if (lane == 0) report_timeout(p, abort_flag);
+            fast_ok = false;
+        }
+        if (fast_ok) load_codes(0);
+    }
+
     // x depends on the previous kernel in the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) TQ2_STAMP(p.seq, 1);
@@ -475,9 +525,6 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
     consumer_barrier();
     if (tid == 0) TQ2_STAMP(p.seq, 2);
 
-    const int g = lane >> 2, t = lane & 3;
-    const int gg = g % (4 * kM);          // x-fragment column this thread supplies
-    const int mcol = (kM == 2) ? (t >> 1) : 0;  // activation row of columns 2t, 2t+1
     float acc[4][2];
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = 0.0f;
@@ -500,18 +547,7 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         }
     };
 
-    // per-thread shared-memory byte offsets, hoisted out of the loops
-    const uint32_t a_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
-    const uint32_t a_half = (uint32_t)(8 * p.rb);             // row g -> row g + 8
-    const uint32_t x_thr = smem_addr(xs) + (uint32_t)(gg * 64 + t * 16);
-    const uint32_t x_blk = 512u * kM;                          // per 256-block
-    const uint32_t x_half = 256u * kM;                         // words 0,1 -> 2,3
-    const uint32_t d_thr = smem_addr(dsm) + (uint32_t)(g * p.dstr) * 4u;
-    const uint32_t d_half = (uint32_t)(8 * p.dstr) * 4u;
-    const uint32_t xs_thr = smem_addr(xsum) + (uint32_t)mcol * 4u;
-    const uint32_t rg_stride_d = (uint32_t)(16 * p.dstr) * 4u;
-
-    if (p.n_kc == 1 && p.rg_s == 1 && p.nbk_full == kUpw * kConsumerWarps) {
+    if (fast) {
         // K = 4096: every stage is one 16-row group, all 16 blocks.  This
         // warp takes blocks warp + u * kConsumerWarps of every stage, so their
         // x sums stay in registers.  The next stage's codes are read as soon
@@ -522,37 +558,9 @@ matvec_mma_kernel(const __grid_constant__ MmaParams<kG, kT> p)
         for (int u = 0; u < kUpw; ++u)
             xi[u] = -lds_f32_c(win, xs_thr + (uint32_t)(warp + u * kConsumerWarps) * (4u * kM)) * 5.9604644775390625e-08f;
         const uint32_t x_warp = x_thr + (uint32_t)warp * x_blk;
-        const uint32_t a_warp = a_thr + (uint32_t)(warp * 64);
-        const uint32_t d_warp = d_thr + (uint32_t)(warp * 4);
-        uint32_t W0[kUpw][4], W1[kUpw][4];
-        float dg[kUpw], dg8[kUpw];
-        auto load_codes = [&](int sl) {
-#pragma unroll
-            for (int u = 0; u < kUpw; ++u) {
-                const uint32_t pa = a_warp + (uint32_t)(sl * p.stage_bytes + u * kConsumerWarps * 64);
-                const uint4 wa = lds128_c(win, pa), wb = lds128_c(win, pa + a_half);
-                W0[u][0] = wa.x; W0[u][1] = wa.y; W0[u][2] = wa.z; W0[u][3] = wa.w;
-                W1[u][0] = wb.x; W1[u][1] = wb.y; W1[u][2] = wb.z; W1[u][3] = wb.w;
-            }
-        };
-        auto load_scales = [&](int rg) {
-#pragma unroll
-            for (int u = 0; u < kUpw; ++u) {
-                const uint32_t pd = d_warp + (uint32_t)rg * rg_stride_d + (uint32_t)(u * kConsumerWarps * 4);
-                dg[u] = lds_f32_c(win, pd);
-                dg8[u] = lds_f32_c(win, pd + d_half);
-            }
-        };
         int sl = 0, ph = 0;
-        bool ok = n_stages > 0;
-        if (ok && !__all_sync(0xffffffffu, mbar_wait_for(smem_addr(&bars[0]), 0u, lim))) {
-            if (lane == 0) report_timeout(p, abort_flag);
-            ok = false;
-        }
-        if (ok) {
-            load_codes(0);
-            load_scales(0);
-        }
+        bool ok = fast_ok;  // stage 0's codes are in registers already
+        if (ok) load_scales(0);
         if (tid == 0) TQ2_STAMP(p.seq, 3);
         for (int s = 0; ok && s < n_stages; ++s) {
             // unit by unit: four class accumulators starting at zero, then
