@@ -86,7 +86,8 @@ def layer_shapes():
 
 def grouped():
     for M, K, Ns in ((1, 4096, (4096, 256, 256)), (2, 8448, (70, 50)), (4, 4096, (4096, 256, 256)),
-                     (8, 4096, (1000, 3000)), (5, 8448, (100, 60))):
+                     (8, 4096, (1000, 3000)), (5, 8448, (100, 60)),
+                     (12, 4096, (4096, 256, 256)), (10, 4096, (1000, 3000)), (16, 2048, (300, 70, 45))):
         mats = []
         for j, N in enumerate(Ns):
             qs_h, _ = oracle.pack(syn.codes(11, N, K, linear=j))

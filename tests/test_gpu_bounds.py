@@ -1,7 +1,9 @@
 """The bounds-checked debug build (TQ2_BOUNDS_CHECK): in a child process
 that loads it, a sweep over tiny shapes (K in {256, 512, 768}, every N in
 1..70, every M in 1..16, each kernel that takes the shape), the decoder
-layer shapes at M = 1..16 and grouped calls must report no out-of-buffer
+layer shapes at M = 1..16, grouped calls (one launch up to M = 16, and
+consecutive calls), the affine-int4 kernel and the tcgen05 GEMM (narrow
+tiles over split-K clusters, with and without the prologue pass) must report no out-of-buffer
 index (TQ2_FLAG_BOUNDS clear) and match the oracle (tests/bounds_sweep.py).
 The checks skip a bad access and set a flag; nothing traps."""
 import os
