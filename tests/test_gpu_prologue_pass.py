@@ -95,6 +95,8 @@ def test_pass_codes_are_the_oracles(T):
     (9, 700, 1024, 1, "gemm"),      # N > 512: ragged weight tile
     (17, 513, 768, 1, "gemm"),      # one row past 4 weight tiles, ragged activation tile
     (65, 100, 512, 1, "gemm"),      # M > 64: the pass pays even on one weight tile
+    (20, 600, 256, 1, "gemm"),      # K = 256: one block, split K impossible
+    (70, 16, 1024, 0, "gemm"),      # M > 64 on a 16-row matrix: 128-column tile, two MMA issuers
     (130, 257, 2048, 1, "gemm"),
     (300, 96, 4096, 0, "gemm"),
     (40, 1000, 8448, 1, "gemm"),    # K not a multiple of 512, split K
