@@ -423,13 +423,49 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
         }
     }
 
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t ring_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
+    const uint32_t a_half = (uint32_t)(8 * p.rb);
+    // K = 4096 fast path (below): with one n-tile (M <= 8) stage 0's codes
+    // are read before the wait on the previous kernel (the weights never
+    // depend on it, and the consumer warps would only idle there), and its
+    // slot released: M = 3..8 2-4 % faster; with two n-tiles no faster, so
+    // they are read after x there.
+    const bool fast = p.n_kc == 1 && p.R == 1 && p.kcb == 16 && p.xkc == 1;
+    constexpr bool kEarly = NT == 1;
+    constexpr int kU = 16 / kWarps;  // fast path: blocks per warp and stage
+    const uint32_t au0 = ring_thr + (uint32_t)(warp * 64);
+#define au(u) (au0 + (uint32_t)((u) * kWarps * 64))
+    uint32_t W[kU][4], V[kU][4];
+    // a stage's codes to registers; the slot is released once they are read
+#define TQ2_PS_LOAD_CODES(SL)                                                              \
+        do {                                                                               \
+            _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
+                const uint32_t pa_ = au(u_) + (uint32_t)((SL) * p.stage_bytes);           \
+                const uint4 va_ = lds128_c(win, pa_), vb_ = lds128_c(win, pa_ + a_half);                 \
+                W[u_][0] = va_.x; W[u_][1] = va_.y; W[u_][2] = va_.z; W[u_][3] = va_.w;    \
+                V[u_][0] = vb_.x; V[u_][1] = vb_.y; V[u_][2] = vb_.z; V[u_][3] = vb_.w;    \
+            }                                                                              \
+            __syncwarp();                                                                  \
+            if (lane == 0) mbar_arrive(smem_addr(&bars[S + (SL)]));                        \
+        } while (0)
+    bool fast_ok = false;
+    auto fast_first = [&]() {  // stage 0's codes to registers
+        fast_ok = n_stages > 0;
+        if (fast_ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[0]), 0u))) {
+            if (lane == 0) report_timeout(p, abort_flag);
+            fast_ok = false;
+        }
+        if (fast_ok) TQ2_PS_LOAD_CODES(0);
+    };
+    if (kEarly && fast) fast_first();
+
     // x depends on the previous kernel in the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     consumers_sync();  // xinfo zeroed before it is written
     stage_x<NT>(p, 0, min(p.xblocks, B), frag, xinfo, warp, lane);
     consumers_sync();
 
-    const int g = lane >> 2, t = lane & 3;
     uint32_t xo[NT][4];  // this lane's B entry of word jw within a block, per n-tile
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -459,9 +495,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
         }
     };
 
-    const uint32_t ring_thr = smem_addr(ring) + (uint32_t)(g * p.rb + t * 16);
-    const uint32_t a_half = (uint32_t)(8 * p.rb);
-
     // K = 4096 with x resident: every stage is one 16-row group x all 16
     // blocks, and warp w takes blocks w and w + 8 of every stage, so its B
     // fragment bases and per-column block terms stay in registers for the
@@ -469,37 +502,20 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
     // landed and the slot is released at once; the next stage's codes are
     // read once this stage's last MMAs are issued.  Four accumulator chains
     // (one per code class) per block.
-    const bool fast = p.n_kc == 1 && p.R == 1 && p.kcb == 16 && p.xkc == 1;
     if (fast) {
-        constexpr int kU = 16 / kWarps;  // blocks per warp and stage
         // shared-memory bases of block warp + u * kWarps, recomputed from the
         // u = 0 ones at each use (holding all of them spills registers)
         const uint32_t fb0 = frag + (uint32_t)(warp * 512 * M), fb_step = (uint32_t)(kWarps * 512 * M);
-        const uint32_t au0 = ring_thr + (uint32_t)(warp * 64);
         const uint32_t du0 = smem_addr(dsm) + (uint32_t)(g * p.dstr + warp) * 4u;
         const uint32_t xi0 = smem_addr(xinfo) + (uint32_t)(warp * 8 * NT + 2 * t) * 8u;  // + 64 per n-tile
 #define fbu(u) (fb0 + (uint32_t)(u) * fb_step)
-#define au(u) (au0 + (uint32_t)((u) * kWarps * 64))
 #define du(u) (du0 + (uint32_t)((u) * kWarps * 4))
 #define xiu(u) (xi0 + (uint32_t)((u) * kWarps * 8 * NT * 8))
         uint32_t h1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) h1[nt] = (uint32_t)(64 * min(8, M - 8 * nt));
         const uint32_t d_half = (uint32_t)(8 * p.dstr) * 4u, d_rg = (uint32_t)(16 * p.dstr) * 4u;
-        uint32_t W[kU][4], V[kU][4];
         float dg[kU], dg8[kU];
-        // a stage's codes to registers; the slot is released once they are read
-#define TQ2_PS_LOAD_CODES(SL)                                                              \
-        do {                                                                               \
-            _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
-                const uint32_t pa_ = au(u_) + (uint32_t)((SL) * p.stage_bytes);           \
-                const uint4 va_ = lds128_c(win, pa_), vb_ = lds128_c(win, pa_ + a_half);                 \
-                W[u_][0] = va_.x; W[u_][1] = va_.y; W[u_][2] = va_.z; W[u_][3] = va_.w;    \
-                V[u_][0] = vb_.x; V[u_][1] = vb_.y; V[u_][2] = vb_.z; V[u_][3] = vb_.w;    \
-            }                                                                              \
-            __syncwarp();                                                                  \
-            if (lane == 0) mbar_arrive(smem_addr(&bars[S + (SL)]));                        \
-        } while (0)
 #define TQ2_PS_LOAD_SCALES(RG)                                                             \
         do {                                                                               \
             _Pragma("unroll") for (int u_ = 0; u_ < kU; ++u_) {                            \
@@ -508,15 +524,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) matvec_ps_kernel(co
             }                                                                              \
         } while (0)
         int sl = 0, ph = 0;
-        bool ok = n_stages > 0;
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bars[0]), 0u))) {
-            if (lane == 0) report_timeout(p, abort_flag);
-            ok = false;
-        }
-        if (ok) {
-            TQ2_PS_LOAD_CODES(0);
-            TQ2_PS_LOAD_SCALES(0);
-        }
+        if (!kEarly) fast_first();
+        bool ok = fast_ok;  // stage 0's codes are in registers
+        if (ok) TQ2_PS_LOAD_SCALES(0);
         for (int s = 0; ok && s < n_stages; ++s) {
             const int nsl = (sl + 1 == S) ? 0 : sl + 1;
             const int nph = (sl + 1 == S) ? (ph ^ 1) : ph;
