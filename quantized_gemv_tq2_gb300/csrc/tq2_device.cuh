@@ -292,11 +292,14 @@ __device__ __forceinline__ float lds_f32_c(const SmemWindow &w, uint32_t addr)
 
 // Static int8 fake-quant code (gemma4 wNa8o8 page, "Implemented"):
 // rint(x * (1/s)) in fp32, ties to even, clamped to [-128, 127]; NaN -> 0.
+// One conversion does the rounding, the clamp and the NaN case: cvt to s8
+// with round-to-nearest-even and saturation (PTX: a NaN source gives 0).
 __device__ __forceinline__ float fq_code(float x, float inv_s)
 {
-    float t = __fmul_rn(x, inv_s);
-    if (t != t) return 0.0f;
-    return fminf(fmaxf(rintf(t), -128.0f), 127.0f);
+    const float t = __fmul_rn(x, inv_s);
+    int q;
+    asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(q) : "f"(t));
+    return (float)q;
 }
 
 // Output requantisation at store (gemma4 wNa8o8 page, "Implemented": the
