@@ -570,15 +570,16 @@ def cpu_baseline_oracle(budget_s=10.0, stack_host=None):
 
 def read_profile_traffic():
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel sources (sha256 of both kernels of the step match);
-    else None."""
+    on the current kernel sources (sha256 of both kernels of the step and of
+    the device header they include match); else None."""
     import hashlib
     csrc = os.path.join(ROOT, "quantized_gemv_tq2_gb300", "csrc")
     prof = os.path.join(ROOT, "profiles", "tq2_matvec_mma_stack_m1.md")
     try:
         sha = {key: hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest()
                for key, f in (("kernel_source_sha256", "tq2_matvec_mma.cu"),
-                              ("smalln_source_sha256", "tq2_matvec_smalln.cu"))}
+                              ("smalln_source_sha256", "tq2_matvec_smalln.cu"),
+                              ("device_header_sha256", "tq2_device.cuh"))}
         vals = {}
         for line in open(prof):
             if ":" in line and line.strip().startswith("- `"):
