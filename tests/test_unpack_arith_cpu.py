@@ -17,7 +17,10 @@ sources, so a change to them is checked here:
     most 2^-19 of x; the scale-back constants are the powers of two;
   * tcgen05 GEMM expand (tq2_gemm_tc05.cu): OR-ing a code into 0x6400 gives
     fp16 1024 + q, adding -1025 gives q - 1 exactly, and (q - 1) * d is exact
-    for every finite fp16 d.
+    for every finite fp16 d;
+  * affine int4 (tq2_matvec_affine4.cu): the nibble masks give q * 2^-24 and
+    q * 2^-20 exactly, and the class and zero-point combination is the
+    affine group sum.
 """
 import os
 import re
@@ -167,3 +170,40 @@ def test_gemm_expand_is_exact():
         assert float(qm1) == q - 1
         prod = (np.full_like(d, qm1) * d).astype(np.float64)
         assert np.array_equal(prod, (q - 1) * d.astype(np.float64))
+
+
+def test_affine4_nibble_unpack_and_combination():
+    """Affine int4 (tq2_matvec_affine4.cu): w & 0x000F000F leaves q * 2^-24,
+    w & 0x00F000F0 leaves 16 q = q * 2^-20, both exact (subnormal) for every
+    lane; the high-nibble class is brought to units of 2^-24 by 1/16 and the
+    group sum back by 2^24, and s * (sum q x - z * sum x) is the affine
+    group's sum_k s (q_k - z) x_k."""
+    a4 = _src("tq2_matvec_affine4.cu")
+    m = re.search(r"kLo = (0x[0-9A-Fa-f]+)u, kHi = (0x[0-9A-Fa-f]+)u;", a4)
+    comb = re.search(r"\(c\[0\]\[0\] \+ c\[1\]\[1\] \* ([0-9.]+)f\)", a4)
+    back = re.search(r"acc_lo = fmaf\(slo \* ([0-9.]+)f, dlo, acc_lo\);", a4)
+    assert m and comb and back, "the affine-int4 unpack changed: update this check"
+    lo, hi = int(m.group(1), 16), int(m.group(2), 16)
+    assert (lo, hi) == (0x000F000F, 0x00F000F0)
+    inv16, two24 = float(comb.group(1)), float(back.group(1))
+    assert (inv16, two24) == (2.0 ** -4, 2.0 ** 24)
+    lane = ALL16
+    assert np.array_equal(_f16(lane & (lo & 0xFFFF)), (lane & 15) * 2.0 ** -24)
+    assert np.array_equal(_f16(lane & (hi & 0xFFFF)), ((lane >> 4) & 15) * 2.0 ** -20)
+    rng = np.random.default_rng(11)
+    for G in (64, 128, 256):
+        q = rng.integers(0, 16, size=G)
+        x = rng.standard_normal(G).astype(np.float16).astype(np.float64)
+        s = float(np.float16(rng.uniform(0.01, 0.1)))
+        z = float(np.float16(rng.integers(0, 16)))
+        # two codes per byte, code k at bits 4 (k % 2) of byte k / 2; 8 per 32-bit word
+        cls = [0.0] * 4
+        for k in range(G):
+            byte, nib = divmod(k, 2)
+            c = 2 * (byte % 2) + nib  # bytes 0 / 2 of a word: classes 0, 1; bytes 1 / 3 (after >> 8): 2, 3
+            shift = 4 * nib
+            cls[c] += _f16((int(q[k]) << shift) & (lo if nib == 0 else hi) & 0xFFFF) * x[k]
+        dsum = cls[0] + cls[1] * inv16 + cls[2] + cls[3] * inv16
+        y = s * two24 * dsum - s * z * x.sum()
+        want = float(np.sum(s * (q - z) * x))
+        assert abs(y - want) <= 1e-12 * max(1.0, float(np.sum(np.abs(s * (q - z) * x))))
